@@ -1,0 +1,137 @@
+/*
+ * cp_oracle.h -- CPU oracle for the CodePredictor speculative round.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is a plain, slow, single-threaded C
+ * restatement of what the method computes, used to check the CUDA library.
+ * Only the test suite, the smoke check and the benchmark's CPU-baseline leg
+ * load it.  It shares no code, header or table with the CUDA path.
+ *
+ * Sources (page title, section):
+ *  - "CodePredictor Speculative Decoding" (TensorRT-Edge-LLM docs),
+ *    sections "Why the draft is free", "How a round works", "Options".
+ *  - "Speculative Decoding, Beyond Text", sections 02 (exact greedy and
+ *    stochastic algorithms, the sum-min = 1 - TV identity), 03 (one round),
+ *    07 (KV transaction / logit shift).
+ *  - "RVQ Position Aware Speculative Decoding for On Device TTS", section 1
+ *    Figure 1 (inner step k consumes c_{k-1}, emits c_k) and 2.1 (one
+ *    embedding table and one LM head per codebook position).
+ *  - "Awesome-ML-SYS-Tutorial" (Fast AR / MTP sections): the two-position
+ *    prefix [hidden, code-0 embedding], per-frame KV rebuilt each frame.
+ *
+ * Precision: the forward pass runs in float64 on weights given as float32
+ * (bf16 and fp32 storage values are exact in float32); logits are rounded
+ * to float32 and all sampling arithmetic is float32 with the exact orders
+ * documented at each function.  Softmax normalisation is float64 rounded to
+ * float32.
+ *
+ * Parity pins: every function here is checked in tests/ against something
+ * other than itself (published Philox known-answer vectors, brute-force
+ * sorting, a torch float64 restatement with library attention/RMSNorm,
+ * no-cache recomputation, exact greedy AR equality, statistical equality of
+ * the speculative and autoregressive output laws, the sum-min identity).
+ * The absolute acceptance rate on synthetic random weights has no pin
+ * ("parity unpinned"): the pages' 1.70 / 2.47 tokens per step need trained
+ * checkpoints and real audio.
+ */
+#ifndef CP_ORACLE_H
+#define CP_ORACLE_H
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORC_DRAFT = 0, ORC_ACCEPT = 1, ORC_TARGET = 2, ORC_INPUT = 3 };
+
+typedef struct {
+  int H, L, nq, nkv, d, F, V, G;
+  double theta, eps;
+  /* all float32, row-major; layer tensors stacked over layers */
+  const float *embed;      /* [G-1][V][H]  table j is E_j (input for position j+1) */
+  const float *head;       /* [G-1][V][H]  index j-1 is head_j                     */
+  const float *final_norm; /* [H]          */
+  const float *attn_norm;  /* [L][H]       */
+  const float *wq;         /* [L][nq*d][H] */
+  const float *wk;         /* [L][nkv*d][H]*/
+  const float *wv;         /* [L][nkv*d][H]*/
+  const float *wo;         /* [L][H][nq*d] */
+  const float *ffn_norm;   /* [L][H]       */
+  const float *w_gate;     /* [L][F][H]    */
+  const float *w_up;       /* [L][F][H]    */
+  const float *w_down;     /* [L][H][F]    */
+} orc_model;
+
+typedef struct {
+  int64_t frames, passes, rounds, committed, bonus, rejections;
+  int64_t drafted_by_offset[9];  /* index t = 1..8 */
+  int64_t accepted_by_offset[9];
+} orc_stats;
+
+typedef struct {
+  int32_t frame, stream, s, n_d, m, n_acc, s_new, pad;
+  int32_t drafts[8];
+  double min_margin;
+} orc_round_rec;
+
+/* Philox4x32-10 block function (Salmon, Moraes, Dror, Shaw, SC'11). */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+/* u = (word0 >> 8) * 2^-24 of Philox(counter = (stream, frame, depth, purpose),
+ * key = (seed mod 2^32, seed >> 32)). */
+float orc_uniform(uint64_t seed, uint32_t stream, uint32_t frame, uint32_t depth, uint32_t purpose);
+void orc_uniform_fill(uint64_t seed, int n, const uint32_t* ctr4 /*[n][4]*/, float* out);
+
+/* Logit processing: T == 0 -> one-hot argmax (lowest index on ties); else
+ * z = fl32(logit / T), keep exactly min(k, V) entries by (z desc, index asc),
+ * p_i = fl32(exp(z_i - zmax) / S), S = float64 sum over the kept set in
+ * ascending index order.  margin (optional) = decision gap in logit units. */
+void orc_process(const float* logits, int V, int top_k, float T, float* probs, double* margin);
+/* Categorical draw: candidates = {i : w_i > 0} ascending; S_j sequential
+ * float32 prefix sums; t = fl32(u * S_last); first j with S_j > t, else the
+ * last candidate.  Returns -1 if no candidate.  margin = relative distance
+ * of t to the nearest adjacent boundary. */
+int orc_sample(const float* w, int V, float u, double* margin);
+/* Left-to-right exact speculative acceptance over n_d drafts with explicit
+ * uniforms.  q: [n_d][V], p: [m][V] with m in {n_d, n_d + 1}; p row t-1
+ * scores draft t.  Accept draft t iff u_acc[t-1] < fl32(p_t(y)/q_t(y)); on
+ * the first rejection emit a draw from norm(max(0, p_t - q_t)) with
+ * u_tgt[t-1] (from p_t if that residual is all zero) and stop; if all are
+ * accepted and m > n_d emit the bonus drawn from p row n_d with u_tgt[n_d].
+ * Returns the number of accepted drafts. */
+int orc_accept_chain(int V, int n_d, int m, const float* q, const int* drafts, const float* p,
+                     const float* u_acc, const float* u_tgt, int* emitted, int* n_emitted,
+                     double* margin);
+/* Acceptance microbenchmark: R independent rounds of N-1 drafts and N
+ * target rows.  mode 0: inputs are logits (processed with top_k / T);
+ * mode 1: inputs are already-processed float32 probabilities.  Philox
+ * counter (stream = r, frame = 0, depth = t, purpose).  tokens: [R][N],
+ * -1 padded; n_acc: [R]; drafts (optional) [R][N-1]; margins optional [R]. */
+void orc_accept_batch(int R, int N, int V, int top_k, float T, uint64_t seed, int mode,
+                      const float* target, const float* draft, int* tokens, int* n_acc,
+                      int* drafts, double* margins);
+
+size_t orc_kv_doubles(const orc_model* M);
+/* One causal block pass: rows at the given positions are appended to the
+ * KV cache (float64 [L][2][G][nkv][d]) and each row attends to cache
+ * positions 0..pos.  out: final-RMSNorm'ed hidden per row [n][H]. */
+void orc_forward(const orc_model* M, double* kv, int n, const double* in_rows, const int* positions,
+                 double* out_normed);
+/* logits of head_j (1 <= j <= G-1) on a normed hidden, float64 and float32. */
+void orc_head_logits(const orc_model* M, int j, const double* hn, double* out64, float* out32);
+/* Teacher-forced logits over positions 0..P-1 of one frame (rows x,
+ * E_0(c_0), ..., E_{P-2}(c_{P-2})): logits [P-1][V] for head_j at position
+ * j; draft (optional) [P-1][n_draft][V] for head_{j+t} at position j (zero
+ * where j+t > G-1). */
+void orc_teacher_logits(const orc_model* M, const float* x, const int* codes, int P, int n_draft,
+                        float* logits, float* draft);
+/* Decode frames.  N = 0: autoregressive loop; N in 2..8: speculative rounds.
+ * top_k / temp per stream [B].  x [F][B][H], c0 [F][B], codes out [F][B][G]
+ * (codes[...][0] = c0).  Returns 0, or -1 on bad arguments. */
+int orc_decode_frames(const orc_model* M, int N, const int* top_k, const float* temp, uint64_t seed,
+                      int B, int F, int first_frame, const float* x, const int* c0, int* codes,
+                      orc_stats* st, orc_round_rec* log, int log_cap, int* n_log);
+
+#ifdef __cplusplus
+}
+#endif
+#endif
