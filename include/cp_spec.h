@@ -1,0 +1,233 @@
+/*
+ * cp_spec.h -- C ABI of the GB300 CodePredictor speculative-decoding library.
+ *
+ * The library runs the inner RVQ loop of a Qwen3-TTS / Qwen3-Omni style
+ * CodePredictor: per audio frame, given the talker hidden x and the first
+ * code c_0, it emits the residual codes c_1..c_{G-1}, either one decoder pass
+ * per code (autoregressive, verify_window = 0) or by speculative rounds
+ * ("CodePredictor Speculative Decoding", section "How a round works"):
+ *   1. draft: lm_head_{s+1..s+N-1} applied to the current hidden h_s
+ *      (section "Why the draft is free"), top-k / temperature sampling;
+ *   2. verify: one causal decoder pass over the committed code and the
+ *      N-1 drafts against the per-stream KV cache;
+ *   3. accept: exact speculative sampling, min(1, p/q), residual
+ *      norm(max(0, p - q)) at the first rejection, bonus code when every
+ *      draft is accepted ("Speculative Decoding, Beyond Text", section 02);
+ *      greedy (temperature 0) is exact argmax equality;
+ *   4. reconcile: the KV cache keeps positions 0..s' (s' = last committed
+ *      depth); rejected entries stay in memory but are never read (section 07).
+ *
+ * Sequence layout of one frame: position 0 holds x, position j >= 1 holds
+ * the embedding E_{j-1}(c_{j-1}); the decoder output at position j, through
+ * the final RMSNorm and head_j, gives the law p_j of c_j ("RVQ Position Aware
+ * Speculative Decoding for On Device TTS", Figure 1 and section 2.1).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named d_* are DEVICE pointers, h_* are HOST pointers.  The
+ *    caller owns all device memory (weights, workspace, inputs, outputs) and
+ *    must keep it alive while work it was passed to is in flight.  The
+ *    library never allocates device memory.  A context (cp_spec_ctx) is host
+ *    memory owned by the library until cp_spec_destroy.
+ *  - Every device pointer must be 16-byte aligned; otherwise the call
+ *    returns CP_SPEC_E_INVALID.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *    stream).  Calls enqueue work on it and return without synchronising,
+ *    except where stated.  Argument errors are returned synchronously and
+ *    enqueue nothing.  Device-side errors (bad code index, a grid barrier
+ *    that timed out) are recorded in a device status word and reported by
+ *    cp_spec_status_word() or by the next call on the same context.
+ *  - Randomness is Philox4x32-10 (Salmon et al., SC'11) with counter
+ *    (stream id, frame index, depth, purpose) and key = (seed mod 2^32,
+ *    seed >> 32); purpose DRAFT = 0, ACCEPT = 1, TARGET = 2.  u = (word0 >> 8)
+ *    * 2^-24.  Results are therefore reproducible bit for bit and
+ *    independent of batching or of how streams are split across calls.
+ *  - No entry point ever traps, asserts or spins without a bound on the GPU.
+ */
+#ifndef CP_SPEC_H
+#define CP_SPEC_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define CP_SPEC_MAX_LAYERS 64
+#define CP_SPEC_MAX_WINDOW 8
+#define CP_SPEC_MAX_CODE_GROUPS 64
+#define CP_SPEC_MAX_VOCAB 8192
+
+typedef enum {
+  CP_SPEC_OK = 0,
+  CP_SPEC_W_AR_FALLBACK = 1,       /* warning: speculation disabled, runs the AR loop */
+  CP_SPEC_E_INVALID = -1,          /* bad argument (range, null, alignment)           */
+  CP_SPEC_E_UNSUPPORTED = -2,      /* shape outside what the kernels implement        */
+  CP_SPEC_E_CUDA = -3,             /* a CUDA runtime call failed                      */
+  CP_SPEC_E_WORKSPACE = -4,        /* workspace smaller than cp_spec_workspace_bytes  */
+  CP_SPEC_E_DEVICE_TIMEOUT = -5,   /* a bounded device-side wait gave up              */
+  CP_SPEC_E_STATE = -6,            /* call out of order (e.g. round before begin)     */
+  CP_SPEC_E_DEVICE = -7            /* device-side check failed (e.g. code out of range) */
+} cp_spec_status;
+
+/* Decoder shape.  dtype: 0 = float32 weights, 1 = bfloat16 weights.
+ * Norm gains are always float32.  Requirements: hidden % 8 == 0,
+ * ffn % 8 == 0, n_q_heads * head_dim % 8 == 0, head_dim even and <= 256,
+ * n_q_heads % n_kv_heads == 0, 1 <= n_layers <= 64,
+ * 2 <= num_code_groups <= 64, 2 <= vocab <= 8192. */
+typedef struct {
+  int32_t hidden, n_layers, n_q_heads, n_kv_heads, head_dim, ffn, vocab, num_code_groups;
+  int32_t dtype;
+  float rope_theta; /* rotary base, rotate-half pairing (i, i + head_dim/2) */
+  float rms_eps;    /* RMSNorm epsilon                                       */
+} cp_spec_model;
+
+/* Device pointers to the weights (borrowed, read-only, row-major).
+ * embed:   [G-1][V][H]   table j (0-based) embeds c_j as the input of position j+1.
+ * lm_head: [G-1][V][H]   index j-1 is head_j (scores c_j).
+ * Per layer l: wq [nq*d][H], wk [nkv*d][H], wv [nkv*d][H], wo [H][nq*d],
+ * w_gate [F][H], w_up [F][H], w_down [H][F]; attn_norm, ffn_norm [H] fp32.
+ * final_norm [H] fp32.  The blocks are pre-norm: h += Wo attn(RMSNorm(h));
+ * h += Wdown (silu(Wgate b) * Wup b) with b = RMSNorm(h). */
+typedef struct {
+  const void* embed;
+  const void* lm_head;
+  const float* final_norm;
+  const float* attn_norm[CP_SPEC_MAX_LAYERS];
+  const void* wq[CP_SPEC_MAX_LAYERS];
+  const void* wk[CP_SPEC_MAX_LAYERS];
+  const void* wv[CP_SPEC_MAX_LAYERS];
+  const void* wo[CP_SPEC_MAX_LAYERS];
+  const float* ffn_norm[CP_SPEC_MAX_LAYERS];
+  const void* w_gate[CP_SPEC_MAX_LAYERS];
+  const void* w_up[CP_SPEC_MAX_LAYERS];
+  const void* w_down[CP_SPEC_MAX_LAYERS];
+} cp_spec_weights;
+
+/* verify_window: 0 = autoregressive loop; 2..8 = one committed depth plus
+ * N-1 drafted depths ("CodePredictor Speculative Decoding", "Options": 1 is
+ * rejected because it leaves no draft slot).  top_k: 1..vocab, the default
+ * for every stream and the maximum any stream may use.  temperature: 0 =
+ * greedy, else in [1e-3, 100].  max_streams: streams the workspace is sized
+ * for (>= 1). */
+typedef struct {
+  int32_t verify_window;
+  int32_t top_k;
+  float temperature;
+  uint64_t seed;
+  int32_t max_streams;
+} cp_spec_config;
+
+/* Counters accumulated since init (or the last cp_spec_reset_stats).
+ * committed = codes c_1..c_{G-1} emitted; passes = decoder passes (frame
+ * prefills + rounds, or AR steps); accepted/drafted_by_offset[t] = drafts at
+ * offset t (1..8) accepted / verified ("report acceptance by offset",
+ * "Speculative Decoding, Beyond Text", section 06).  weight_bytes and
+ * kv_bytes count the algorithmic HBM bytes of all decoder passes (every
+ * layer matrix once per pass, each distinct lm_head applied in the pass
+ * once, the KV positions each pass reads). */
+typedef struct {
+  int64_t frames, passes, rounds, committed, bonus, rejections;
+  int64_t drafted_by_offset[9];
+  int64_t accepted_by_offset[9];
+  int64_t weight_bytes, kv_bytes, heads_applied;
+} cp_spec_stats;
+
+typedef struct cp_spec_ctx cp_spec_ctx;
+
+/* Bytes of device workspace cp_spec_init needs for this model/config
+ * (KV cache, activations, logits, sampling lists, per-stream state).
+ * Returns 0 if the arguments are invalid. */
+size_t cp_spec_workspace_bytes(const cp_spec_model* model, const cp_spec_config* config);
+
+/* Validate, carve the caller's workspace (d_workspace, >= the size above),
+ * initialise device state on the current device (synchronously) and return a
+ * context in *out.  Returns CP_SPEC_W_AR_FALLBACK (and a usable context in AR
+ * mode) when verify_window >= 2 but num_code_groups < 3, i.e. there is no
+ * draft slot after the first code ("CodePredictor Speculative Decoding",
+ * "Limitations": automatic fallback).  vocab above CP_SPEC_MAX_VOCAB returns
+ * CP_SPEC_E_UNSUPPORTED: there is no second backend and no CPU fallback. */
+cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* weights,
+                            const cp_spec_config* config, void* d_workspace, size_t workspace_bytes,
+                            cp_spec_ctx** out);
+
+/* Per-stream sampling overrides, HOST arrays of n entries (n <= max_streams):
+ * top_k in 1..config.top_k, temperature 0 (greedy) or in [1e-3, 100].
+ * Synchronous (small host-to-device copy). */
+cp_spec_status cp_spec_set_stream_sampling(cp_spec_ctx* ctx, int32_t n, const int32_t* h_top_k,
+                                           const float* h_temperature);
+
+/* Decode n_frames frames for streams 0..n_streams-1 (n_streams <= max_streams).
+ * d_x: [n_frames][n_streams][H] float32 talker hiddens; d_c0: [n_frames][n_streams]
+ * int32 first codes; d_codes (out): [n_frames][n_streams][G] int32, with
+ * d_codes[f][b][0] = c_0.  Frame f uses Philox frame index first_frame + f.
+ * One launch on `stream`; streams advance through their frames independently.
+ * Asynchronous. */
+cp_spec_status cp_spec_decode_frames(cp_spec_ctx* ctx, int32_t n_streams, int32_t n_frames,
+                                     int32_t first_frame, const float* d_x, const int32_t* d_c0,
+                                     int32_t* d_codes, void* stream);
+
+/* Step-wise API.  cp_spec_begin_frame stages one frame for every stream
+ * (d_x [n_streams][H], d_c0 [n_streams], both read by later rounds and kept
+ * alive by the caller until the frame completes).  Each cp_spec_round runs
+ * one decoder pass for every unfinished stream: the first is the frame
+ * prefill (rows x, E_0(c_0); commits c_1), later ones are speculative
+ * rounds (or AR steps).  d_codes [n_streams][G] receives codes as they are
+ * committed; d_committed [n_streams] (optional) receives s+1, the number of
+ * codes of the frame known so far (G when the frame is complete).
+ * Asynchronous. */
+cp_spec_status cp_spec_begin_frame(cp_spec_ctx* ctx, int32_t n_streams, const float* d_x,
+                                   const int32_t* d_c0, int32_t frame_idx, void* stream);
+cp_spec_status cp_spec_round(cp_spec_ctx* ctx, int32_t* d_codes, int32_t* d_committed, void* stream);
+
+/* Teacher-forced logits, for checking the decoder numerics: rows x,
+ * E_0(c_0), ..., E_{P-2}(c_{P-2}) at positions 0..P-1 (2 <= P <= G) for each
+ * stream, run through the same verify-pass kernels in chunks of at most
+ * max(verify_window, 2) rows.  d_codes [n_streams][P-1]; d_logits (out)
+ * [n_streams][P-1][V] = head_j at position j; d_draft_logits (optional, out,
+ * speculative configs only) [n_streams][P-1][N-1][V] = head_{j+t} at
+ * position j (zero where j+t > G-1).  Asynchronous. */
+cp_spec_status cp_spec_teacher_logits(cp_spec_ctx* ctx, int32_t n_streams, int32_t P, const float* d_x,
+                                      const int32_t* d_codes, float* d_logits, float* d_draft_logits,
+                                      void* stream);
+
+/* Acceptance kernels alone (no model): R independent rounds of N-1 drafts
+ * verified against N target rows (2 <= N <= 8, 2 <= V <= 8192).
+ * mode 0: d_target [R][N][V] and d_draft [R][N-1][V] are float32 logits,
+ *         processed with top_k / temperature as in the full path;
+ * mode 1: they are already-processed float32 probabilities (each row's
+ *         non-zero entries are its support; top_k/temperature ignored,
+ *         temperature 0 not allowed).
+ * Draft t (1..N-1) is drawn from draft row t-1 with Philox (r, 0, t, DRAFT),
+ * accepted with (r, 0, t, ACCEPT); residual / bonus draws use (r, 0, t,
+ * TARGET).  Outputs: d_tokens [R][N] committed codes, -1 padded;
+ * d_n_accepted [R]; d_drafts [R][N-1] (optional).  Asynchronous; needs no
+ * context and no workspace. */
+cp_spec_status cp_spec_accept_batch(int32_t R, int32_t N, int32_t V, int32_t top_k, float temperature,
+                                    uint64_t seed, int32_t mode, const float* d_target,
+                                    const float* d_draft, int32_t* d_tokens, int32_t* d_n_accepted,
+                                    int32_t* d_drafts, void* stream);
+
+/* Synchronise `stream` and return the device status word of the context:
+ * CP_SPEC_OK, CP_SPEC_E_DEVICE_TIMEOUT or CP_SPEC_E_DEVICE.  Clears it. */
+cp_spec_status cp_spec_status_word(cp_spec_ctx* ctx, void* stream);
+
+/* Synchronise `stream` and copy the counters to *h_stats. */
+cp_spec_status cp_spec_read_stats(cp_spec_ctx* ctx, cp_spec_stats* h_stats, void* stream);
+cp_spec_status cp_spec_reset_stats(cp_spec_ctx* ctx, void* stream);
+
+/* Number of kernel launches the library has enqueued on this context
+ * (cp_spec_accept_batch counts in a process-wide counter, ctx = NULL). */
+int64_t cp_spec_launch_count(const cp_spec_ctx* ctx);
+
+/* Last error message of the context (or of the last context-free call when
+ * ctx is NULL).  Never NULL. */
+const char* cp_spec_last_error(const cp_spec_ctx* ctx);
+
+/* Release the host context.  Does not touch the caller's device memory. */
+void cp_spec_destroy(cp_spec_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* CP_SPEC_H */

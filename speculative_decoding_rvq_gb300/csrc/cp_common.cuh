@@ -1,0 +1,136 @@
+// cp_common.cuh -- device helpers shared by the kernels of the CUDA library.
+#pragma once
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace cpk {
+
+// ---------------------------------------------------------------- Philox
+// Philox4x32-10 written from its published definition (Salmon, Moraes,
+// Dror, Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC'11):
+// round (x0..x3) -> (hi(M1*x2) ^ x1 ^ k0, lo(M1*x2), hi(M0*x0) ^ x3 ^ k1,
+// lo(M0*x0)), key bumped by the Weyl constants between rounds.
+struct Philox {
+  static constexpr uint32_t kM0 = 0xD2511F53u, kM1 = 0xCD9E8D57u;
+  static constexpr uint32_t kW0 = 0x9E3779B9u, kW1 = 0xBB67AE85u;
+  __device__ __forceinline__ static uint4 block(uint4 x, uint2 k) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+      if (r) { k.x += kW0; k.y += kW1; }
+      const uint32_t lo0 = kM0 * x.x, hi0 = __umulhi(kM0, x.x);
+      const uint32_t lo1 = kM1 * x.z, hi1 = __umulhi(kM1, x.z);
+      x = make_uint4(hi1 ^ x.y ^ k.x, lo1, hi0 ^ x.w ^ k.y, lo0);
+    }
+    return x;
+  }
+};
+
+enum : uint32_t { kDraft = 0, kAccept = 1, kTarget = 2 };
+
+// u in [0, 1): top 24 bits of word 0, exact in float32.
+__device__ __forceinline__ float philox_uniform(uint64_t seed, uint32_t stream, uint32_t frame,
+                                                uint32_t depth, uint32_t purpose) {
+  const uint4 o = Philox::block(make_uint4(stream, frame, depth, purpose),
+                                make_uint2((uint32_t)(seed & 0xFFFFFFFFull), (uint32_t)(seed >> 32)));
+  return __uint2float_rn(o.x >> 8) * 5.9604644775390625e-08f;  // 2^-24
+}
+
+// ----------------------------------------------------------------- memory
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p));
+  return v;
+}
+
+// Bulk prefetch of a byte range into L2 (Hopper/Blackwell bulk-copy unit).
+// addr and bytes must be multiples of 16.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ uint64_t ld_acquire_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ int ld_relaxed_i32(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// bf16x2 word -> two floats (low half = element 0).
+__device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
+  return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+
+// Order-preserving map float -> uint32 (larger float, larger key; -0 < +0).
+__device__ __forceinline__ uint32_t float_key(float f) {
+  const uint32_t u = __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
+// Device status word values (mirror cp_spec_status).
+enum : int { kStatusOk = 0, kStatusTimeout = -5, kStatusDevice = -7 };
+
+__device__ __forceinline__ void raise_status(int* status, int code) { atomicCAS(status, 0, code); }
+
+// Grid-wide barrier for a cooperative launch.  `counter` is zeroed before the
+// launch; generation g completes when it reaches g * gridDim.x.  Every wait
+// is bounded by `timeout_ns` of %globaltimer and by the status word: on
+// timeout the status is set and the function returns false so the caller
+// can leave the kernel; nothing spins forever.
+__device__ __forceinline__ bool grid_barrier(unsigned long long* counter, int* status,
+                                             unsigned long long& gen, uint64_t timeout_ns) {
+  __syncthreads();
+  bool ok = true;
+  if (threadIdx.x == 0) {
+    ++gen;
+    const unsigned long long target = gen * (unsigned long long)gridDim.x;
+    __threadfence();
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(counter) : "memory");
+    uint64_t t0 = globaltimer_ns();
+    uint32_t spins = 0;
+    while (ld_acquire_u64(counter) < target) {
+      ++spins;
+      if ((spins & 63u) == 0) {
+        const uint64_t now = globaltimer_ns();
+        // bounded twice over: by the global timer and by an iteration count
+        if (now - t0 > timeout_ns || spins > (1u << 30)) { raise_status(status, kStatusTimeout); ok = false; break; }
+        if (ld_relaxed_i32(status) != 0) { ok = false; break; }
+      }
+      if (spins > 4096u) __nanosleep(256);
+    }
+  } else {
+    ++gen;
+  }
+  // broadcast the verdict through shared memory
+  __shared__ int s_ok;
+  if (threadIdx.x == 0) s_ok = ok ? 1 : 0;
+  __syncthreads();
+  return s_ok != 0;
+}
+
+}  // namespace cpk

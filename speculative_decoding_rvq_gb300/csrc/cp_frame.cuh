@@ -1,0 +1,146 @@
+// cp_frame.cuh -- parameter block and workspace layout of the persistent
+// frame kernel (shared by the kernel and the host-side C ABI).
+#pragma once
+#include <stdint.h>
+
+#include "../../include/cp_spec.h"
+
+namespace cpk {
+
+enum StreamPhase : int { kPhasePrefill = 0, kPhaseAR = 1, kPhaseSpec = 2, kPhaseTeacher = 3, kPhaseDone = 4 };
+enum RunMode : int { kModeDecode = 0, kModeTeacher = 1 };
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+// Per-stream device state (one warp owns it in the accept phase).
+struct StreamState {
+  int phase;      // StreamPhase of the pass that is in flight
+  int frame;      // frame index within the current launch sequence
+  int frame_abs;  // Philox frame index
+  int s;          // committed depth (codes c_0..c_s known)
+  int m;          // rows in the pass in flight
+  int pos0;       // position of row 0 of the pass
+  int n_d;        // drafts verified by the pass in flight
+  int pad;
+  int drafts[8];
+  int codes[CP_SPEC_MAX_CODE_GROUPS];
+};
+
+struct StreamStats {
+  long long frames, passes, rounds, committed, bonus, rejections;
+  long long drafted[9], accepted[9];
+};
+
+// Persistent control words (survive across launches, except `bar`).
+struct Control {
+  unsigned long long bar;            // grid barrier counter, zeroed before each launch
+  unsigned long long head_mask[2];   // lm_heads needed by the next pass (double-buffered by pass parity)
+  long long weight_bytes, kv_bytes, heads_applied, passes;
+  int active;                        // streams with frames left
+  int pass_global;                   // passes run since init (parity of head_mask)
+  int status;                        // device status word (cp_spec_status values)
+  int pad;
+  int dbg_pass, dbg_phase, dbg_active, dbg_gen;  // progress record of CTA 0 (diagnostics)
+};
+
+struct FrameParams {
+  // model
+  int H, L, nq, nkv, d, F, V, G, dtype;
+  float eps;
+  int N;    // verify window (0 = autoregressive)
+  int NS;   // row slots per stream = max(N, 2)
+  int ND;   // draft logit slots per row = max(N - 1, 0)
+  int KC;   // list capacity = min(max top_k, V)
+  int RB;   // activation rows per GEMV chunk
+  int proc_warps;  // warps per CTA that run the top-k phase
+  unsigned long long seed;
+  unsigned long long timeout_ns;
+  long long layer_bytes, head_bytes;  // algorithmic bytes per layer / per lm_head
+  const void* embed;
+  const void* head;
+  const float* final_norm;
+  const float* attn_norm[CP_SPEC_MAX_LAYERS];
+  const void* wq[CP_SPEC_MAX_LAYERS];
+  const void* wk[CP_SPEC_MAX_LAYERS];
+  const void* wv[CP_SPEC_MAX_LAYERS];
+  const void* wo[CP_SPEC_MAX_LAYERS];
+  const float* ffn_norm[CP_SPEC_MAX_LAYERS];
+  const void* w_gate[CP_SPEC_MAX_LAYERS];
+  const void* w_up[CP_SPEC_MAX_LAYERS];
+  const void* w_down[CP_SPEC_MAX_LAYERS];
+  // workspace
+  float* kv;       // [Bmax][L][2][G][nkv][d]
+  float* h;        // [Bmax*NS][H]
+  float* qbuf;     // [Bmax*NS][nq*d]
+  float* obuf;     // [Bmax*NS][nq*d]
+  float* act;      // [Bmax*NS][F]
+  float* logits;   // [Bmax*NS][1+ND][V]
+  int* lidx;       // [Bmax*NS][1+ND][KC]
+  float* lprob;    // [Bmax*NS][1+ND][KC]
+  int* lcount;     // [Bmax*NS][1+ND]
+  int* qidx;       // [Bmax][max(ND,1)][KC]
+  float* qprob;    // [Bmax][max(ND,1)][KC]
+  int* qcount;     // [Bmax][max(ND,1)]
+  int* row_pos;    // [Bmax*NS] position, -1 = inactive
+  StreamState* st; // [Bmax]
+  StreamStats* sstats;  // [Bmax]
+  float2* rope;    // [G][d/2] (cos, sin)
+  int* top_k;      // [Bmax]
+  float* temp;     // [Bmax]
+  Control* ctl;
+  // this launch
+  int mode;        // RunMode
+  int B;           // streams
+  int n_frames;
+  int first_frame;
+  int max_passes;  // 0 = until every stream finished
+  int do_setup;    // stage the first frame / teacher chunk before the first pass
+  const float* x;  // [n_frames][B][H]
+  const int* c0;   // [n_frames][B]
+  int* codes_out;  // [n_frames][B][G]
+  int* committed_out;  // [B] or null
+  int P;                 // teacher positions
+  const int* t_codes;    // [B][P-1]
+  float* t_logits;       // [B][P-1][V]
+  float* t_draft;        // [B][P-1][ND][V] or null
+};
+
+// Workspace carve-up, computed identically by the host for sizing.
+struct Layout {
+  size_t kv, h, qbuf, obuf, act, logits, lidx, lprob, lcount, qidx, qprob, qcount, row_pos, st, sstats,
+      rope, top_k, temp, ctl, total;
+};
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+inline Layout make_layout(int H, int L, int nq, int nkv, int d, int F, int V, int G, int N, int KC, int Bmax) {
+  const int NS = N > 2 ? N : 2, ND = N > 1 ? N - 1 : 0, NDq = ND > 0 ? ND : 1;
+  const size_t rows = (size_t)Bmax * NS;
+  Layout o{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes, 256); return at; };
+  o.kv = take(sizeof(float) * (size_t)Bmax * L * 2 * G * nkv * d);
+  o.h = take(sizeof(float) * rows * H);
+  o.qbuf = take(sizeof(float) * rows * nq * d);
+  o.obuf = take(sizeof(float) * rows * nq * d);
+  o.act = take(sizeof(float) * rows * F);
+  o.logits = take(sizeof(float) * rows * (1 + ND) * V);
+  o.lidx = take(sizeof(int) * rows * (1 + ND) * KC);
+  o.lprob = take(sizeof(float) * rows * (1 + ND) * KC);
+  o.lcount = take(sizeof(int) * rows * (1 + ND));
+  o.qidx = take(sizeof(int) * (size_t)Bmax * NDq * KC);
+  o.qprob = take(sizeof(float) * (size_t)Bmax * NDq * KC);
+  o.qcount = take(sizeof(int) * (size_t)Bmax * NDq);
+  o.row_pos = take(sizeof(int) * rows);
+  o.st = take(sizeof(StreamState) * (size_t)Bmax);
+  o.sstats = take(sizeof(StreamStats) * (size_t)Bmax);
+  o.rope = take(sizeof(float) * 2 * (size_t)G * (d / 2));
+  o.top_k = take(sizeof(int) * (size_t)Bmax);
+  o.temp = take(sizeof(float) * (size_t)Bmax);
+  o.ctl = take(sizeof(Control));
+  o.total = off;
+  return o;
+}
+
+}  // namespace cpk

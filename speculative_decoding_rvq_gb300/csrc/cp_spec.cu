@@ -1,0 +1,419 @@
+// cp_spec.cu -- host side of the C ABI declared in include/cp_spec.h.
+//
+// Validates arguments, carves the caller's workspace, fills the launch
+// parameter block and enqueues the kernels.  Never allocates device memory.
+#include <cuda_runtime.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <new>
+#include <string>
+
+#include "../../include/cp_spec.h"
+#include "cp_frame.cuh"
+
+namespace cpk_host {
+cudaError_t launch_frame_kernel(const cpk::FrameParams& P, int grid, size_t smem, cudaStream_t stream);
+cudaError_t frame_kernel_config(int dtype, size_t smem, int* max_blocks_per_sm);
+cudaError_t launch_init_tables(float2* rope, int G, int d, double theta, int* top_k, float* temp, int Bmax, int k,
+                               float T, cudaStream_t stream);
+cudaError_t launch_accept_batch(int R, int N, int V, int k, float T, unsigned long long seed, int mode,
+                                const float* tgt, const float* drf, int* tokens, int* nacc, int* drafts,
+                                cudaStream_t stream);
+}  // namespace cpk_host
+
+struct cp_spec_ctx {
+  cp_spec_model model;
+  cp_spec_weights weights;
+  cp_spec_config config;
+  int N;  // effective window (0 after an AR fallback)
+  int device, grid;
+  size_t smem;
+  cpk::Layout lay;
+  unsigned char* ws;
+  cpk::FrameParams base;
+  long long launches;
+  std::string err;
+  // step-wise API
+  bool staged, need_setup;
+  int staged_B, staged_frame;
+  const float* staged_x;
+  const int* staged_c0;
+};
+
+namespace {
+
+std::string g_err = "";
+std::atomic<long long> g_free_launches{0};
+constexpr unsigned long long kBarrierTimeoutNs = 20ull * 1000ull * 1000ull * 1000ull;  // 20 s per wait
+
+cp_spec_status fail(cp_spec_ctx* c, cp_spec_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (c) c->err = buf; else g_err = buf;
+  return s;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+cp_spec_status check_cuda(cp_spec_ctx* c, cudaError_t e, const char* what) {
+  if (e == cudaSuccess) return CP_SPEC_OK;
+  return fail(c, CP_SPEC_E_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+int window_of(const cp_spec_config* cfg) { return cfg->verify_window; }
+
+cp_spec_status validate(const cp_spec_model* m, const cp_spec_config* cfg, cp_spec_ctx* c) {
+  if (!m || !cfg) return fail(c, CP_SPEC_E_INVALID, "null model or config");
+  if (m->dtype != 0 && m->dtype != 1) return fail(c, CP_SPEC_E_INVALID, "dtype must be 0 (fp32) or 1 (bf16)");
+  if (m->hidden <= 0 || m->hidden % 8) return fail(c, CP_SPEC_E_UNSUPPORTED, "hidden must be a positive multiple of 8");
+  if (m->ffn <= 0 || m->ffn % 8) return fail(c, CP_SPEC_E_UNSUPPORTED, "ffn must be a positive multiple of 8");
+  if (m->head_dim <= 0 || m->head_dim % 8 || m->head_dim > 256)
+    return fail(c, CP_SPEC_E_UNSUPPORTED, "head_dim must be a multiple of 8 in [8, 256]");
+  if (m->n_q_heads <= 0 || m->n_kv_heads <= 0 || m->n_q_heads % m->n_kv_heads)
+    return fail(c, CP_SPEC_E_UNSUPPORTED, "n_q_heads must be a positive multiple of n_kv_heads");
+  if ((m->n_q_heads * m->head_dim) % 8) return fail(c, CP_SPEC_E_UNSUPPORTED, "n_q_heads*head_dim must be a multiple of 8");
+  if (m->n_layers < 1 || m->n_layers > CP_SPEC_MAX_LAYERS) return fail(c, CP_SPEC_E_UNSUPPORTED, "n_layers must be in [1, 64]");
+  if (m->num_code_groups < 2 || m->num_code_groups > CP_SPEC_MAX_CODE_GROUPS)
+    return fail(c, CP_SPEC_E_INVALID, "num_code_groups must be in [2, 64]");
+  if (m->vocab < 2 || m->vocab % 2) return fail(c, CP_SPEC_E_UNSUPPORTED, "vocab must be even and >= 2");
+  if (m->vocab > CP_SPEC_MAX_VOCAB)
+    return fail(c, CP_SPEC_E_UNSUPPORTED, "vocab %d above the small-vocabulary bound %d", m->vocab, CP_SPEC_MAX_VOCAB);
+  if (!(m->rope_theta > 0.0f) || !(m->rms_eps >= 0.0f)) return fail(c, CP_SPEC_E_INVALID, "bad rope_theta or rms_eps");
+  const int N = window_of(cfg);
+  if (!(N == 0 || (N >= 2 && N <= CP_SPEC_MAX_WINDOW)))
+    return fail(c, CP_SPEC_E_INVALID, "verify_window must be 0 or in [2, 8] (1 leaves no draft slot)");
+  if (cfg->top_k < 1 || cfg->top_k > m->vocab) return fail(c, CP_SPEC_E_INVALID, "top_k must be in [1, vocab]");
+  const float T = cfg->temperature;
+  if (!(T == 0.0f || (T >= 1e-3f && T <= 100.0f))) return fail(c, CP_SPEC_E_INVALID, "temperature must be 0 or in [1e-3, 100]");
+  if (cfg->max_streams < 1) return fail(c, CP_SPEC_E_INVALID, "max_streams must be >= 1");
+  return CP_SPEC_OK;
+}
+
+int effective_window(const cp_spec_model* m, const cp_spec_config* cfg) {
+  const int N = window_of(cfg);
+  if (N >= 2 && m->num_code_groups < 3) return 0;  // no draft slot after c_1: AR fallback
+  return N;
+}
+
+cpk::Layout layout_for(const cp_spec_model* m, const cp_spec_config* cfg, int N) {
+  const int KC = cfg->top_k < m->vocab ? cfg->top_k : m->vocab;
+  return cpk::make_layout(m->hidden, m->n_layers, m->n_q_heads, m->n_kv_heads, m->head_dim, m->ffn, m->vocab,
+                          m->num_code_groups, N, KC, cfg->max_streams);
+}
+
+struct SmemPlan {
+  int RB, proc_warps;
+  size_t bytes;
+};
+
+SmemPlan smem_plan(const cp_spec_model* m, int N, int KC, int Bmax) {
+  const int NS = N > 2 ? N : 2;
+  const int Kmax = std::max(std::max(m->hidden, m->n_q_heads * m->head_dim), m->ffn);
+  int RB = 8;
+  while (RB > 1 && (size_t)RB * Kmax * 4 > 98304) RB /= 2;
+  const size_t gemv = (size_t)RB * Kmax * 4 + (size_t)cpk::kWarps * 2 * RB * 4;
+  const size_t attn = (size_t)cpk::kWarps * (256 + 64) * 4;
+  const size_t per_warp = ((size_t)m->vocab * 4 + 1024 + (size_t)KC * 8 + 15) / 16 * 16;
+  int pw = (int)std::min<size_t>(cpk::kWarps, std::max<size_t>(1, (size_t)150 * 1024 / per_warp));
+  const size_t proc = per_warp * pw;
+  const size_t acc = (size_t)cpk::kWarps * sizeof(cpk::StreamState);
+  const size_t uni = std::max(std::max(gemv, attn), std::max(proc, acc));
+  const size_t rows = ((size_t)Bmax * NS * 4 + 15) / 16 * 16;
+  return SmemPlan{RB, pw, rows + uni};
+}
+
+template <typename T>
+T* at(unsigned char* base, size_t off) { return reinterpret_cast<T*>(base + off); }
+
+cp_spec_status enqueue_frame(cp_spec_ctx* c, const cpk::FrameParams& P, bool clear_masks, cudaStream_t s) {
+  cpk::Control* ctl = at<cpk::Control>(c->ws, c->lay.ctl);
+  cudaError_t e = cudaMemsetAsync(ctl, 0, clear_masks ? 3 * sizeof(unsigned long long) : sizeof(unsigned long long), s);
+  if (e != cudaSuccess) return check_cuda(c, e, "cudaMemsetAsync(control)");
+  e = cpk_host::launch_frame_kernel(P, c->grid, c->smem, s);
+  if (e != cudaSuccess) return check_cuda(c, e, "frame kernel launch");
+  c->launches += 1;
+  return CP_SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t cp_spec_workspace_bytes(const cp_spec_model* model, const cp_spec_config* config) {
+  if (validate(model, config, nullptr) != CP_SPEC_OK) return 0;
+  return layout_for(model, config, effective_window(model, config)).total;
+}
+
+cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* weights, const cp_spec_config* config,
+                            void* d_workspace, size_t workspace_bytes, cp_spec_ctx** out) {
+  if (!out) return fail(nullptr, CP_SPEC_E_INVALID, "out is null");
+  *out = nullptr;
+  cp_spec_status v = validate(model, config, nullptr);
+  if (v != CP_SPEC_OK) return v;
+  if (!weights) return fail(nullptr, CP_SPEC_E_INVALID, "weights is null");
+  const int L = model->n_layers;
+  const void* ptrs[] = {weights->embed, weights->lm_head, weights->final_norm};
+  for (const void* p : ptrs)
+    if (!p || !aligned16(p)) return fail(nullptr, CP_SPEC_E_INVALID, "embed/lm_head/final_norm null or not 16-byte aligned");
+  for (int l = 0; l < L; ++l) {
+    const void* lp[] = {weights->attn_norm[l], weights->wq[l], weights->wk[l], weights->wv[l], weights->wo[l],
+                        weights->ffn_norm[l], weights->w_gate[l], weights->w_up[l], weights->w_down[l]};
+    for (const void* p : lp)
+      if (!p || !aligned16(p)) return fail(nullptr, CP_SPEC_E_INVALID, "layer %d weight null or not 16-byte aligned", l);
+  }
+  if (!d_workspace || !aligned16(d_workspace)) return fail(nullptr, CP_SPEC_E_INVALID, "workspace null or not 16-byte aligned");
+  const int N = effective_window(model, config);
+  const cpk::Layout lay = layout_for(model, config, N);
+  if (workspace_bytes < lay.total)
+    return fail(nullptr, CP_SPEC_E_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes, lay.total);
+  int dev = 0, sms = 0, coop = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  if (e != cudaSuccess) return check_cuda(nullptr, e, "device query");
+  if (!coop) return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "device does not support cooperative launches");
+  const int KC = config->top_k < model->vocab ? config->top_k : model->vocab;
+  const SmemPlan sp = smem_plan(model, N, KC, config->max_streams);
+  int maxb = 0;
+  e = cpk_host::frame_kernel_config(model->dtype, sp.bytes, &maxb);
+  if (e != cudaSuccess) return check_cuda(nullptr, e, "frame kernel attributes");
+  if (maxb < 1) return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "frame kernel needs %zu bytes of shared memory per CTA", sp.bytes);
+  const int NS = N > 2 ? N : 2;
+  if ((long long)config->max_streams > (long long)sms * cpk::kWarps)
+    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "max_streams above %d (one accept warp per stream)", sms * cpk::kWarps);
+
+  cp_spec_ctx* c = new (std::nothrow) cp_spec_ctx();
+  if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "host allocation failed");
+  c->model = *model;
+  c->weights = *weights;
+  c->config = *config;
+  c->N = N;
+  c->device = dev;
+  c->grid = sms;
+  c->smem = sp.bytes;
+  c->lay = lay;
+  c->ws = static_cast<unsigned char*>(d_workspace);
+  c->launches = 0;
+  c->staged = c->need_setup = false;
+
+  cpk::FrameParams& P = c->base;
+  memset(&P, 0, sizeof P);
+  P.H = model->hidden; P.L = L; P.nq = model->n_q_heads; P.nkv = model->n_kv_heads; P.d = model->head_dim;
+  P.F = model->ffn; P.V = model->vocab; P.G = model->num_code_groups; P.dtype = model->dtype;
+  P.eps = model->rms_eps;
+  P.N = N; P.NS = NS; P.ND = N > 1 ? N - 1 : 0; P.KC = KC; P.RB = sp.RB; P.proc_warps = sp.proc_warps;
+  P.seed = config->seed;
+  P.timeout_ns = kBarrierTimeoutNs;
+  const long long eb = model->dtype == 1 ? 2 : 4;
+  const long long H = model->hidden, qd = (long long)model->n_q_heads * model->head_dim,
+                  kvd = (long long)model->n_kv_heads * model->head_dim, F = model->ffn;
+  P.layer_bytes = (qd * H + 2 * kvd * H + H * qd + 3 * F * H) * eb + 2 * H * 4;
+  P.head_bytes = (long long)model->vocab * H * eb;
+  P.embed = weights->embed; P.head = weights->lm_head; P.final_norm = weights->final_norm;
+  for (int l = 0; l < L; ++l) {
+    P.attn_norm[l] = weights->attn_norm[l]; P.wq[l] = weights->wq[l]; P.wk[l] = weights->wk[l];
+    P.wv[l] = weights->wv[l]; P.wo[l] = weights->wo[l]; P.ffn_norm[l] = weights->ffn_norm[l];
+    P.w_gate[l] = weights->w_gate[l]; P.w_up[l] = weights->w_up[l]; P.w_down[l] = weights->w_down[l];
+  }
+  unsigned char* ws = c->ws;
+  P.kv = at<float>(ws, lay.kv); P.h = at<float>(ws, lay.h); P.qbuf = at<float>(ws, lay.qbuf);
+  P.obuf = at<float>(ws, lay.obuf); P.act = at<float>(ws, lay.act); P.logits = at<float>(ws, lay.logits);
+  P.lidx = at<int>(ws, lay.lidx); P.lprob = at<float>(ws, lay.lprob); P.lcount = at<int>(ws, lay.lcount);
+  P.qidx = at<int>(ws, lay.qidx); P.qprob = at<float>(ws, lay.qprob); P.qcount = at<int>(ws, lay.qcount);
+  P.row_pos = at<int>(ws, lay.row_pos); P.st = at<cpk::StreamState>(ws, lay.st);
+  P.sstats = at<cpk::StreamStats>(ws, lay.sstats); P.rope = at<float2>(ws, lay.rope);
+  P.top_k = at<int>(ws, lay.top_k); P.temp = at<float>(ws, lay.temp); P.ctl = at<cpk::Control>(ws, lay.ctl);
+
+  e = cudaMemset(ws, 0, lay.total);
+  if (e == cudaSuccess)
+    e = cudaMemset(P.row_pos, 0xFF, sizeof(int) * (size_t)config->max_streams * NS);
+  if (e == cudaSuccess)
+    e = cpk_host::launch_init_tables(P.rope, P.G, P.d, (double)model->rope_theta, P.top_k, P.temp, config->max_streams,
+                                     config->top_k, config->temperature, 0);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    cp_spec_status s = check_cuda(nullptr, e, "workspace initialisation");
+    delete c;
+    return s;
+  }
+  c->launches += 1;
+  *out = c;
+  if (N != window_of(config)) {
+    c->err = "speculation disabled: fewer than 3 code groups leave no draft slot; running the autoregressive loop";
+    return CP_SPEC_W_AR_FALLBACK;
+  }
+  return CP_SPEC_OK;
+}
+
+cp_spec_status cp_spec_set_stream_sampling(cp_spec_ctx* c, int32_t n, const int32_t* h_top_k, const float* h_temp) {
+  if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "null context");
+  if (n < 1 || n > c->config.max_streams || !h_top_k || !h_temp)
+    return fail(c, CP_SPEC_E_INVALID, "n must be in [1, max_streams] with non-null arrays");
+  for (int i = 0; i < n; ++i) {
+    if (h_top_k[i] < 1 || h_top_k[i] > c->base.KC) return fail(c, CP_SPEC_E_INVALID, "stream %d: top_k out of [1, %d]", i, c->base.KC);
+    const float T = h_temp[i];
+    if (!(T == 0.0f || (T >= 1e-3f && T <= 100.0f))) return fail(c, CP_SPEC_E_INVALID, "stream %d: bad temperature", i);
+  }
+  cudaError_t e = cudaMemcpy(c->base.top_k, h_top_k, sizeof(int) * n, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess) e = cudaMemcpy(c->base.temp, h_temp, sizeof(float) * n, cudaMemcpyHostToDevice);
+  return check_cuda(c, e, "set_stream_sampling copy");
+}
+
+cp_spec_status cp_spec_decode_frames(cp_spec_ctx* c, int32_t n_streams, int32_t n_frames, int32_t first_frame,
+                                     const float* d_x, const int32_t* d_c0, int32_t* d_codes, void* stream) {
+  if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "null context");
+  if (n_streams < 1 || n_streams > c->config.max_streams) return fail(c, CP_SPEC_E_INVALID, "n_streams out of [1, max_streams]");
+  if (n_frames < 0 || first_frame < 0) return fail(c, CP_SPEC_E_INVALID, "negative n_frames or first_frame");
+  if (n_frames == 0) return CP_SPEC_OK;
+  if (!d_x || !d_c0 || !d_codes || !aligned16(d_x) || !aligned16(d_c0) || !aligned16(d_codes))
+    return fail(c, CP_SPEC_E_INVALID, "x/c0/codes null or not 16-byte aligned");
+  cpk::FrameParams P = c->base;
+  P.mode = cpk::kModeDecode;
+  P.B = n_streams; P.n_frames = n_frames; P.first_frame = first_frame;
+  P.max_passes = 0; P.do_setup = 1;
+  P.x = d_x; P.c0 = d_c0; P.codes_out = d_codes; P.committed_out = nullptr;
+  c->staged = false;
+  return enqueue_frame(c, P, true, static_cast<cudaStream_t>(stream));
+}
+
+cp_spec_status cp_spec_begin_frame(cp_spec_ctx* c, int32_t n_streams, const float* d_x, const int32_t* d_c0,
+                                   int32_t frame_idx, void* stream) {
+  (void)stream;
+  if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "null context");
+  if (n_streams < 1 || n_streams > c->config.max_streams) return fail(c, CP_SPEC_E_INVALID, "n_streams out of [1, max_streams]");
+  if (frame_idx < 0) return fail(c, CP_SPEC_E_INVALID, "negative frame index");
+  if (!d_x || !d_c0 || !aligned16(d_x) || !aligned16(d_c0)) return fail(c, CP_SPEC_E_INVALID, "x/c0 null or misaligned");
+  c->staged = true;
+  c->need_setup = true;
+  c->staged_B = n_streams;
+  c->staged_frame = frame_idx;
+  c->staged_x = d_x;
+  c->staged_c0 = d_c0;
+  return CP_SPEC_OK;
+}
+
+cp_spec_status cp_spec_round(cp_spec_ctx* c, int32_t* d_codes, int32_t* d_committed, void* stream) {
+  if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "null context");
+  if (!c->staged) return fail(c, CP_SPEC_E_STATE, "cp_spec_round before cp_spec_begin_frame");
+  if (!d_codes || !aligned16(d_codes) || (d_committed && !aligned16(d_committed)))
+    return fail(c, CP_SPEC_E_INVALID, "codes null or misaligned");
+  cpk::FrameParams P = c->base;
+  P.mode = cpk::kModeDecode;
+  P.B = c->staged_B; P.n_frames = 1; P.first_frame = c->staged_frame;
+  P.max_passes = 1; P.do_setup = c->need_setup ? 1 : 0;
+  P.x = c->staged_x; P.c0 = c->staged_c0; P.codes_out = d_codes; P.committed_out = d_committed;
+  const bool setup = c->need_setup;
+  c->need_setup = false;
+  return enqueue_frame(c, P, setup, static_cast<cudaStream_t>(stream));
+}
+
+cp_spec_status cp_spec_teacher_logits(cp_spec_ctx* c, int32_t n_streams, int32_t P_, const float* d_x,
+                                      const int32_t* d_codes, float* d_logits, float* d_draft_logits, void* stream) {
+  if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "null context");
+  if (n_streams < 1 || n_streams > c->config.max_streams) return fail(c, CP_SPEC_E_INVALID, "n_streams out of [1, max_streams]");
+  if (P_ < 2 || P_ > c->model.num_code_groups) return fail(c, CP_SPEC_E_INVALID, "P must be in [2, num_code_groups]");
+  if (!d_x || !d_codes || !d_logits || !aligned16(d_x) || !aligned16(d_codes) || !aligned16(d_logits))
+    return fail(c, CP_SPEC_E_INVALID, "x/codes/logits null or misaligned");
+  if (d_draft_logits && (c->N < 2 || !aligned16(d_draft_logits)))
+    return fail(c, CP_SPEC_E_INVALID, "draft logits need a speculative window and 16-byte alignment");
+  cpk::FrameParams P = c->base;
+  P.mode = cpk::kModeTeacher;
+  P.B = n_streams; P.n_frames = 1; P.first_frame = 0;
+  P.max_passes = 0; P.do_setup = 1;
+  P.x = d_x; P.c0 = nullptr; P.codes_out = nullptr; P.committed_out = nullptr;
+  P.P = P_; P.t_codes = d_codes; P.t_logits = d_logits; P.t_draft = d_draft_logits;
+  c->staged = false;
+  return enqueue_frame(c, P, true, static_cast<cudaStream_t>(stream));
+}
+
+cp_spec_status cp_spec_accept_batch(int32_t R, int32_t N, int32_t V, int32_t top_k, float temperature, uint64_t seed,
+                                    int32_t mode, const float* d_target, const float* d_draft, int32_t* d_tokens,
+                                    int32_t* d_n_accepted, int32_t* d_drafts, void* stream) {
+  if (R < 0) return fail(nullptr, CP_SPEC_E_INVALID, "R must be >= 0");
+  if (N < 2 || N > CP_SPEC_MAX_WINDOW) return fail(nullptr, CP_SPEC_E_INVALID, "N must be in [2, 8]");
+  if (V < 2 || V > CP_SPEC_MAX_VOCAB) return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "V must be in [2, %d]", CP_SPEC_MAX_VOCAB);
+  if (mode != 0 && mode != 1) return fail(nullptr, CP_SPEC_E_INVALID, "mode must be 0 (logits) or 1 (probabilities)");
+  if (mode == 0) {
+    if (top_k < 1 || top_k > V) return fail(nullptr, CP_SPEC_E_INVALID, "top_k must be in [1, V]");
+    if (!(temperature == 0.0f || (temperature >= 1e-3f && temperature <= 100.0f)))
+      return fail(nullptr, CP_SPEC_E_INVALID, "temperature must be 0 or in [1e-3, 100]");
+  } else {
+    top_k = 1;  // lists unused in probability mode
+    temperature = 1.0f;
+  }
+  if (R == 0) return CP_SPEC_OK;
+  if (!d_target || !d_draft || !d_tokens || !d_n_accepted || !aligned16(d_target) || !aligned16(d_draft) ||
+      !aligned16(d_tokens) || !aligned16(d_n_accepted) || (d_drafts && !aligned16(d_drafts)))
+    return fail(nullptr, CP_SPEC_E_INVALID, "null or misaligned pointer");
+  cudaError_t e = cpk_host::launch_accept_batch(R, N, V, top_k, temperature, seed, mode, d_target, d_draft, d_tokens,
+                                                d_n_accepted, d_drafts, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return check_cuda(nullptr, e, "accept kernel launch");
+  g_free_launches.fetch_add(1);
+  return CP_SPEC_OK;
+}
+
+cp_spec_status cp_spec_status_word(cp_spec_ctx* c, void* stream) {
+  if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "null context");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return check_cuda(c, e, "stream synchronize");
+  cpk::Control* ctl = c->base.ctl;
+  int st = 0;
+  e = cudaMemcpy(&st, &ctl->status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess && st != 0) e = cudaMemset(&ctl->status, 0, sizeof(int));
+  if (e != cudaSuccess) return check_cuda(c, e, "status word read");
+  if (st == CP_SPEC_E_DEVICE_TIMEOUT) return fail(c, CP_SPEC_E_DEVICE_TIMEOUT, "a device grid barrier timed out");
+  if (st != 0) return fail(c, CP_SPEC_E_DEVICE, "device-side check failed (code out of range)");
+  return CP_SPEC_OK;
+}
+
+cp_spec_status cp_spec_read_stats(cp_spec_ctx* c, cp_spec_stats* out, void* stream) {
+  if (!c || !out) return fail(c, CP_SPEC_E_INVALID, "null argument");
+  cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return check_cuda(c, e, "stream synchronize");
+  const int B = c->config.max_streams;
+  cpk::StreamStats* hs = new (std::nothrow) cpk::StreamStats[B];
+  if (!hs) return fail(c, CP_SPEC_E_INVALID, "host allocation failed");
+  cpk::Control ctl;
+  e = cudaMemcpy(hs, c->base.sstats, sizeof(cpk::StreamStats) * B, cudaMemcpyDeviceToHost);
+  if (e == cudaSuccess) e = cudaMemcpy(&ctl, c->base.ctl, sizeof ctl, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) { delete[] hs; return check_cuda(c, e, "stats copy"); }
+  memset(out, 0, sizeof *out);
+  for (int b = 0; b < B; ++b) {
+    out->frames += hs[b].frames; out->rounds += hs[b].rounds; out->committed += hs[b].committed;
+    out->bonus += hs[b].bonus; out->rejections += hs[b].rejections;
+    for (int t = 0; t < 9; ++t) { out->drafted_by_offset[t] += hs[b].drafted[t]; out->accepted_by_offset[t] += hs[b].accepted[t]; }
+  }
+  out->passes = ctl.passes;
+  out->weight_bytes = ctl.weight_bytes;
+  out->kv_bytes = ctl.kv_bytes;
+  out->heads_applied = ctl.heads_applied;
+  delete[] hs;
+  return CP_SPEC_OK;
+}
+
+cp_spec_status cp_spec_reset_stats(cp_spec_ctx* c, void* stream) {
+  if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "null context");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(c->base.sstats, 0, sizeof(cpk::StreamStats) * c->config.max_streams, s);
+  if (e == cudaSuccess)
+    e = cudaMemsetAsync(&c->base.ctl->weight_bytes, 0, 4 * sizeof(long long), s);
+  return check_cuda(c, e, "reset stats");
+}
+
+int64_t cp_spec_launch_count(const cp_spec_ctx* c) {
+  return c ? c->launches : g_free_launches.load();
+}
+
+const char* cp_spec_last_error(const cp_spec_ctx* c) { return c ? c->err.c_str() : g_err.c_str(); }
+
+void cp_spec_destroy(cp_spec_ctx* c) { delete c; }
+
+}  // extern "C"

@@ -1,0 +1,87 @@
+"""The C-ABI library loads on a machine without a GPU, exports every symbol
+include/cp_spec.h declares, and rejects bad arguments on the host (no device
+work is enqueued for an argument error)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from speculative_decoding_rvq_gb300 import build, binding
+    build.build()
+    return binding.load()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names |= set(re.findall(r"\b(cp_spec_\w+)\s*\(", txt))
+    return names
+
+
+def test_exports_every_declared_symbol(lib):
+    from speculative_decoding_rvq_gb300 import binding
+    declared = _declared()
+    assert declared == set(binding.EXPORTS)
+    for n in declared:
+        assert hasattr(lib, n), n
+
+
+def _cfg(b, **kw):
+    d = dict(verify_window=4, top_k=50, temperature=0.9, seed=1, max_streams=1)
+    d.update(kw)
+    return b.Config(**d)
+
+
+def test_workspace_bytes_validates(lib):
+    from speculative_decoding_rvq_gb300 import binding as b, synth as S
+    m = b.model_struct(S.TTS06B_BF16)
+    assert lib.cp_spec_workspace_bytes(C.byref(m), C.byref(_cfg(b))) > 0
+    for bad in (dict(verify_window=1), dict(verify_window=9), dict(verify_window=-1), dict(top_k=0),
+                dict(top_k=5000), dict(temperature=-1.0), dict(temperature=1e-6), dict(max_streams=0)):
+        assert lib.cp_spec_workspace_bytes(C.byref(m), C.byref(_cfg(b, **bad))) == 0, bad
+    big = b.model_struct(S.ModelSpec(1024, 2, 8, 8, 128, 3072, 16384, 16, 1))
+    assert lib.cp_spec_workspace_bytes(C.byref(big), C.byref(_cfg(b))) == 0
+    # workspace grows with the number of streams
+    one = lib.cp_spec_workspace_bytes(C.byref(m), C.byref(_cfg(b)))
+    many = lib.cp_spec_workspace_bytes(C.byref(m), C.byref(_cfg(b, max_streams=64)))
+    assert many > 32 * one // 2
+
+
+def test_init_rejects_on_host(lib):
+    from speculative_decoding_rvq_gb300 import binding as b, synth as S
+    m = b.model_struct(S.TINY_FP32)
+    w = b.Weights()
+    ctx = C.c_void_p()
+    assert lib.cp_spec_init(C.byref(m), C.byref(w), C.byref(_cfg(b)), None, 0, None) == b.E_INVALID
+    assert lib.cp_spec_init(C.byref(m), C.byref(w), C.byref(_cfg(b, verify_window=1)), None, 0, C.byref(ctx)) == b.E_INVALID
+    # null weight pointers are caught before any device call
+    assert lib.cp_spec_init(C.byref(m), C.byref(w), C.byref(_cfg(b)), C.c_void_p(16), 1 << 30, C.byref(ctx)) == b.E_INVALID
+    assert b"aligned" in lib.cp_spec_last_error(None) or b"null" in lib.cp_spec_last_error(None)
+
+
+def test_context_free_calls_reject_bad_arguments(lib):
+    from speculative_decoding_rvq_gb300 import binding as b
+    assert lib.cp_spec_accept_batch(4, 1, 256, 50, 0.9, 1, 0, None, None, None, None, None, None) == b.E_INVALID
+    assert lib.cp_spec_accept_batch(4, 9, 256, 50, 0.9, 1, 0, None, None, None, None, None, None) == b.E_INVALID
+    assert lib.cp_spec_accept_batch(4, 4, 9000, 50, 0.9, 1, 0, None, None, None, None, None, None) == b.E_UNSUPPORTED
+    assert lib.cp_spec_accept_batch(4, 4, 256, 0, 0.9, 1, 0, None, None, None, None, None, None) == b.E_INVALID
+    assert lib.cp_spec_accept_batch(4, 4, 256, 50, 0.9, 1, 2, None, None, None, None, None, None) == b.E_INVALID
+    assert lib.cp_spec_accept_batch(4, 4, 256, 50, 0.9, 1, 0, None, None, None, None, None, None) == b.E_INVALID
+    assert lib.cp_spec_accept_batch(0, 4, 256, 50, 0.9, 1, 0, None, None, None, None, None, None) == b.OK
+    for fn, args in (("cp_spec_decode_frames", (1, 1, 0, None, None, None, None)),
+                     ("cp_spec_round", (None, None, None)),
+                     ("cp_spec_begin_frame", (1, None, None, 0, None)),
+                     ("cp_spec_status_word", (None,)),
+                     ("cp_spec_reset_stats", (None,))):
+        assert getattr(lib, fn)(None, *args) == b.E_INVALID, fn
+    assert lib.cp_spec_launch_count(None) >= 0
+    lib.cp_spec_destroy(None)
