@@ -1,0 +1,379 @@
+#!/usr/bin/env python3
+"""Benchmark: committed RVQ codes/s of the CodePredictor speculative round.
+
+Workload (one step): decode 1000 frames of 1 stream with the bf16
+0.6B-class synthetic CodePredictor (hidden 1024, 5 layers, 16 q / 8 kv heads
+of 128, SwiGLU 3072, vocab 2048, 16 code groups), verify window N = 4,
+top-k 50, temperature 0.9, weights N(0, 0.02) from seed 0, per-frame talker
+hidden N(0, 1) and first code uniform.  Inputs are resident in HBM when the
+timed region starts; weights (220 MB with the lm_heads) exceed the 129 MB
+L2, so no flush is needed between steps.
+
+One JSON line on rank 0.  --impl reference times the CPU oracle (the
+reference arm of this build) on a bounded sample of the same workload.
+Multi-GPU (torchrun): every rank decodes its own replica of the workload
+(streams are independent; no collective on the data path); the timed region
+is bracketed by barriers and the maximum over ranks is reported.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "committed RVQ codes/s (B=1 and batched); verify-pass HBM GB/s vs GB300 peak"
+UNIT = "codes/s"
+FRAMES = 1000
+WINDOW = 4
+TOP_K, TEMP, SEED = 50, 0.9, 1
+
+
+def workload_config(spec, frames, n_streams, window):
+    return {
+        "workload": (f"bf16 0.6B-class CodePredictor (H{spec.hidden}, {spec.n_layers}L, {spec.n_q_heads}q/"
+                     f"{spec.n_kv_heads}kv x{spec.head_dim}, FFN{spec.ffn}, V{spec.vocab}, G{spec.num_code_groups}),"
+                     f" {n_streams} stream x {frames} frames, N={window}, top-k {TOP_K}, T {TEMP}"),
+        "streams": n_streams, "frames": frames, "verify_window": window, "top_k": TOP_K, "temperature": TEMP,
+        "weights": "synthetic N(0,0.02) bf16, seed 0", "inputs": "x ~ N(0,1), c0 ~ U[0,V), seed 1",
+        "l2": "no flush: weights + lm_heads 220 MB > 129 MB L2",
+        "compute": "bf16 weights, fp32 accumulation and activations, fp32 KV cache",
+    }
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.rows = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 8:
+                self.rows.append(parts)
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"]}
+        sm = [float(r[0]) for r in self.rows if r[0].replace(".", "").isdigit()]
+        mx = [float(r[1]) for r in self.rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in self.rows for i in range(4) if r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.rows)}
+
+
+# ------------------------------------------------------------------- peaks
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "speculative_decoding_rvq_gb300", "csrc")
+    for fn in sorted(os.listdir(csrc)):
+        if fn.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, fn), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of the frame kernel from the committed ncu summary, if it
+    was taken on the current kernel sources (else None)."""
+    p = os.path.join(ROOT, "profiles", "frame_kernel_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return d.get("dram_bytes_per_frame")
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, rank, world):
+    import numpy as np
+    import torch
+
+    from speculative_decoding_rvq_gb300 import binding, synth as S
+
+    torch.cuda.set_device(rank % max(torch.cuda.device_count(), 1))
+    spec = S.TTS06B_BF16
+    w = S.gen_weights(spec, 0)
+    dw = binding.weights_to_device(spec, w)
+    frames = args.frames
+    x, c0 = S.gen_frames(spec, 1, frames, seed=SEED)
+    xd, cd = torch.from_numpy(x).cuda(), torch.from_numpy(c0).cuda()
+    cp = binding.CpSpec(spec, dw, args.window, TOP_K, TEMP, SEED, max_streams=1)
+    codes = torch.empty((frames, 1, spec.num_code_groups), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        cp.decode_frames(xd, cd, codes)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    cp.status()
+    cp.reset_stats()
+    l0 = cp.launch_count()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t0 = torch.cuda.Event(enable_timing=True)
+        t1 = torch.cuda.Event(enable_timing=True)
+        t0.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = t0.elapsed_time(t1)
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    launches = cp.launch_count() - l0
+    st = cp.stats()
+    cp.status()
+    codes_total = args.steps * frames * (spec.num_code_groups - 1)
+    if world > 1:
+        t = torch.tensor([total_ms], device="cuda")
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = codes_total * world / (total_ms / 1e3)
+
+    peak, peak_kind = measured_peaks()
+    per_launch_bytes = (st["weight_bytes"] + st["kv_bytes"]) / args.steps
+    mean_launch_s = statistics.mean(launch_ms) / 1e3
+    achieved = per_launch_bytes / mean_launch_s / 1e9
+    traffic_pf = recorded_traffic()
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                "traffic": (round(traffic_pf * frames) if traffic_pf else None),
+                "kernel": "frame_kernel<bf16> (one cooperative launch per step)",
+                "algorithmic_bytes_per_launch": int(per_launch_bytes),
+                "mean_launch_ms": round(statistics.mean(launch_ms), 3)}
+    passes = st["passes"] / args.steps
+    rounds = st["rounds"] / args.steps
+    result = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": dict(workload_config(spec, frames, 1, args.window), parallelism=f"replicas x{world}"),
+        "roofline": roofline, "gpu_launches": int(launches),
+        "decode": {"passes_per_frame": round(passes / frames, 3),
+                   "codes_per_round": round((frames * (spec.num_code_groups - 2)) / max(rounds, 1), 3),
+                   "accepted_by_offset": st["accepted_by_offset"][1:args.window],
+                   "drafted_by_offset": st["drafted_by_offset"][1:args.window],
+                   "us_per_pass": round(mean_launch_s * 1e6 / passes, 2),
+                   "heads_per_pass": round(st["heads_applied"] / st["passes"], 2)},
+        "clocks": clk.summary(),
+    }
+
+    # end to end through the C ABI with host buffers: pinned H2D of the step's
+    # inputs, decode, D2H of the codes, every step
+    xh = torch.from_numpy(x).pin_memory()
+    ch = torch.from_numpy(c0).pin_memory()
+    out_h = torch.empty((frames, 1, spec.num_code_groups), dtype=torch.int32).pin_memory()
+    for _ in range(2):
+        xd.copy_(xh, non_blocking=True); cd.copy_(ch, non_blocking=True); step()
+        out_h.copy_(codes, non_blocking=True)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e_steps = max(2, args.steps // 2)
+    e0.record(stream)
+    for _ in range(e_steps):
+        xd.copy_(xh, non_blocking=True)
+        cd.copy_(ch, non_blocking=True)
+        step()
+        out_h.copy_(codes, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1)
+    result["e2e"] = {"value": round(e_steps * frames * (spec.num_code_groups - 1) / (e_ms / 1e3), 1), "unit": UNIT,
+                     "h2d_bytes_per_step": int(xh.numel() * 4 + ch.numel() * 4),
+                     "d2h_bytes_per_step": int(out_h.numel() * 4)}
+
+    if rank == 0 and not args.no_sweep:
+        result["sweep"] = sweep(cp_factory=lambda n: binding.CpSpec(spec, dw, n, TOP_K, TEMP, SEED, 1),
+                                xd=xd[:200], cd=cd[:200], G=spec.num_code_groups, peak=peak)
+        result["accept_microbench"] = accept_microbench(peak)
+    return result
+
+
+def sweep(cp_factory, xd, cd, G, peak):
+    """codes/s and per-pass time for the AR loop (N=0) and windows 2..8 on 200 frames."""
+    import torch
+    out = {}
+    F = xd.shape[0]
+    for n in (0, 2, 3, 4, 5, 6, 7, 8):
+        cp = cp_factory(n)
+        codes = torch.empty((F, 1, G), dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            cp.decode_frames(xd, cd, codes)
+        torch.cuda.synchronize()
+        cp.reset_stats()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        reps = 3
+        a.record()
+        for _ in range(reps):
+            cp.decode_frames(xd, cd, codes)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        st = cp.stats()
+        passes = st["passes"] / reps
+        out[f"N{n}"] = {"codes_per_s": round(F * (G - 1) / (ms / 1e3), 1), "passes_per_frame": round(passes / F, 3),
+                        "us_per_pass": round(ms * 1e3 / passes, 2),
+                        "hbm_frac": round((st["weight_bytes"] + st["kv_bytes"]) / reps / (ms / 1e3) / 1e9 / peak, 4)}
+        cp.close()
+    return out
+
+
+def accept_microbench(peak):
+    """Acceptance kernels alone: 65536 rounds, V 2048, rho 0.7, top-k 50, T 0.9 (logit mode)."""
+    import torch
+    from speculative_decoding_rvq_gb300 import binding
+    R, V = 65536, 2048
+    res = {}
+    g = torch.Generator(device="cuda").manual_seed(1)
+    for N in (2, 4, 8):
+        tgt = torch.randn((R, N, V), device="cuda", generator=g) * 3.0
+        drf = 0.7 * tgt[:, : N - 1] + (1 - 0.49) ** 0.5 * torch.randn((R, N - 1, V), device="cuda", generator=g) * 3.0
+        drf = drf.contiguous()
+        for _ in range(3):
+            binding.accept_batch(tgt, drf, TOP_K, TEMP, SEED, 0)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        reps = 5
+        for _ in range(reps):
+            tok, na, _ = binding.accept_batch(tgt, drf, TOP_K, TEMP, SEED, 0)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        gbs = (2 * N - 1) * V * 4 * R / (ms / 1e3) / 1e9
+        res[f"N{N}"] = {"rounds_per_s": round(R / (ms / 1e3), 1), "ms": round(ms, 3), "GB_s": round(gbs, 1),
+                        "hbm_frac": round(gbs / peak, 4),
+                        "mean_accepted": round(float(na.float().mean().item()), 4)}
+        del tgt, drf
+    return res
+
+
+# ------------------------------------------------------------ CPU baselines
+def oracle_codes_per_s(frames: int, window: int):
+    """The CPU oracle (single-threaded C, float64 forward) on `frames` frames of the workload."""
+    from oracle import oracle as O
+    from speculative_decoding_rvq_gb300 import synth as S
+    spec = S.TTS06B_BF16
+    w = S.gen_weights(spec, 0)
+    m = O.Model(spec, w)
+    x, c0 = S.gen_frames(spec, 1, frames, seed=SEED)
+    t = time.perf_counter()
+    m.decode_frames(window, TOP_K, TEMP, SEED, x, c0)
+    dt = time.perf_counter() - t
+    return frames * (spec.num_code_groups - 1) / dt, dt
+
+
+def cpu_baseline_entry(frames=3):
+    v, dt = oracle_codes_per_s(frames, WINDOW)
+    return {"value": round(v, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{frames} frames of the 1-stream workload (N={WINDOW}), {dt:.1f} s single-threaded"}
+
+
+def run_reference(args, rank, world):
+    spec_frames = max(1, args.ref_frames)
+    times = []
+    for _ in range(args.warmup if args.warmup < 1 else 1):
+        oracle_codes_per_s(1, WINDOW)
+    vals = []
+    for _ in range(args.steps):
+        v, dt = oracle_codes_per_s(spec_frames, WINDOW)
+        vals.append(v)
+        times.append(dt)
+    from speculative_decoding_rvq_gb300 import synth as S
+    value = statistics.mean(vals)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(times), 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": dict(workload_config(S.TTS06B_BF16, FRAMES, 1, WINDOW), parallelism="cpu oracle, 1 thread"),
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{spec_frames} frames per step of the 1-stream workload"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--frames", type=int, default=FRAMES)
+    ap.add_argument("--window", type=int, default=WINDOW)
+    ap.add_argument("--ref-frames", type=int, default=2)
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args, rank, world)), flush=True)
+        return
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    res = run_gpu(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            res["cpu_baseline"] = cpu_baseline_entry()
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()
