@@ -131,6 +131,11 @@ typedef struct {
   int64_t drafted_by_offset[9];
   int64_t accepted_by_offset[9];
   int64_t weight_bytes, kv_bytes, heads_applied;
+  /* Critical-path nanoseconds per pass phase, measured on the GPU between
+   * grid barriers: [0] QKV+RoPE+KV append, [1] attention, [2] O projection,
+   * [3] RMSNorm+gate/up+SwiGLU, [4] down projection, [5] lm_heads,
+   * [6] top-k/softmax, [7] accept/commit/stage. */
+  int64_t phase_ns[8];
 } cp_spec_stats;
 
 typedef struct cp_spec_ctx cp_spec_ctx;

@@ -37,6 +37,7 @@ struct Control {
   unsigned long long bar;            // grid barrier counter, zeroed before each launch
   unsigned long long head_mask[2];   // lm_heads needed by the next pass (double-buffered by pass parity)
   long long weight_bytes, kv_bytes, heads_applied, passes;
+  long long phase_ns[8];             // critical-path ns per phase kind (CTA 0)
   int active;                        // streams with frames left
   int pass_global;                   // passes run since init (parity of head_mask)
   int status;                        // device status word (cp_spec_status values)
@@ -51,9 +52,12 @@ struct FrameParams {
   int N;    // verify window (0 = autoregressive)
   int NS;   // row slots per stream = max(N, 2)
   int ND;   // draft logit slots per row = max(N - 1, 0)
-  int KC;   // list capacity = min(max top_k, V)
+  int KC;   // list capacity = min(max top_k, V) rounded up to a multiple of 4
   int RB;   // activation rows per GEMV chunk
   int proc_warps;  // warps per CTA that run the top-k phase
+  int accept_warps;  // warps per CTA that own streams in the accept phase
+  int attn_warps;    // warps per CTA that run attention items
+  int slot_bytes;    // bytes of each of the two weight-stream slots
   unsigned long long seed;
   unsigned long long timeout_ns;
   long long layer_bytes, head_bytes;  // algorithmic bytes per layer / per lm_head
@@ -105,6 +109,13 @@ struct FrameParams {
   float* t_logits;       // [B][P-1][V]
   float* t_draft;        // [B][P-1][ND][V] or null
 };
+
+// Per-warp shared scratch of the accept phase: the stream state plus 2*NS
+// staged probability lists (index and probability arrays of capacity KC)
+// and their lengths.
+inline __host__ __device__ size_t accept_scratch_bytes(int NS, int KC) {
+  return (sizeof(StreamState) + (size_t)2 * NS * KC * 8 + (size_t)2 * NS * 4 + 15) / 16 * 16;
+}
 
 // Workspace carve-up, computed identically by the host for sizing.
 struct Layout {

@@ -61,6 +61,14 @@ struct CtaShared {
   int nrows;
   int nheads;
   int heads[CP_SPEC_MAX_CODE_GROUPS];
+  const int* rpos;  // positions of the active rows (shared memory, parallel to the row list)
+  int kind, layer;  // GEMV phase to run (read at run time so the code is not cloned per phase)
+  // weight stream (thread 0 produces; every thread tracks `consumed` itself)
+  uint64_t wbar[2];     // one mbarrier per shared-memory slot
+  int issued;           // tiles issued since kernel start
+  int cur_w, cur_t;     // next tile to issue: launch-relative weight phase, tile within it
+  int pass;             // pass being run (launch-relative)
+  int wok;              // verdict of the last slot wait
 };
 
 // Pair p of a GEMV phase -> the two weight rows it reads.
@@ -125,137 +133,242 @@ __device__ __forceinline__ void cta_pair_range(int np, int& p0, int& p1) {
   p1 = (int)(((long long)np * (blockIdx.x + 1)) / gridDim.x);
 }
 
-// Issue bulk L2 prefetches for this CTA's share of a weight phase.
+// ------------------------------------------------------- weight stream
+// Each CTA streams its share of every weight phase into a ring of two
+// shared-memory slots with 1-D TMA bulk copies; a slot is refilled with the
+// next tile of the sequence (phases of this pass, then the next pass) as soon
+// as it is consumed, so weights arrive while earlier phases and barriers run.
+// A tile is a run of whole pairs.  Layouts in a slot: "split" (QKV, gate/up):
+// first-row block then second-row block; "adjacent" (O, down, lm_heads): the
+// two rows of a pair are neighbours, as in global memory.
+
 template <typename WT>
-__device__ __noinline__ void prefetch_phase(const FrameParams& P, int kind, int l, const CtaShared& cs) {
-  if (threadIdx.x != 0) return;
-  const int np = gemv_pairs(P, kind, cs);
+__device__ __forceinline__ int pair_row_bytes(const FrameParams& P, int kind) {
+  return gemv_K(P, kind) * (int)sizeof(WT);
+}
+
+template <typename WT>
+__device__ __forceinline__ int pairs_per_tile(const FrameParams& P, int kind) {
+  return max(1, P.slot_bytes / (2 * pair_row_bytes<WT>(P, kind)));
+}
+
+template <typename WT>
+__device__ __forceinline__ int phase_tiles(const FrameParams& P, const CtaShared& cs, int kind) {
   int p0, p1;
-  cta_pair_range(np, p0, p1);
-  const size_t rb = (size_t)gemv_K(P, kind) * sizeof(WT);
-  for (int which = 0; which < 2; ++which) {
-    const char* start = nullptr;
-    size_t len = 0;
-    for (int p = p0; p < p1; ++p) {
-      const WT *w0, *w1;
-      pair_rows<WT>(P, kind, l, p, cs, w0, w1);
-      const char* r = (const char*)(which ? w1 : w0);
-      if (kind == kO || kind == kDown || kind == kHeads) {  // both rows adjacent: one range
-        if (which) break;
-        const char* r0 = (const char*)w0;
-        if (start && r0 == start + len) { len += 2 * rb; continue; }
-        if (start) prefetch_l2(start, (uint32_t)len);
-        start = r0; len = 2 * rb;
-        continue;
+  cta_pair_range(gemv_pairs(P, kind, cs), p0, p1);
+  const int ppt = pairs_per_tile<WT>(P, kind);
+  return p1 > p0 ? (p1 - p0 + ppt - 1) / ppt : 0;
+}
+
+template <typename WT>
+__device__ __forceinline__ void tile_pairs(const FrameParams& P, const CtaShared& cs, int kind, int t, int& pa, int& pb) {
+  int p0, p1;
+  cta_pair_range(gemv_pairs(P, kind, cs), p0, p1);
+  const int ppt = pairs_per_tile<WT>(P, kind);
+  pa = p0 + t * ppt;
+  pb = min(p1, pa + ppt);
+}
+
+__device__ __forceinline__ void weight_phase_of(const FrameParams& P, int w, int& kind, int& l) {
+  const int idx = w % (4 * P.L + 1);
+  if (idx == 4 * P.L) { kind = kHeads; l = 0; }
+  else { kind = idx % 4; l = idx / 4; }
+}
+
+__device__ __forceinline__ unsigned char* slot_base(const FrameParams& P, unsigned char* slots, int slot) {
+  return slots + (size_t)slot * P.slot_bytes;
+}
+
+// Thread 0: issue the bulk copies of tile (kind, l, t) into `slot`.
+template <typename WT>
+__device__ __noinline__ void issue_tile(const FrameParams& P, CtaShared& cs, unsigned char* slots, int slot, int kind,
+                                        int l, int t) {
+  int pa, pb;
+  tile_pairs<WT>(P, cs, kind, t, pa, pb);
+  const int n = pb - pa;
+  const size_t K = (size_t)gemv_K(P, kind);
+  const uint32_t rb = (uint32_t)(K * sizeof(WT));
+  unsigned char* dst = slot_base(P, slots, slot);
+  uint64_t* bar = &cs.wbar[slot];
+  mbar_arrive_expect_tx(bar, 2u * rb * (uint32_t)n);
+  switch (kind) {
+    case kQKV: {  // pair (head hh, e): rows hh*d + e (first block) and hh*d + e + d/2 (second block)
+      const int half = P.d / 2;
+      for (int hh = pa / half; hh * half < pb; ++hh) {
+        const int e0 = max(pa - hh * half, 0), e1 = min(pb - hh * half, half);
+        const WT* base;
+        int hr;
+        if (hh < P.nq) { base = (const WT*)P.wq[l]; hr = hh; }
+        else if (hh < P.nq + P.nkv) { base = (const WT*)P.wk[l]; hr = hh - P.nq; }
+        else { base = (const WT*)P.wv[l]; hr = hh - P.nq - P.nkv; }
+        const int off = hh * half + e0 - pa;
+        bulk_copy_g2s(dst + (size_t)off * rb, base + ((size_t)hr * P.d + e0) * K, (uint32_t)(e1 - e0) * rb, bar);
+        bulk_copy_g2s(dst + (size_t)(n + off) * rb, base + ((size_t)hr * P.d + e0 + half) * K,
+                      (uint32_t)(e1 - e0) * rb, bar);
       }
-      if (start && r == start + len) { len += rb; continue; }
-      if (start) prefetch_l2(start, (uint32_t)len);
-      start = r; len = rb;
+      break;
     }
-    if (start) prefetch_l2(start, (uint32_t)len);
+    case kGU:
+      bulk_copy_g2s(dst, (const WT*)P.w_gate[l] + (size_t)pa * K, (uint32_t)n * rb, bar);
+      bulk_copy_g2s(dst + (size_t)n * rb, (const WT*)P.w_up[l] + (size_t)pa * K, (uint32_t)n * rb, bar);
+      break;
+    case kO:
+      bulk_copy_g2s(dst, (const WT*)P.wo[l] + (size_t)(2 * pa) * K, 2u * (uint32_t)n * rb, bar);
+      break;
+    case kDown:
+      bulk_copy_g2s(dst, (const WT*)P.w_down[l] + (size_t)(2 * pa) * K, 2u * (uint32_t)n * rb, bar);
+      break;
+    default: {  // lm_heads: features 2pa .. 2pb of the needed-head list, one copy per head
+      const int f0 = 2 * pa, f1 = 2 * pb;
+      for (int hi = f0 / P.V; hi * P.V < f1; ++hi) {
+        const int v0 = max(f0 - hi * P.V, 0), v1 = min(f1 - hi * P.V, P.V);
+        bulk_copy_g2s(dst + (size_t)(hi * P.V + v0 - f0) * rb,
+                      (const WT*)P.head + ((size_t)(cs.heads[hi] - 1) * P.V + v0) * K, (uint32_t)(v1 - v0) * rb, bar);
+      }
+    }
   }
 }
 
-// Stage activation rows into shared memory (optionally RMS-normalised).
-// bf16 weights use a split layout: element k of a row goes to half
-// (k & 7) >> 2, slot 4*(k >> 3) + (k & 3), so a lane's 8-element chunk is
-// two conflict-free float4 reads.
+// Thread 0: keep both slots filled.  `consumed` tiles have been released.
+// The lm_head tiles of a later pass are never issued early (their heads are
+// only known once that pass starts).
+template <typename WT>
+__device__ __noinline__ void refill_slots(const FrameParams& P, CtaShared& cs, unsigned char* slots, int consumed) {
+  if (threadIdx.x != 0) return;
+  const int per_pass = 4 * P.L + 1;
+  int guard = 0;
+  while (cs.issued - consumed < 2 && guard++ < 2 * per_pass + 4) {
+    int kind, l;
+    weight_phase_of(P, cs.cur_w, kind, l);
+    if (kind == kHeads && cs.cur_w / per_pass != cs.pass) break;
+    const int nt = phase_tiles<WT>(P, cs, kind);
+    if (cs.cur_t >= nt) { cs.cur_w += 1; cs.cur_t = 0; continue; }
+    issue_tile<WT>(P, cs, slots, cs.issued & 1, kind, l, cs.cur_t);
+    cs.issued += 1;
+    cs.cur_t += 1;
+  }
+}
+
+// Stage activation rows into shared memory (optionally RMS-normalised) in
+// one round trip: every thread issues 16-byte cp.async copies, then each
+// warp normalises its rows in place.  bf16 weights use a split layout:
+// element k of a row goes to half (k & 7) >> 2, slot 4*(k >> 3) + (k & 3),
+// so a lane's 8-element weight chunk meets two conflict-free float4 reads.
+// Must be called by the whole CTA.
 template <typename WT>
 __device__ void stage_rows(const FrameParams& P, const float* src, int ld, int K, const float* gain,
                            const int* rows, int nr, float* xs) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int r = warp; r < nr; r += kWarps) {
-    const float* s = src + (size_t)rows[r] * ld;
-    float inv = 1.0f;
-    if (gain) {
+  constexpr bool split = WTraits<WT>::EPC == 8;
+  const int n4 = K >> 2;
+  for (int i = threadIdx.x; i < nr * n4; i += kThreads) {
+    const int r = i / n4, k = (i - r * n4) << 2;
+    float* dst = xs + (size_t)r * K + (split ? ((k & 7) >> 2) * (K >> 1) + 4 * (k >> 3) : k);
+    cp_async16(dst, src + (size_t)rows[r] * ld + k);
+  }
+  cp_async_wait_all();
+  __syncthreads();
+  if (gain) {
+    for (int r = warp; r < nr; r += kWarps) {
+      float* x = xs + (size_t)r * K;
       float ss = 0.0f;
-      for (int k = lane * 4; k < K; k += 128) {
-        const float4 v = __ldcg(reinterpret_cast<const float4*>(s + k));
+      for (int i = lane * 4; i < K; i += 128) {
+        const float4 v = *reinterpret_cast<const float4*>(x + i);
         ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
       }
       ss = warp_sum(ss);
-      inv = 1.0f / sqrtf(ss / (float)K + P.eps);
-    }
-    float* dst = xs + (size_t)r * K;
-    for (int k = lane * 4; k < K; k += 128) {
-      float4 v = __ldcg(reinterpret_cast<const float4*>(s + k));
-      if (gain) {
+      const float inv = 1.0f / sqrtf(ss / (float)K + P.eps);
+      for (int i = lane * 4; i < K; i += 128) {
+        // smem slot i holds element k of the row
+        const int k = split ? (8 * ((i % (K >> 1)) >> 2) + 4 * (i / (K >> 1))) : i;
         const float4 g = __ldg(reinterpret_cast<const float4*>(gain + k));
+        float4 v = *reinterpret_cast<const float4*>(x + i);
         v.x = v.x * inv * g.x; v.y = v.y * inv * g.y; v.z = v.z * inv * g.z; v.w = v.w * inv * g.w;
-      }
-      if (WTraits<WT>::EPC == 8) {
-        const int c = k >> 3, hf = (k & 7) >> 2;
-        *reinterpret_cast<float4*>(dst + hf * (K / 2) + 4 * c) = v;
-      } else {
-        *reinterpret_cast<float4*>(dst + k) = v;
+        *reinterpret_cast<float4*>(x + i) = v;
       }
     }
+    __syncthreads();
   }
 }
 
-// Partial dot products of two weight rows with nr staged rows over chunks
-// [cb, ce) (16-byte chunks), lanes striding by 32 chunks.
-template <typename WT, int RB>
-__device__ __forceinline__ void gemv_pair_partial(const WT* __restrict__ w0, const WT* __restrict__ w1,
-                                                  const float* xs, int K, int nr, int cb, int ce,
-                                                  float (&a0)[RB], float (&a1)[RB]) {
+// A GEMV task is (pair, K-slice): one warp, at most kU 16-byte chunks of
+// each of the pair's two weight rows per lane (lane owns chunks cb + lane +
+// 32 j), held in registers as floats.
+constexpr int kU = 4;
+
+template <typename WT>
+struct PairChunks {
+  float w0[kU][WTraits<WT>::EPC], w1[kU][WTraits<WT>::EPC];
+};
+
+// Load this lane's chunks of a pair's two rows from a shared-memory tile.
+template <typename WT>
+__device__ __forceinline__ void gemv_load_task(const WT* r0, const WT* r1, int cb, int ce, uint4 (&u0)[kU],
+                                               uint4 (&u1)[kU]) {
   constexpr int EPC = WTraits<WT>::EPC;
   const int lane = threadIdx.x & 31;
 #pragma unroll
-  for (int r = 0; r < RB; ++r) { a0[r] = 0.0f; a1[r] = 0.0f; }
-  constexpr int U = 4;
-  for (int c0 = cb + lane; c0 < ce; c0 += 32 * U) {
-    uint4 u0[U], u1[U];
-#pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const int c = c0 + 32 * j;
-      if (c < ce) { u0[j] = ldg_stream(w0 + (size_t)c * EPC); u1[j] = ldg_stream(w1 + (size_t)c * EPC); }
+  for (int j = 0; j < kU; ++j) {
+    const int c = cb + lane + 32 * j;
+    u0[j] = make_uint4(0, 0, 0, 0);
+    u1[j] = u0[j];
+    if (c < ce) {
+      u0[j] = *reinterpret_cast<const uint4*>(r0 + (size_t)c * EPC);
+      u1[j] = *reinterpret_cast<const uint4*>(r1 + (size_t)c * EPC);
     }
+  }
+}
+
+// Dot products of the task's chunks with staged rows 0..nr-1 (runtime loop,
+// fixed (chunk, element) accumulation order), reduced over the warp; lane 0
+// stores the two sums of row r at red[r] and red[RBS + r].
+template <typename WT>
+__device__ __noinline__ void gemv_task_rows(const uint4 (&u0)[kU], const uint4 (&u1)[kU], int cb, int ce,
+                                            const float* xs, int K, int nr, float* red, int RBS) {
+  constexpr int EPC = WTraits<WT>::EPC;
+  const int lane = threadIdx.x & 31;
+  float f0[kU][EPC], f1[kU][EPC];
 #pragma unroll
-    for (int j = 0; j < U; ++j) {
-      const int c = c0 + 32 * j;
-      if (c >= ce) break;
-      float f0[EPC], f1[EPC];
-      WTraits<WT>::unpack(u0[j], f0);
-      WTraits<WT>::unpack(u1[j], f1);
+  for (int j = 0; j < kU; ++j) { WTraits<WT>::unpack(u0[j], f0[j]); WTraits<WT>::unpack(u1[j], f1[j]); }
+#pragma unroll 1
+  for (int r = 0; r < nr; ++r) {
+    const float* xr = xs + (size_t)r * K;
+    float s0 = 0.0f, s1 = 0.0f;
 #pragma unroll
-      for (int r = 0; r < RB; ++r) {
-        if (r >= nr) break;
-        const float* xr = xs + (size_t)r * K;
+    for (int j = 0; j < kU; ++j) {
+      const int c = cb + lane + 32 * j;
+      if (c < ce) {
         if (EPC == 8) {
           const float4 x0 = *reinterpret_cast<const float4*>(xr + 4 * c);
           const float4 x1 = *reinterpret_cast<const float4*>(xr + K / 2 + 4 * c);
-          float s0 = a0[r], s1 = a1[r];
-          s0 = fmaf(f0[0], x0.x, s0); s0 = fmaf(f0[1], x0.y, s0); s0 = fmaf(f0[2], x0.z, s0); s0 = fmaf(f0[3], x0.w, s0);
-          s0 = fmaf(f0[4], x1.x, s0); s0 = fmaf(f0[5], x1.y, s0); s0 = fmaf(f0[6], x1.z, s0); s0 = fmaf(f0[7], x1.w, s0);
-          s1 = fmaf(f1[0], x0.x, s1); s1 = fmaf(f1[1], x0.y, s1); s1 = fmaf(f1[2], x0.z, s1); s1 = fmaf(f1[3], x0.w, s1);
-          s1 = fmaf(f1[4], x1.x, s1); s1 = fmaf(f1[5], x1.y, s1); s1 = fmaf(f1[6], x1.z, s1); s1 = fmaf(f1[7], x1.w, s1);
-          a0[r] = s0; a1[r] = s1;
+          const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+          for (int e = 0; e < 8; ++e) { s0 = fmaf(f0[j][e], x[e], s0); s1 = fmaf(f1[j][e], x[e], s1); }
         } else {
           const float4 x0 = *reinterpret_cast<const float4*>(xr + 4 * c);
-          float s0 = a0[r], s1 = a1[r];
-          s0 = fmaf(f0[0], x0.x, s0); s0 = fmaf(f0[1], x0.y, s0); s0 = fmaf(f0[2], x0.z, s0); s0 = fmaf(f0[3], x0.w, s0);
-          s1 = fmaf(f1[0], x0.x, s1); s1 = fmaf(f1[1], x0.y, s1); s1 = fmaf(f1[2], x0.z, s1); s1 = fmaf(f1[3], x0.w, s1);
-          a0[r] = s0; a1[r] = s1;
+          const float x[4] = {x0.x, x0.y, x0.z, x0.w};
+#pragma unroll
+          for (int e = 0; e < EPC; ++e) { s0 = fmaf(f0[j][e], x[e], s0); s1 = fmaf(f1[j][e], x[e], s1); }
         }
       }
     }
+    s0 = warp_sum(s0);
+    s1 = warp_sum(s1);
+    if (lane == 0) { red[r] = s0; red[RBS + r] = s1; }
   }
-#pragma unroll
-  for (int r = 0; r < RB; ++r) { a0[r] = warp_sum(a0[r]); a1[r] = warp_sum(a1[r]); }
 }
 
-// Epilogue of one (pair, row): writes the phase's outputs.
+// Epilogue of one (pair, row): writes the phase's outputs.  `pos` is the
+// row's position; `rope` the staged (cos, sin) row of that position (QKV).
 template <typename WT>
-__device__ __forceinline__ void gemv_epilogue(const FrameParams& P, int kind, int l, int p, int row, float y0,
-                                              float y1, const CtaShared& cs) {
+__device__ __noinline__ void gemv_epilogue(const FrameParams& P, int kind, int l, int p, int row, int pos,
+                                              const float2* rope, float y0, float y1, const CtaShared& cs) {
   switch (kind) {
     case kQKV: {
       const int half = P.d / 2, hh = p / half, e = p % half;
-      const int pos = __ldcg(P.row_pos + row);
       const int b = row / P.NS;
       if (hh < P.nq + P.nkv) {
-        const float2 cs2 = P.rope[(size_t)pos * half + e];
+        const float2 cs2 = rope[e];
         const float r0 = y0 * cs2.x - y1 * cs2.y;
         const float r1 = y1 * cs2.x + y0 * cs2.y;
         if (hh < P.nq) {
@@ -285,7 +398,6 @@ __device__ __forceinline__ void gemv_epilogue(const FrameParams& P, int kind, in
     }
     default: {
       const int f = 2 * p, hd = cs.heads[f / P.V], v = f % P.V;
-      const int pos = __ldcg(P.row_pos + row);
       const int slot = hd - pos;
       if (pos >= 1 && slot >= 0 && slot <= P.ND) {
         float* dst = P.logits + ((size_t)row * (1 + P.ND) + slot) * P.V + v;
@@ -295,15 +407,24 @@ __device__ __forceinline__ void gemv_epilogue(const FrameParams& P, int kind, in
   }
 }
 
-template <typename WT, int RB>
-__device__ __noinline__ void gemv_phase(const FrameParams& P, int kind, int l, const CtaShared& cs, const int* rows,
-                           float* uni) {
+// K-split of a GEMV phase: a fixed function of the shapes (never of the row
+// count), so each (row, feature) is reduced in the same order in every pass.
+__device__ __forceinline__ int gemv_ksplit(int nch, int npc) {
+  int KS = 1;
+  while (KS < kWarps && nch > KS * 32 * kU) KS *= 2;                     // <= kU chunks per lane
+  while (KS < kWarps && npc * KS * 2 <= kWarps && nch / (KS * 2) >= 32) KS *= 2;  // fill the warps
+  return KS;
+}
+
+// One GEMV phase over the tiles of this CTA's pair range.  Returns the
+// number of weight tiles it consumed (the caller's running count).
+template <typename WT>
+__device__ __noinline__ int gemv_phase(const FrameParams& P, CtaShared& cs, const int* rows, float* uni,
+                                       unsigned char* slots, int consumed) {
+  const int kind = cs.kind, l = cs.layer;
   const int K = gemv_K(P, kind);
-  const int np = gemv_pairs(P, kind, cs);
-  int p0, p1;
-  cta_pair_range(np, p0, p1);
-  const int npc = p1 - p0;
-  if (npc <= 0 || cs.nrows <= 0) return;
+  const int nt = phase_tiles<WT>(P, cs, kind);
+  if (nt == 0) return consumed;
   const float* src;
   int ld;
   const float* gain;
@@ -316,161 +437,401 @@ __device__ __noinline__ void gemv_phase(const FrameParams& P, int kind, int l, c
   }
   constexpr int EPC = WTraits<WT>::EPC;
   const int nch = K / EPC;
-  // K-split factor: a fixed function of the shapes, never of the row count
-  int KS = 1;
-  while (KS < 8 && npc * KS * 2 <= kWarps && nch / (KS * 2) >= 32) KS *= 2;
-  const int gpr = kWarps / KS;  // groups (pairs) per round
+  const bool split = (kind == kQKV || kind == kGU);
+  const int KS = gemv_ksplit(nch, pairs_per_tile<WT>(P, kind));
+  const int ppr = kWarps / KS;  // pairs per round
+  const int RB = P.RB;
   float* xs = uni;
   float* red = uni + (size_t)RB * K;  // [kWarps][2][RB]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  for (int cb = 0; cb < cs.nrows; cb += RB) {
-    const int nr = min(RB, cs.nrows - cb);
-    __syncthreads();
-    stage_rows<WT>(P, src, ld, K, gain, rows + cb, nr, xs);
-    __syncthreads();
-    for (int g0 = 0; g0 < npc; g0 += gpr) {
-      const int g = g0 + warp / KS, ks = warp % KS;
-      float a0[RB], a1[RB];
-      if (g < npc) {
-        const WT *w0, *w1;
-        pair_rows<WT>(P, kind, l, p0 + g, cs, w0, w1);
-        const int cb_ = (int)(((long long)nch * ks) / KS), ce_ = (int)(((long long)nch * (ks + 1)) / KS);
-        gemv_pair_partial<WT, RB>(w0, w1, xs, K, nr, cb_, ce_, a0, a1);
+  float2* srope = reinterpret_cast<float2*>(red + (size_t)kWarps * 2 * RB);  // [RB][d/2]
+  const int half = P.d / 2;
+  const int warp = threadIdx.x >> 5;
+  const int ks = warp % KS;
+  const int cb = (int)(((long long)nch * ks) / KS), ce = (int)(((long long)nch * (ks + 1)) / KS);
+  const int nchunks = (cs.nrows + RB - 1) / RB;
+  int staged = -1;
+  for (int t = 0; t < nt; ++t) {
+    int pa, pb;
+    tile_pairs<WT>(P, cs, kind, t, pa, pb);
+    const int npt = pb - pa;
+    const int slot = consumed & 1;
+    const WT* tile = reinterpret_cast<const WT*>(slot_base(P, slots, slot));
+    for (int ch = 0; ch < nchunks; ++ch) {
+      const int rb0 = ch * RB, nr = min(RB, cs.nrows - rb0);
+      if (staged != ch) {
+        __syncthreads();  // the previous chunk is done with xs / srope
+        if (kind == kQKV)
+          for (int i = threadIdx.x; i < nr * (half / 2); i += kThreads) {
+            const int r = i / (half / 2), c = i - r * (half / 2);
+            cp_async16(srope + (size_t)r * half + 2 * c, P.rope + (size_t)cs.rpos[rb0 + r] * half + 2 * c);
+          }
+        stage_rows<WT>(P, src, ld, K, gain, rows + rb0, nr, xs);
+        staged = ch;
       }
-      if (KS == 1) {
-        if (g < npc) {
-#pragma unroll
-          for (int r = 0; r < RB; ++r)
-            if (r < nr && lane == r) gemv_epilogue<WT>(P, kind, l, p0 + g, rows[cb + r], a0[r], a1[r], cs);
+      if (ch == 0) {
+        // thread 0 waits (bounded) and publishes the verdict so every thread takes the same path;
+        // the others then observe the completed phase themselves (acquire of the TMA writes)
+        const uint32_t par = (uint32_t)((consumed >> 1) & 1);
+        if (threadIdx.x == 0) cs.wok = mbar_wait_bounded(&cs.wbar[slot], par, &P.ctl->status, P.timeout_ns) ? 1 : 0;
+        __syncthreads();
+        if (!cs.wok) return -1;
+        while (!mbar_try_wait(&cs.wbar[slot], par)) {
         }
-      } else {
-        if (g < npc) {
-#pragma unroll
-          for (int r = 0; r < RB; ++r)
-            if (lane == r) { red[(warp * 2 + 0) * RB + r] = a0[r]; red[(warp * 2 + 1) * RB + r] = a1[r]; }
+      }
+      const int rounds = (npt + ppr - 1) / ppr;
+      for (int rd = 0; rd < rounds; ++rd) {
+        const int g = rd * ppr + warp / KS;  // pair within the tile
+        if (g < npt) {
+          const WT *r0, *r1;
+          if (split) { r0 = tile + (size_t)g * K; r1 = tile + (size_t)(npt + g) * K; }
+          else { r0 = tile + (size_t)(2 * g) * K; r1 = r0 + K; }
+          uint4 u0[kU], u1[kU];
+          gemv_load_task<WT>(r0, r1, cb, ce, u0, u1);
+          gemv_task_rows<WT>(u0, u1, cb, ce, xs, K, nr, red + (size_t)warp * 2 * RB, RB);
         }
         __syncthreads();
-        if (g < npc && ks == 0 && lane < nr) {
+        // finish: sum the K-split partials in order, then the epilogue
+        for (int i = threadIdx.x; i < ppr * nr; i += kThreads) {
+          const int gi = i / nr, r = i - gi * nr;
+          const int gg = rd * ppr + gi;
+          if (gg >= npt) continue;
           float y0 = 0.0f, y1 = 0.0f;
           for (int j = 0; j < KS; ++j) {
-            y0 += red[((warp + j) * 2 + 0) * RB + lane];
-            y1 += red[((warp + j) * 2 + 1) * RB + lane];
+            y0 += red[((gi * KS + j) * 2 + 0) * RB + r];
+            y1 += red[((gi * KS + j) * 2 + 1) * RB + r];
           }
-          gemv_epilogue<WT>(P, kind, l, p0 + g, rows[cb + lane], y0, y1, cs);
+          gemv_epilogue<WT>(P, kind, l, pa + gg, rows[rb0 + r], cs.rpos[rb0 + r], srope + (size_t)r * half, y0, y1, cs);
         }
         __syncthreads();
       }
     }
+    // the slot is free: refill it with the next tile of the sequence
+    ++consumed;
+    refill_slots<WT>(P, cs, slots, consumed);
   }
+  return consumed;
 }
 
 template <typename WT>
-__device__ void gemv_dispatch(const FrameParams& P, int kind, int l, const CtaShared& cs, const int* rows,
-                              float* uni) {
-  switch (P.RB) {
-    case 8: gemv_phase<WT, 8>(P, kind, l, cs, rows, uni); break;
-    case 4: gemv_phase<WT, 4>(P, kind, l, cs, rows, uni); break;
-    case 2: gemv_phase<WT, 2>(P, kind, l, cs, rows, uni); break;
-    default: gemv_phase<WT, 1>(P, kind, l, cs, rows, uni); break;
-  }
+__device__ int gemv_dispatch(const FrameParams& P, int kind, int l, CtaShared& cs, const int* rows, float* uni,
+                             unsigned char* slots, int consumed) {
+  if (threadIdx.x == 0) { cs.kind = kind; cs.layer = l; }
+  __syncthreads();
+  return gemv_phase<WT>(P, cs, rows, uni, slots, consumed);
 }
 
-// Causal GQA attention of every (row, query head) over positions 0..pos.
-__device__ __noinline__ void attention_phase(const FrameParams& P, int l, const CtaShared& cs, const int* rows, float* uni) {
+// Causal GQA attention of every (row, query head) over positions 0..pos,
+// one warp per item.  The query and 16-position blocks of keys and values
+// are staged into warp-private shared memory with cp.async (one memory round
+// trip per block); lane j scores position j of a block, lanes then split the
+// head dimension for the weighted sum.  Orders are fixed for every row.
+__device__ __noinline__ void attention_phase(const FrameParams& P, int l, const CtaShared& cs, const int* rows,
+                                             float* uni) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float* sq = uni + (size_t)warp * (256 + 64);
-  float* sw = sq + 256;
-  const int items = cs.nrows * P.nq;
-  const int grp = P.nq / P.nkv, d = P.d;
+  if (warp >= P.attn_warps) return;
+  const int d = P.d, grp = P.nq / P.nkv;
+  float* sq = uni + (size_t)warp * (33 * d + 64);  // [d] query, [16][d] keys, [16][d] values, [64] scores
+  float* sk = sq + d;
+  float* sv = sk + 16 * d;
+  float* sw = sv + 16 * d;
   const float scale = 1.0f / sqrtf((float)d);
-  for (int it = blockIdx.x * kWarps + warp; it < items; it += gridDim.x * kWarps) {
+  const size_t pos_stride = (size_t)P.nkv * d;
+  const int items = cs.nrows * P.nq;
+  for (int it = blockIdx.x * P.attn_warps + warp; it < items; it += gridDim.x * P.attn_warps) {
     const int r = rows[it / P.nq], hq = it % P.nq, g = hq / grp;
     const int b = r / P.NS;
-    const int pos = __ldcg(P.row_pos + r);
-    const float* qv = P.qbuf + (size_t)r * P.nq * d + (size_t)hq * d;
-    for (int e = lane * 4; e < d; e += 128)
-      *reinterpret_cast<float4*>(sq + e) = __ldcg(reinterpret_cast<const float4*>(qv + e));
-    __syncwarp();
-    const float* kb = P.kv + ((((size_t)b * P.L + l) * 2 + 0) * P.G) * P.nkv * d + (size_t)g * d;
-    const float* vb = P.kv + ((((size_t)b * P.L + l) * 2 + 1) * P.G) * P.nkv * d + (size_t)g * d;
-    float sc[2] = {-INFINITY, -INFINITY};
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj) {
-      const int j = lane + 32 * jj;
-      if (j <= pos) {
-        const float* kj = kb + (size_t)j * P.nkv * d;
-        float s = 0.0f;
+    const int pos = cs.rpos[it / P.nq];
+    const float* kb = P.kv + ((((size_t)b * P.L + l) * 2 + 0) * P.G) * pos_stride + (size_t)g * d;
+    const float* vb = P.kv + ((((size_t)b * P.L + l) * 2 + 1) * P.G) * pos_stride + (size_t)g * d;
+    warp_copy_async(sq, P.qbuf + (size_t)r * P.nq * d + (size_t)hq * d, d * 4);
+    float mx = -INFINITY;
+    for (int j0 = 0; j0 <= pos; j0 += 16) {
+      const int nb = min(16, pos + 1 - j0);
+      for (int jj = 0; jj < nb; ++jj) warp_copy_async(sk + jj * d, kb + (size_t)(j0 + jj) * pos_stride, d * 4);
+      if (j0 == 0)
+        for (int jj = 0; jj < nb; ++jj) warp_copy_async(sv + jj * d, vb + (size_t)jj * pos_stride, d * 4);
+      cp_async_wait_all();
+      __syncwarp();
+      if (lane < nb) {
+        const float* kr = sk + lane * d;
+        float sdot = 0.0f;
+#pragma unroll 4
         for (int e = 0; e < d; e += 4) {
-          const float4 kk = __ldcg(reinterpret_cast<const float4*>(kj + e));
+          const float4 kk = *reinterpret_cast<const float4*>(kr + e);
           const float4 qq = *reinterpret_cast<const float4*>(sq + e);
-          s = fmaf(qq.x, kk.x, s); s = fmaf(qq.y, kk.y, s); s = fmaf(qq.z, kk.z, s); s = fmaf(qq.w, kk.w, s);
+          sdot = fmaf(qq.x, kk.x, sdot); sdot = fmaf(qq.y, kk.y, sdot);
+          sdot = fmaf(qq.z, kk.z, sdot); sdot = fmaf(qq.w, kk.w, sdot);
         }
-        sc[jj] = s * scale;
+        sw[j0 + lane] = sdot * scale;
+      }
+      __syncwarp();
+    }
+    for (int j = 0; j <= pos; ++j) mx = fmaxf(mx, sw[j]);
+    float den = 0.0f;
+    for (int j = 0; j <= pos; ++j) den += expf(sw[j] - mx);  // same order in every lane
+    float4 o[2] = {make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
+    for (int j0 = 0; j0 <= pos; j0 += 16) {
+      const int nb = min(16, pos + 1 - j0);
+      if (j0 > 0) {
+        __syncwarp();
+        for (int jj = 0; jj < nb; ++jj) warp_copy_async(sv + jj * d, vb + (size_t)(j0 + jj) * pos_stride, d * 4);
+        cp_async_wait_all();
+        __syncwarp();
+      }
+      for (int jj = 0; jj < nb; ++jj) {
+        const float w = expf(sw[j0 + jj] - mx) / den;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const int e = 4 * (lane + 32 * c);
+          if (e < d) {
+            const float4 vv = *reinterpret_cast<const float4*>(sv + jj * d + e);
+            o[c].x = fmaf(w, vv.x, o[c].x); o[c].y = fmaf(w, vv.y, o[c].y);
+            o[c].z = fmaf(w, vv.z, o[c].z); o[c].w = fmaf(w, vv.w, o[c].w);
+          }
+        }
       }
     }
-    const float mx = warp_max(fmaxf(sc[0], sc[1]));
-    float ex[2];
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj) ex[jj] = (lane + 32 * jj <= pos) ? expf(sc[jj] - mx) : 0.0f;
-    const float den = warp_sum(ex[0] + ex[1]);
-#pragma unroll
-    for (int jj = 0; jj < 2; ++jj)
-      if (lane + 32 * jj <= pos) sw[lane + 32 * jj] = ex[jj] / den;
-    __syncwarp();
     float* ov = P.obuf + (size_t)r * P.nq * d + (size_t)hq * d;
-    for (int e = lane * 4; e < d; e += 128) {
-      float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-      for (int j = 0; j <= pos; ++j) {
-        const float w = sw[j];
-        const float4 vv = __ldcg(reinterpret_cast<const float4*>(vb + (size_t)j * P.nkv * d + e));
-        o.x = fmaf(w, vv.x, o.x); o.y = fmaf(w, vv.y, o.y); o.z = fmaf(w, vv.z, o.z); o.w = fmaf(w, vv.w, o.w);
-      }
-      *reinterpret_cast<float4*>(ov + e) = o;
+#pragma unroll
+    for (int c = 0; c < 2; ++c) {
+      const int e = 4 * (lane + 32 * c);
+      if (e < d) *reinterpret_cast<float4*>(ov + e) = o[c];
     }
     __syncwarp();
   }
 }
 
-// Top-k / temperature / softmax of every (row, slot) vocabulary row.
+// Exclusive block-wide prefix sum of one int per thread (all threads call).
+__device__ __forceinline__ int block_exclusive_scan(int v, int* sscan, int& total) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sscan[warp] = incl;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int w = 0; w < kWarps; ++w) { const int t = sscan[w]; sscan[w] = acc; acc += t; }
+    sscan[kWarps] = acc;
+  }
+  __syncthreads();
+  total = sscan[kWarps];
+  const int r = sscan[warp] + incl - v;
+  __syncthreads();
+  return r;
+}
+
+// One vocabulary row processed by the whole CTA: the same semantics as
+// warp_process_row (z = fl32(logit/T), exact top-k by (z desc, index asc)
+// with an MSB-first radix select, float64 softmax summed in index order).
+// Thread t owns indices [t*E, t*E + E) so the compaction is in index order.
+// Returns the list length.
+__device__ __noinline__ int block_process_row(const float* __restrict__ logits, int V, int k, float T,
+                                              uint32_t* keys, int* sscan, double* ebuf, int* out_idx,
+                                              float* out_prob) {
+  __shared__ uint32_t hist[256];
+  __shared__ uint32_t s_sel[4];
+  __shared__ double s_sum;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  float* row = reinterpret_cast<float*>(keys);
+  // stage the row (16-byte async copies when aligned)
+  int done = 0;
+  if ((((uintptr_t)logits) & 15u) == 0) {
+    done = V & ~3;
+    for (int i = tid * 4; i < done; i += kThreads * 4) cp_async16(row + i, logits + i);
+  }
+  for (int i = done + tid; i < V; i += kThreads) row[i] = __ldcg(logits + i);
+  cp_async_wait_all();
+  __syncthreads();
+  const int E = (V + kThreads - 1) / kThreads;
+  const int i0 = tid * E, i1 = min(V, i0 + E);
+  if (T == 0.0f) {
+    float best = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int i = i0; i < i1; ++i)
+      if (row[i] > best) { best = row[i]; bi = i; }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+    }
+    float* sbest = reinterpret_cast<float*>(sscan + kWarps + 1);
+    int* sbi = sscan + 2 * (kWarps + 1);
+    if (lane == 0) { sbest[warp] = best; sbi[warp] = bi; }
+    __syncthreads();
+    if (tid == 0) {
+      float b = sbest[0];
+      int ix = sbi[0];
+      for (int w = 1; w < kWarps; ++w)
+        if (sbest[w] > b || (sbest[w] == b && sbi[w] < ix)) { b = sbest[w]; ix = sbi[w]; }
+      out_idx[0] = ix;
+      out_prob[0] = 1.0f;
+    }
+    __syncthreads();
+    return 1;
+  }
+  uint32_t kmax = 0;
+  for (int i = i0; i < i1; ++i) {
+    float z = __fdiv_rn(row[i], T);
+    if (z == 0.0f) z = 0.0f;
+    const uint32_t key = float_key(z);
+    keys[i] = key;
+    kmax = max(kmax, key);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  if (lane == 0) sscan[warp] = (int)kmax;
+  __syncthreads();
+  if (tid == 0) {
+    uint32_t m = 0;
+    for (int w = 0; w < kWarps; ++w) m = max(m, (uint32_t)sscan[w]);
+    s_sel[3] = m;
+  }
+  __syncthreads();
+  kmax = s_sel[3];
+  const int kk = k < V ? k : V;
+  uint32_t prefix = 0, mask = 0;
+  int need = kk;
+  bool eq_all = (kk == V);
+  for (int shift = 24; shift >= 0 && !eq_all; shift -= 8) {
+    hist[tid & 255] = 0;
+    __syncthreads();
+    for (int i = i0; i < i1; ++i) {
+      const uint32_t key = keys[i];
+      if ((key & mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1u);
+    }
+    __syncthreads();
+    if (warp == 0) {
+      uint32_t cnt[8];
+      uint32_t chunk = 0;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) { cnt[m] = hist[255 - 8 * lane - m]; chunk += cnt[m]; }
+      uint32_t incl = chunk;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const uint32_t excl = incl - chunk;
+      if (excl < (uint32_t)need && (uint32_t)need <= incl) {
+        uint32_t acc = excl;
+        for (int m = 0; m < 8; ++m) {
+          if (acc + cnt[m] >= (uint32_t)need) { s_sel[0] = 255 - 8 * lane - m; s_sel[1] = acc; s_sel[2] = cnt[m]; break; }
+          acc += cnt[m];
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t bin = s_sel[0], above = s_sel[1], cbin = s_sel[2];
+    need -= (int)above;
+    prefix |= bin << shift;
+    mask |= 0xFFu << shift;
+    if ((int)cbin == need) eq_all = true;
+    __syncthreads();
+  }
+  // rank among keys equal to the threshold (index order), then compaction
+  int n_eq = 0;
+  for (int i = i0; i < i1; ++i) n_eq += ((keys[i] & mask) == prefix);
+  int tot;
+  int eq_before = block_exclusive_scan(n_eq, sscan, tot);
+  int n_sel = 0;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t km = keys[i] & mask;
+    if (km > prefix) ++n_sel;
+    else if (km == prefix) { if (eq_all || eq_before < need) ++n_sel; ++eq_before; }
+  }
+  int sel_before = block_exclusive_scan(n_sel, sscan, tot);
+  eq_before = block_exclusive_scan(n_eq, sscan, tot);
+  const double zmax = (double)key_float(kmax);
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = keys[i];
+    const uint32_t km = key & mask;
+    bool sel = km > prefix;
+    if (km == prefix) { sel = eq_all || eq_before < need; ++eq_before; }
+    if (sel) {
+      out_idx[sel_before] = i;
+      ebuf[sel_before] = exp((double)key_float(key) - zmax);
+      ++sel_before;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    double S = 0.0;
+    for (int p = 0; p < kk; ++p) S = __dadd_rn(S, ebuf[p]);
+    s_sum = S;
+  }
+  __syncthreads();
+  const double S = s_sum;
+  for (int p = tid; p < kk; p += kThreads) out_prob[p] = __double2float_rn(__ddiv_rn(ebuf[p], S));
+  __syncthreads();
+  return kk;
+}
+
+// Top-k / temperature / softmax of every (row, slot) vocabulary row, one CTA
+// per row.
 __device__ __noinline__ void proc_phase(const FrameParams& P, const CtaShared& cs, const int* rows, float* uni) {
-  const int warp = threadIdx.x >> 5;
-  if (warp >= P.proc_warps) return;
-  const size_t per_warp = (size_t)P.V * 4 + 1024 + (size_t)P.KC * 8;
-  unsigned char* base = reinterpret_cast<unsigned char*>(uni) + (size_t)warp * ((per_warp + 15) / 16 * 16);
-  double* ebuf = reinterpret_cast<double*>(base);
-  uint32_t* hist = reinterpret_cast<uint32_t*>(base + (size_t)P.KC * 8);
-  uint32_t* keys = hist + 256;
+  const size_t keys_bytes = ((size_t)P.V * 4 + 15) / 16 * 16;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(uni);
+  int* sscan = reinterpret_cast<int*>(reinterpret_cast<unsigned char*>(uni) + keys_bytes);  // 3*(kWarps+1) ints
+  double* ebuf = reinterpret_cast<double*>(reinterpret_cast<unsigned char*>(uni) + keys_bytes + 128);
   const int slots = 1 + P.ND;
   const int items = cs.nrows * slots;
-  for (int it = blockIdx.x + gridDim.x * warp; it < items; it += gridDim.x * P.proc_warps) {
+  for (int it = blockIdx.x; it < items; it += gridDim.x) {
     const int r = rows[it / slots], t = it % slots;
-    const int pos = __ldcg(P.row_pos + r);
+    const int pos = cs.rpos[it / slots];
     if (pos < 1 || pos + t > P.G - 1) continue;
     const int b = r / P.NS;
-    const int k = P.top_k[b];
-    const float T = P.temp[b];
     const size_t li = (size_t)r * slots + t;
-    const int n = warp_process_row(P.logits + li * P.V, P.V, k, T, keys, hist, ebuf, P.lidx + li * P.KC,
-                                   P.lprob + li * P.KC);
-    if ((threadIdx.x & 31) == 0) P.lcount[li] = n;
+    const int n = block_process_row(P.logits + li * P.V, P.V, P.top_k[b], P.temp[b], keys, sscan, ebuf,
+                                    P.lidx + li * P.KC, P.lprob + li * P.KC);
+    if (threadIdx.x == 0) P.lcount[li] = n;
   }
 }
 
 // ------------------------------------------------------ per-stream logic
-struct WarpScratch {
-  StreamState s;
-};
-
+// Write the input rows of the next pass into the residual buffer: x at
+// position 0, E_{pos-1}(code) otherwise, as float32.  All m rows are gathered
+// together with 16-byte loads, 8 in flight per lane.
 template <typename WT>
-__device__ void stage_input_row(const FrameParams& P, int row, int pos, int code, const float* x) {
+__device__ __noinline__ void stage_input_rows(const FrameParams& P, int b, int pos0, int m, const int* codes_in, const float* x) {
   const int lane = threadIdx.x & 31;
-  float* dst = P.h + (size_t)row * P.H;
-  if (pos == 0) {
-    for (int k = lane * 4; k < P.H; k += 128)
-      *reinterpret_cast<float4*>(dst + k) = __ldg(reinterpret_cast<const float4*>(x + k));
-  } else {
-    const WT* e = (const WT*)P.embed + ((size_t)(pos - 1) * P.V + code) * P.H;
-    for (int k = lane; k < P.H; k += 32) dst[k] = WTraits<WT>::load1(e + k);
+  constexpr int EPC = WTraits<WT>::EPC;
+  const int cpr = P.H / EPC;  // 16-byte chunks per embedding row
+  const int total = m * cpr;
+  for (int c0 = lane; c0 < total; c0 += 32 * 8) {
+    uint4 u[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = c0 + 32 * j;
+      if (c < total) {
+        const int i = c / cpr, k = (c - i * cpr) * EPC, pos = pos0 + i;
+        const void* src;
+        if (pos == 0) src = x + k;  // EPC floats of x: for bf16 two float4 loads below
+        else src = (const WT*)P.embed + ((size_t)(pos - 1) * P.V + codes_in[i]) * P.H + k;
+        u[j] = (pos == 0) ? make_uint4(0, 0, 0, 0) : ldg_stream(src);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int c = c0 + 32 * j;
+      if (c >= total) break;
+      const int i = c / cpr, k = (c - i * cpr) * EPC, pos = pos0 + i;
+      float* dst = P.h + (size_t)(b * P.NS + i) * P.H + k;
+      if (pos == 0) {
+#pragma unroll
+        for (int q = 0; q < EPC; q += 4)
+          *reinterpret_cast<float4*>(dst + q) = __ldg(reinterpret_cast<const float4*>(x + k + q));
+      } else {
+        float f[EPC];
+        WTraits<WT>::unpack(u[j], f);
+#pragma unroll
+        for (int q = 0; q < EPC; q += 4) *reinterpret_cast<float4*>(dst + q) = make_float4(f[q], f[q + 1], f[q + 2], f[q + 3]);
+      }
+    }
   }
 }
 
@@ -487,21 +848,11 @@ __device__ __forceinline__ void mark_heads(const FrameParams& P, int pos0, int m
 
 // Stage the rows of the next pass for stream b (state already updated in S).
 template <typename WT>
-__device__ void stage_pass_rows(const FrameParams& P, int b, StreamState& S, const int* codes_in,
+__device__ __noinline__ void stage_pass_rows(const FrameParams& P, int b, StreamState& S, const int* codes_in,
                                 const float* x, int parity_next) {
   const int lane = threadIdx.x & 31;
-  for (int i = 0; i < P.NS; ++i) {
-    const int row = b * P.NS + i;
-    if (i < S.m) {
-      const int pos = S.pos0 + i;
-      int code = 0;
-      if (pos > 0) code = codes_in[i];
-      if (lane == 0) P.row_pos[row] = pos;
-      stage_input_row<WT>(P, row, pos, code, x);
-    } else if (lane == 0) {
-      P.row_pos[row] = -1;
-    }
-  }
+  if (lane < P.NS) P.row_pos[b * P.NS + lane] = lane < S.m ? S.pos0 + lane : -1;
+  stage_input_rows<WT>(P, b, S.pos0, S.m, codes_in, x);
   if (lane == 0) {
     mark_heads(P, S.pos0, S.m, parity_next);
     const long long kvb = (long long)(S.pos0 + S.m) * P.L * 2 * P.nkv * P.d * (long long)sizeof(float);
@@ -520,7 +871,7 @@ __device__ __forceinline__ int valid_code(const FrameParams& P, int c) {
 // Scalar state fields are written by lane 0 only; every all-lane read of them
 // follows a __syncwarp().
 template <typename WT>
-__device__ void setup_frame(const FrameParams& P, int b, StreamState& S, int frame, int parity_next) {
+__device__ __noinline__ void setup_frame(const FrameParams& P, int b, StreamState& S, int frame, int parity_next) {
   const int lane = threadIdx.x & 31;
   __syncwarp();
   if (lane == 0) {
@@ -542,7 +893,7 @@ __device__ void setup_frame(const FrameParams& P, int b, StreamState& S, int fra
 }
 
 template <typename WT>
-__device__ void setup_teacher_chunk(const FrameParams& P, int b, StreamState& S, int parity_next) {
+__device__ __noinline__ void setup_teacher_chunk(const FrameParams& P, int b, StreamState& S, int parity_next) {
   const int lane = threadIdx.x & 31;
   __syncwarp();
   const int pos0 = S.pos0;
@@ -575,9 +926,36 @@ __device__ __forceinline__ void store_state(const FrameParams& P, int b, const S
   __syncwarp();
 }
 
+// Per-warp view of the accept scratch (see accept_scratch_bytes).
+struct AcceptScratch {
+  StreamState* S;
+  int* idx;    // [2*NS][KC]
+  float* prob; // [2*NS][KC]
+  int* cnt;    // [2*NS]
+};
+
+__device__ __forceinline__ AcceptScratch accept_scratch(const FrameParams& P, float* uni) {
+  const int warp = threadIdx.x >> 5;
+  unsigned char* base = reinterpret_cast<unsigned char*>(uni) + (size_t)warp * accept_scratch_bytes(P.NS, P.KC);
+  AcceptScratch a;
+  a.S = reinterpret_cast<StreamState*>(base);
+  a.idx = reinterpret_cast<int*>(base + sizeof(StreamState));
+  a.prob = reinterpret_cast<float*>(a.idx + (size_t)2 * P.NS * P.KC);
+  a.cnt = reinterpret_cast<int*>(a.prob + (size_t)2 * P.NS * P.KC);
+  return a;
+}
+
+// Issue the async copy of one global list (capacity KC) into scratch slot `slot`.
+__device__ __forceinline__ void stage_list_async(const FrameParams& P, AcceptScratch& A, int slot, const int* gidx,
+                                                 const float* gprob) {
+  warp_copy_async(A.idx + (size_t)slot * P.KC, gidx, P.KC * 4);
+  warp_copy_async(A.prob + (size_t)slot * P.KC, gprob, P.KC * 4);
+}
+
 // After codes up to depth s_new are committed: finish the frame or stage the next pass.
 template <typename WT>
-__device__ void after_commit(const FrameParams& P, int b, StreamState& S, int s_new, int hrow, int parity_next) {
+__device__ __noinline__ void after_commit(const FrameParams& P, int b, AcceptScratch& A, int s_new, int hrow, int parity_next) {
+  StreamState& S = *A.S;
   const int lane = threadIdx.x & 31;
   StreamStats* ss = P.sstats + b;
   __syncwarp();
@@ -609,25 +987,23 @@ __device__ void after_commit(const FrameParams& P, int b, StreamState& S, int s_
   const int R = P.G - 1 - s_new;
   const int n_d = min(P.N - 1, R);
   const int slots = 1 + P.ND;
-  // save the draft distributions q_t = proc(head_{s+t} . h_s): they are the
-  // rows of this pass's speculative draft slots on the row at position s_new
+  // The draft distributions q_t = proc(head_{s+t} . h_s), t = 1..n_d, are
+  // this pass's speculative draft slots on the row at position s_new: stage
+  // them, sample the drafts, and keep them for the next pass's acceptance.
+  int cnt = 0;
+  if (lane < n_d) cnt = __ldcg(P.lcount + (size_t)hrow * slots + 1 + lane);
   for (int t = 1; t <= n_d; ++t) {
     const size_t li = (size_t)hrow * slots + t;
-    const int n = __ldcg(P.lcount + li);
-    const size_t qi = ((size_t)b * P.ND + (t - 1)) * P.KC;
-    for (int j = lane; j < n; j += 32) {
-      P.qidx[qi + j] = __ldcg(P.lidx + li * P.KC + j);
-      P.qprob[qi + j] = __ldcg(P.lprob + li * P.KC + j);
-    }
-    if (lane == 0) P.qcount[(size_t)b * P.ND + (t - 1)] = n;
+    stage_list_async(P, A, t - 1, P.lidx + li * P.KC, P.lprob + li * P.KC);
   }
+  if (lane < n_d) A.cnt[lane] = cnt;
+  cp_async_wait_all();
   __syncwarp();
   if (lane == 0) {
     for (int t = 1; t <= n_d; ++t) {
-      const size_t qi = ((size_t)b * P.ND + (t - 1)) * P.KC;
-      const int n = P.qcount[(size_t)b * P.ND + (t - 1)];
       const float u = philox_uniform(P.seed, (uint32_t)b, (uint32_t)S.frame_abs, (uint32_t)(s_new + t), kDraft);
-      S.drafts[t - 1] = valid_code(P, list_sample(P.qidx + qi, P.qprob + qi, n, u));
+      S.drafts[t - 1] = valid_code(P, list_sample(A.idx + (size_t)(t - 1) * P.KC, A.prob + (size_t)(t - 1) * P.KC,
+                                                  A.cnt[t - 1], u));
     }
     S.s = s_new;
     S.n_d = n_d;
@@ -635,6 +1011,15 @@ __device__ void after_commit(const FrameParams& P, int b, StreamState& S, int s_
     S.pos0 = s_new + 1;
     S.phase = kPhaseSpec;
   }
+  // save q_1..q_{n_d} (16-byte stores) for the next pass's acceptance
+  const int kc4 = P.KC >> 2;
+  for (int i = lane; i < n_d * kc4; i += 32) {
+    const int t = i / kc4, c = i - t * kc4;
+    const size_t qi = ((size_t)b * P.ND + t) * P.KC;
+    reinterpret_cast<int4*>(P.qidx + qi)[c] = reinterpret_cast<const int4*>(A.idx + (size_t)t * P.KC)[c];
+    reinterpret_cast<float4*>(P.qprob + qi)[c] = reinterpret_cast<const float4*>(A.prob + (size_t)t * P.KC)[c];
+  }
+  if (lane < n_d) P.qcount[(size_t)b * P.ND + lane] = A.cnt[lane];
   __syncwarp();
   int codes_in[CP_SPEC_MAX_WINDOW];
   const int m = S.m;
@@ -644,7 +1029,8 @@ __device__ void after_commit(const FrameParams& P, int b, StreamState& S, int s_
 }
 
 template <typename WT>
-__device__ void accept_stream(const FrameParams& P, int b, StreamState& S, int parity_next) {
+__device__ void accept_stream(const FrameParams& P, int b, AcceptScratch& A, int parity_next) {
+  StreamState& S = *A.S;
   const int lane = threadIdx.x & 31;
   load_state(P, b, S);
   if (S.phase == kPhaseDone) return;
@@ -684,20 +1070,45 @@ __device__ void accept_stream(const FrameParams& P, int b, StreamState& S, int p
     store_state(P, b, S);
     return;
   }
+  // Stage the lists this decision reads: the target rows' slot-0 lists
+  // (p_{s+1..s+m}) and, for a speculative round, the saved draft lists q_t.
+  const bool spec = S.phase == kPhaseSpec;
+  const int nl = spec ? S.m + S.n_d : 1;
+  const int row0 = b * P.NS + (S.phase == kPhasePrefill ? 1 : 0);
+  int cnt = 0;
+  if (spec) {
+    if (lane < S.m) cnt = __ldcg(P.lcount + (size_t)(b * P.NS + lane) * slots);
+    else if (lane < nl) cnt = __ldcg(P.qcount + (size_t)b * P.ND + (lane - S.m));
+    for (int i = 0; i < S.m; ++i) {
+      const size_t li = (size_t)(b * P.NS + i) * slots;
+      stage_list_async(P, A, i, P.lidx + li * P.KC, P.lprob + li * P.KC);
+    }
+    for (int t = 0; t < S.n_d; ++t) {
+      const size_t qi = ((size_t)b * P.ND + t) * P.KC;
+      stage_list_async(P, A, S.m + t, P.qidx + qi, P.qprob + qi);
+    }
+  } else {
+    if (lane == 0) cnt = __ldcg(P.lcount + (size_t)row0 * slots);
+    stage_list_async(P, A, 0, P.lidx + (size_t)row0 * slots * P.KC, P.lprob + (size_t)row0 * slots * P.KC);
+  }
+  if (lane < nl) A.cnt[lane] = cnt;
+  cp_async_wait_all();
+  __syncwarp();
+  const int* Li = A.idx;
+  const float* Lp = A.prob;
+  const int KC = P.KC;
   int s_new = 0, hrow = 0;
   if (lane == 0) {
     const uint32_t fr = (uint32_t)S.frame_abs;
     const int s = S.s;
-    if (S.phase == kPhasePrefill || S.phase == kPhaseAR) {
+    if (!spec) {
       const int j = s + 1;  // the pass scored c_j
-      const int row = b * P.NS + (S.phase == kPhasePrefill ? 1 : 0);
-      const size_t li = (size_t)row * slots;
       const float u = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)j, kTarget);
-      const int c = valid_code(P, list_sample<LdCG>(P.lidx + li * P.KC, P.lprob + li * P.KC, __ldcg(P.lcount + li), u));
+      const int c = valid_code(P, list_sample(Li, Lp, A.cnt[0], u));
       S.codes[j] = c;
       P.codes_out[((size_t)S.frame * P.B + b) * P.G + j] = c;
       s_new = j;
-      hrow = row;
+      hrow = row0;
       ss->passes += 1;
     } else {  // speculative round: exact left-to-right acceptance
       const int n_d = S.n_d, m = S.m;
@@ -705,14 +1116,9 @@ __device__ void accept_stream(const FrameParams& P, int b, StreamState& S, int p
       bool rejected = false;
       for (; t <= n_d; ++t) {
         const int y = S.drafts[t - 1];
-        const size_t qi = ((size_t)b * P.ND + (t - 1)) * P.KC;
-        const int nq = P.qcount[(size_t)b * P.ND + (t - 1)];
-        const size_t li = (size_t)(b * P.NS + t - 1) * slots;
-        const int np = __ldcg(P.lcount + li);
-        const int* pi = P.lidx + li * P.KC;
-        const float* pp = P.lprob + li * P.KC;
-        const float qy = list_lookup(P.qidx + qi, P.qprob + qi, nq, y);
-        const float py = list_lookup<LdCG>(pi, pp, np, y);
+        const int qs = m + t - 1, ps = t - 1;  // scratch slots of q_t and p_{s+t}
+        const float qy = list_lookup(Li + (size_t)qs * KC, Lp + (size_t)qs * KC, A.cnt[qs], y);
+        const float py = list_lookup(Li + (size_t)ps * KC, Lp + (size_t)ps * KC, A.cnt[ps], y);
         const float ratio = __fdiv_rn(py, qy);
         ss->drafted[t] += 1;
         const float ua = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + t), kAccept);
@@ -722,8 +1128,9 @@ __device__ void accept_stream(const FrameParams& P, int b, StreamState& S, int p
           continue;
         }
         const float ut = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + t), kTarget);
-        int c = residual_sample<LdCG>(pi, pp, np, P.qidx + qi, P.qprob + qi, nq, ut);
-        if (c < 0) c = list_sample<LdCG>(pi, pp, np, ut);
+        int c = residual_sample(Li + (size_t)ps * KC, Lp + (size_t)ps * KC, A.cnt[ps], Li + (size_t)qs * KC,
+                                Lp + (size_t)qs * KC, A.cnt[qs], ut);
+        if (c < 0) c = list_sample(Li + (size_t)ps * KC, Lp + (size_t)ps * KC, A.cnt[ps], ut);
         S.codes[s + t] = valid_code(P, c);
         rejected = true;
         break;
@@ -732,10 +1139,9 @@ __device__ void accept_stream(const FrameParams& P, int b, StreamState& S, int p
         s_new = s + t;
         ss->rejections += 1;
       } else if (m > n_d) {
-        const size_t li = (size_t)(b * P.NS + n_d) * slots;
         const float ut = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + n_d + 1), kTarget);
         S.codes[s + n_d + 1] =
-            valid_code(P, list_sample<LdCG>(P.lidx + li * P.KC, P.lprob + li * P.KC, __ldcg(P.lcount + li), ut));
+            valid_code(P, list_sample(Li + (size_t)n_d * KC, Lp + (size_t)n_d * KC, A.cnt[n_d], ut));
         ss->bonus += 1;
         s_new = s + n_d + 1;
       } else {
@@ -751,50 +1157,53 @@ __device__ void accept_stream(const FrameParams& P, int b, StreamState& S, int p
   s_new = __shfl_sync(0xffffffffu, s_new, 0);
   hrow = __shfl_sync(0xffffffffu, hrow, 0);
   __syncwarp();
-  after_commit<WT>(P, b, S, s_new, hrow, parity_next);
+  after_commit<WT>(P, b, A, s_new, hrow, parity_next);
   store_state(P, b, S);
 }
 
 template <typename WT>
 __device__ __noinline__ void accept_phase(const FrameParams& P, int parity_next, float* uni, bool setup) {
   const int warp = threadIdx.x >> 5;
-  StreamState& S = reinterpret_cast<WarpScratch*>(uni)[warp].s;
-  for (int b = blockIdx.x + gridDim.x * warp; b < P.B; b += gridDim.x * kWarps) {
+  if (warp >= P.accept_warps) return;
+  AcceptScratch A = accept_scratch(P, uni);
+  StreamState& S = *A.S;
+  for (int b = blockIdx.x + gridDim.x * warp; b < P.B; b += gridDim.x * P.accept_warps) {
     if (setup) {
+      for (int i = threadIdx.x & 31; i < (int)(sizeof(StreamState) / 4); i += 32) reinterpret_cast<int*>(&S)[i] = 0;
+      __syncwarp();
       if (P.mode == kModeTeacher) {
-        for (int i = threadIdx.x & 31; i < (int)(sizeof(StreamState) / 4); i += 32) reinterpret_cast<int*>(&S)[i] = 0;
-        __syncwarp();
         if ((threadIdx.x & 31) == 0) { S.frame_abs = P.first_frame; S.pos0 = 0; }
         setup_teacher_chunk<WT>(P, b, S, parity_next);
       } else {
-        for (int i = threadIdx.x & 31; i < (int)(sizeof(StreamState) / 4); i += 32) reinterpret_cast<int*>(&S)[i] = 0;
-        __syncwarp();
         setup_frame<WT>(P, b, S, 0, parity_next);
       }
       store_state(P, b, S);
     } else {
-      accept_stream<WT>(P, b, S, parity_next);
+      accept_stream<WT>(P, b, A, parity_next);
     }
   }
 }
 
-// Active rows of the pass and the lm_heads it needs, identical in every CTA.
-__device__ __noinline__ void build_pass_lists(const FrameParams& P, int parity, CtaShared& cs, int* rows) {
+// Active rows of the pass, their positions and the lm_heads the pass needs,
+// identical in every CTA (rows[] and rpos[] live in shared memory).
+__device__ __noinline__ void build_pass_lists(const FrameParams& P, int parity, CtaShared& cs, int* rows, int* rpos) {
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     const unsigned lt = (1u << lane) - 1u;
     int n = 0;
     const int total = P.B * P.NS;
+    const unsigned long long mask = __ldcg(&P.ctl->head_mask[parity]);
     for (int j0 = 0; j0 < total; j0 += 32) {
       const int r = j0 + lane;
-      const bool on = r < total && __ldcg(P.row_pos + r) >= 0;
+      const int pos = r < total ? __ldcg(P.row_pos + r) : -1;
+      const bool on = pos >= 0;
       const uint32_t bal = __ballot_sync(0xffffffffu, on);
-      if (on) rows[n + __popc(bal & lt)] = r;
+      if (on) { rows[n + __popc(bal & lt)] = r; rpos[n + __popc(bal & lt)] = pos; }
       n += __popc(bal);
     }
     if (lane == 0) {
       cs.nrows = n;
-      const unsigned long long mask = __ldcg(&P.ctl->head_mask[parity]);
+      cs.rpos = rpos;
       int nh = 0;
       for (int hd = 1; hd < P.G && hd < 64; ++hd)
         if ((mask >> hd) & 1ull) cs.heads[nh++] = hd;
@@ -804,100 +1213,136 @@ __device__ __noinline__ void build_pass_lists(const FrameParams& P, int parity, 
   __syncthreads();
 }
 
-template <typename WT>
-__device__ void prefetch_weight_phase(const FrameParams& P, int w, CtaShared& cs) {
-  const int per_pass = 4 * P.L + 1;
-  const int idx = w % per_pass;
-  if (idx == 4 * P.L) {
-    prefetch_phase<WT>(P, kHeads, 0, cs);
-  } else {
-    const int l = idx / 4, kind = idx % 4;  // kQKV, kO, kGU, kDown
-    prefetch_phase<WT>(P, kind, l, cs);
+// Grid barrier that also charges the elapsed critical-path time since the
+// previous barrier exit to phase `kind` (measured by CTA 0, %globaltimer,
+// accumulated in registers and flushed when the kernel ends).
+struct PhaseClock {
+  uint64_t last;
+  long long ns[8];
+};
+
+__device__ __forceinline__ bool phase_barrier(Control* ctl, unsigned long long& gen, uint64_t timeout_ns, int kind,
+                                              PhaseClock& clk) {
+  if (!grid_barrier(&ctl->bar, &ctl->status, gen, timeout_ns)) return false;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    const uint64_t now = globaltimer_ns();
+    clk.ns[kind] += (long long)(now - clk.last);
+    clk.last = now;
   }
+  return true;
 }
 
 template <typename WT>
-__global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constant__ FrameParams P) {
+__global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constant__ FrameParams Pg) {
+  // The parameter block is copied to shared memory once: every phase reads
+  // its fields through a reference, and a generic reference into the
+  // parameter buffer would become an L2 round trip after each grid barrier
+  // (the barrier's acquire invalidates L1).
+  __shared__ __align__(16) FrameParams sP;
+  {
+    const int4* src = reinterpret_cast<const int4*>(&Pg);
+    int4* dst = reinterpret_cast<int4*>(&sP);
+    for (int i = threadIdx.x; i < (int)(sizeof(FrameParams) / 16); i += kThreads) dst[i] = src[i];
+    if (threadIdx.x == 0)
+      for (size_t i = sizeof(FrameParams) / 16 * 16; i < sizeof(FrameParams); ++i)
+        reinterpret_cast<char*>(&sP)[i] = reinterpret_cast<const char*>(&Pg)[i];
+    __syncthreads();
+  }
+  const FrameParams& P = sP;
   extern __shared__ __align__(16) unsigned char smem_raw[];
-  // dynamic shared memory: [active row list, B*NS ints][phase union region]
+  // dynamic shared memory: [active rows, their positions][2 weight slots][phase union region]
   int* rows = reinterpret_cast<int*>(smem_raw);
-  const size_t rows_bytes = ((size_t)P.B * P.NS * 4 + 15) / 16 * 16;
-  float* uni = reinterpret_cast<float*>(smem_raw + rows_bytes);
+  int* rpos = rows + (size_t)P.B * P.NS;
+  const size_t rows_bytes = ((size_t)P.B * P.NS * 8 + 127) / 128 * 128;
+  unsigned char* slots = smem_raw + rows_bytes;
+  float* uni = reinterpret_cast<float*>(slots + 2 * (size_t)P.slot_bytes);
   __shared__ CtaShared cs;
   Control* ctl = P.ctl;
   unsigned long long gen = 0;
+  PhaseClock clk = {};    // CTA 0: per-phase critical-path time
+  long long n_pass = 0, w_bytes = 0, n_heads = 0;
   const int pass_base = __ldcg(&ctl->pass_global);
-  int pass = 0;
+  int pass = 0, consumed = 0;
+  if (threadIdx.x == 0) {
+    mbar_init(&cs.wbar[0], 1);
+    mbar_init(&cs.wbar[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    cs.issued = 0; cs.cur_w = 0; cs.cur_t = 0; cs.pass = -1; cs.nheads = 0;
+  }
+  __syncthreads();
+  refill_slots<WT>(P, cs, slots, consumed);  // layer-0 weights stream during the setup
   if (P.do_setup) {
     if (blockIdx.x == 0 && threadIdx.x == 0) ctl->active = P.B;
     accept_phase<WT>(P, pass_base & 1, uni, true);
-    if (!grid_barrier(&ctl->bar, &ctl->status, gen, P.timeout_ns)) return;
+    if (!grid_barrier(&ctl->bar, &ctl->status, gen, P.timeout_ns)) goto drain;
   }
-  // Every pass commits at least one code of every unfinished stream, so a
-  // decode needs at most n_frames * (G - 1) passes and a teacher run
-  // ceil(P / NS); anything beyond that is a logic error, reported, not looped.
-  const int pass_cap = P.max_passes > 0 ? P.max_passes
-                       : (P.mode == kModeTeacher ? (P.P + P.NS - 1) / P.NS + 1 : P.n_frames * (P.G - 1) + 1);
-  const int per_pass = 4 * P.L + 1;  // weight phases per pass: 4 per layer + lm_heads
-  int wcur = 0;                      // next weight phase of this launch to prefetch
-  // Prefetch every weight phase up to index `upto` (two phases of lookahead).
-  // A heads phase is only reached by the cursor inside its own pass, when the
-  // pass's head list is known.
-  auto advance = [&](int upto) {
-    for (; wcur <= upto; ++wcur) prefetch_weight_phase<WT>(P, wcur, cs);
-  };
-  for (;;) {
-    if (*(volatile int*)&ctl->active <= 0) break;
-    if (pass >= pass_cap) {
-      if (P.max_passes == 0 && blockIdx.x == 0 && threadIdx.x == 0) raise_status(&ctl->status, kStatusDevice);
-      break;
+  if (blockIdx.x == 0 && threadIdx.x == 0) clk.last = globaltimer_ns();
+  {
+    // Every pass commits at least one code of every unfinished stream, so a
+    // decode needs at most n_frames * (G - 1) passes and a teacher run
+    // ceil(P / NS); anything beyond that is a logic error, reported, not looped.
+    const int pass_cap = P.max_passes > 0 ? P.max_passes
+                         : (P.mode == kModeTeacher ? (P.P + P.NS - 1) / P.NS + 1 : P.n_frames * (P.G - 1) + 1);
+    for (;;) {
+      if (*(volatile int*)&ctl->active <= 0) break;
+      if (pass >= pass_cap) {
+        if (P.max_passes == 0 && blockIdx.x == 0 && threadIdx.x == 0) raise_status(&ctl->status, kStatusDevice);
+        break;
+      }
+      const int parity = (pass_base + pass) & 1;
+      build_pass_lists(P, parity, cs, rows, rpos);
+      if (threadIdx.x == 0) cs.pass = pass;
+      refill_slots<WT>(P, cs, slots, consumed);
+      if (blockIdx.x == 0 && threadIdx.x == 0) {
+        ctl->head_mask[parity ^ 1] = 0ull;
+        n_pass += 1;
+        w_bytes += (long long)P.L * P.layer_bytes + (long long)cs.nheads * P.head_bytes;
+        n_heads += cs.nheads;
+      }
+      for (int l = 0; l < P.L; ++l) {
+        consumed = gemv_dispatch<WT>(P, kQKV, l, cs, rows, uni, slots, consumed);
+        if (consumed < 0 || !phase_barrier(ctl, gen, P.timeout_ns, 0, clk)) goto drain;
+        attention_phase(P, l, cs, rows, uni);
+        if (!phase_barrier(ctl, gen, P.timeout_ns, 1, clk)) goto drain;
+        consumed = gemv_dispatch<WT>(P, kO, l, cs, rows, uni, slots, consumed);
+        if (consumed < 0 || !phase_barrier(ctl, gen, P.timeout_ns, 2, clk)) goto drain;
+        consumed = gemv_dispatch<WT>(P, kGU, l, cs, rows, uni, slots, consumed);
+        if (consumed < 0 || !phase_barrier(ctl, gen, P.timeout_ns, 3, clk)) goto drain;
+        consumed = gemv_dispatch<WT>(P, kDown, l, cs, rows, uni, slots, consumed);
+        if (consumed < 0 || !phase_barrier(ctl, gen, P.timeout_ns, 4, clk)) goto drain;
+      }
+      consumed = gemv_dispatch<WT>(P, kHeads, 0, cs, rows, uni, slots, consumed);
+      if (consumed < 0 || !phase_barrier(ctl, gen, P.timeout_ns, 5, clk)) goto drain;
+      if (P.mode == kModeDecode) {
+        proc_phase(P, cs, rows, uni);
+        if (!phase_barrier(ctl, gen, P.timeout_ns, 6, clk)) goto drain;
+      }
+      accept_phase<WT>(P, parity ^ 1, uni, false);
+      if (!phase_barrier(ctl, gen, P.timeout_ns, 7, clk)) goto drain;
+      ++pass;
     }
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-      ctl->dbg_pass = pass;
-      ctl->dbg_active = *(volatile int*)&ctl->active;
-      ctl->dbg_gen = (int)gen;
-    }
-    const int parity = (pass_base + pass) & 1;
-    build_pass_lists(P, parity, cs, rows);
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-      ctl->head_mask[parity ^ 1] = 0ull;
-      ctl->passes += 1;
-      ctl->weight_bytes += (long long)P.L * P.layer_bytes + (long long)cs.nheads * P.head_bytes;
-      ctl->heads_applied += cs.nheads;
-    }
-    const int wbase = pass * per_pass;
-    for (int l = 0; l < P.L; ++l) {
-      advance(wbase + 4 * l + 2);
-      gemv_dispatch<WT>(P, kQKV, l, cs, rows, uni);
-      if (!grid_barrier(&ctl->bar, &ctl->status, gen, P.timeout_ns)) return;
-      attention_phase(P, l, cs, rows, uni);
-      if (!grid_barrier(&ctl->bar, &ctl->status, gen, P.timeout_ns)) return;
-      advance(wbase + 4 * l + 3);
-      gemv_dispatch<WT>(P, kO, l, cs, rows, uni);
-      if (!grid_barrier(&ctl->bar, &ctl->status, gen, P.timeout_ns)) return;
-      advance(wbase + 4 * l + 4);
-      gemv_dispatch<WT>(P, kGU, l, cs, rows, uni);
-      if (!grid_barrier(&ctl->bar, &ctl->status, gen, P.timeout_ns)) return;
-      advance(wbase + 4 * l + 5);
-      gemv_dispatch<WT>(P, kDown, l, cs, rows, uni);
-      if (!grid_barrier(&ctl->bar, &ctl->status, gen, P.timeout_ns)) return;
-    }
-    advance(wbase + 4 * P.L + 2);
-    gemv_dispatch<WT>(P, kHeads, 0, cs, rows, uni);
-    if (!grid_barrier(&ctl->bar, &ctl->status, gen, P.timeout_ns)) return;
-    if (P.mode == kModeDecode) {
-      proc_phase(P, cs, rows, uni);
-      if (!grid_barrier(&ctl->bar, &ctl->status, gen, P.timeout_ns)) return;
-    }
-    accept_phase<WT>(P, parity ^ 1, uni, false);
-    if (!grid_barrier(&ctl->bar, &ctl->status, gen, P.timeout_ns)) return;
-    ++pass;
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) ctl->pass_global = pass_base + pass;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    ctl->pass_global = pass_base + pass;
+    ctl->passes += n_pass;
+    ctl->weight_bytes += w_bytes;
+    ctl->heads_applied += n_heads;
+    for (int i = 0; i < 8; ++i) ctl->phase_ns[i] += clk.ns[i];
+    ctl->dbg_pass = pass;
+    ctl->dbg_gen = (int)gen;
+  }
+drain:
+  // never leave with a bulk copy in flight into this CTA's shared memory
+  __syncthreads();
+  if (threadIdx.x == 0 && consumed >= 0) {
+    for (int i = consumed; i < cs.issued; ++i)
+      if (!mbar_wait_bounded(&cs.wbar[i & 1], (uint32_t)((i >> 1) & 1), &ctl->status, P.timeout_ns)) break;
+  }
+  __syncthreads();
 }
 
-template __global__ void frame_kernel<float>(const __grid_constant__ FrameParams P);
-template __global__ void frame_kernel<__nv_bfloat16>(const __grid_constant__ FrameParams P);
+template __global__ void frame_kernel<float>(const __grid_constant__ FrameParams Pg);
+template __global__ void frame_kernel<__nv_bfloat16>(const __grid_constant__ FrameParams Pg);
 
 // ------------------------------------------------------------- init kernels
 __global__ void init_tables_kernel(float2* rope, int G, int d, double theta, int* top_k, float* temp, int Bmax,

@@ -29,19 +29,49 @@ struct LdPlain {
   template <typename T> __device__ __forceinline__ static T ld(const T* p) { return *p; }
 };
 
+// Stage a row of V floats from global into warp-private shared memory in
+// one round trip: 16-byte async copies when the row is 16-byte aligned,
+// batched scalar L2 loads for the tail or an unaligned row.
+__device__ __forceinline__ void warp_stage_row(float* dst, const float* __restrict__ src, int V) {
+  const int lane = threadIdx.x & 31;
+  int done = 0;
+  if ((((uintptr_t)src) & 15u) == 0) {
+    done = V & ~3;
+    warp_copy_async(dst, src, done * 4);
+  }
+  for (int i0 = done; i0 < V; i0 += 32 * 8) {
+    float v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + lane + 32 * j;
+      v[j] = i < V ? __ldcg(src + i) : 0.0f;
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int i = i0 + lane + 32 * j;
+      if (i < V) dst[i] = v[j];
+    }
+  }
+  cp_async_wait_all();
+  __syncwarp();
+}
+
 // Processes one row of V float32 logits with one warp.  keys: warp-private
-// scratch of V uint32; hist: warp-private 256 uint32; ebuf: warp-private
-// min(k, V) doubles; out_idx / out_prob: capacity min(k, V) (1 when T == 0).
+// scratch of V uint32 (the row is staged there, then replaced by its keys);
+// hist: warp-private 256 uint32; ebuf: warp-private min(k, V) doubles;
+// out_idx / out_prob: capacity min(k, V) (1 when T == 0).
 // Returns the list length (all lanes).
 static __device__ __noinline__ int warp_process_row(const float* __restrict__ logits, int V, int k, float T,
-                                             uint32_t* keys, uint32_t* hist, double* ebuf, int* out_idx,
-                                             float* out_prob) {
+                                                    uint32_t* keys, uint32_t* hist, double* ebuf, int* out_idx,
+                                                    float* out_prob) {
   const int lane = threadIdx.x & 31;
+  float* row = reinterpret_cast<float*>(keys);
+  warp_stage_row(row, logits, V);
   if (T == 0.0f) {
     float best = -INFINITY;
     int bi = 0x7fffffff;
     for (int i = lane; i < V; i += 32) {
-      const float v = __ldcg(logits + i);
+      const float v = row[i];
       if (v > best || (v == best && i < bi)) { best = v; bi = i; }
     }
 #pragma unroll
@@ -54,10 +84,10 @@ static __device__ __noinline__ int warp_process_row(const float* __restrict__ lo
     __syncwarp();
     return 1;
   }
-  // keys of z = fl32(logit / T); -0 is folded into +0 so ties match float compares
+  // keys of z = fl32(logit / T), in place; -0 is folded into +0 so ties match float compares
   uint32_t kmax = 0;
   for (int i = lane; i < V; i += 32) {
-    float z = __fdiv_rn(__ldcg(logits + i), T);
+    float z = __fdiv_rn(row[i], T);
     if (z == 0.0f) z = 0.0f;
     const uint32_t key = float_key(z);
     keys[i] = key;
@@ -65,6 +95,7 @@ static __device__ __noinline__ int warp_process_row(const float* __restrict__ lo
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) kmax = max(kmax, __shfl_xor_sync(0xffffffffu, kmax, o));
+  __syncwarp();
   const int kk = k < V ? k : V;
   uint32_t prefix = 0, mask = 0;
   int need = kk;
@@ -110,14 +141,18 @@ static __device__ __noinline__ int warp_process_row(const float* __restrict__ lo
     if ((int)cbin == need) eq_all = true;
     __syncwarp();
   }
-  // compaction in ascending index order (strided layout: index = j*32 + lane)
+  // compaction in ascending index order (strided layout: index = j*32 + lane);
+  // each kept entry's exp(z - zmax) is computed in float64 on the way
+  const double zmax = (double)key_float(kmax);
   int base = 0, eq_seen = 0;
   const unsigned lt = (1u << lane) - 1u;
   for (int j0 = 0; j0 < V; j0 += 32) {
     const int i = j0 + lane;
     bool sel = false, eq = false;
+    uint32_t key = 0;
     if (i < V) {
-      const uint32_t km = keys[i] & mask;
+      key = keys[i];
+      const uint32_t km = key & mask;
       sel = km > prefix;
       eq = (km == prefix);
     }
@@ -128,20 +163,12 @@ static __device__ __noinline__ int warp_process_row(const float* __restrict__ lo
     if (sel) {
       const int pos = base + __popc(selb & lt);
       out_idx[pos] = i;
+      ebuf[pos] = exp((double)key_float(key) - zmax);
     }
     base += __popc(selb);
   }
   __syncwarp();
-  // softmax over the kept set: exp in float64, sequential float64 sum in index order
-  const uint32_t mk = kmax;
-  const float zmaxf = __uint_as_float((mk & 0x80000000u) ? (mk & 0x7FFFFFFFu) : ~mk);
-  const double zmax = (double)zmaxf;
-  for (int p = lane; p < kk; p += 32) {
-    const int i = out_idx[p];
-    const float z = __fdiv_rn(__ldcg(logits + i), T);
-    ebuf[p] = exp((double)z - zmax);
-  }
-  __syncwarp();
+  // softmax normalisation: sequential float64 sum in index order
   double S = 0.0;
   if (lane == 0)
     for (int p = 0; p < kk; ++p) S = __dadd_rn(S, ebuf[p]);

@@ -103,31 +103,55 @@ int effective_window(const cp_spec_model* m, const cp_spec_config* cfg) {
   return N;
 }
 
+// List capacity: min(top_k, V) rounded up to a multiple of 4 so every list
+// row is 16-byte aligned for cp.async staging.
+int list_capacity(const cp_spec_model* m, const cp_spec_config* cfg) {
+  const int k = cfg->top_k < m->vocab ? cfg->top_k : m->vocab;
+  return (k + 3) / 4 * 4;
+}
+
 cpk::Layout layout_for(const cp_spec_model* m, const cp_spec_config* cfg, int N) {
-  const int KC = cfg->top_k < m->vocab ? cfg->top_k : m->vocab;
+  const int KC = list_capacity(m, cfg);
   return cpk::make_layout(m->hidden, m->n_layers, m->n_q_heads, m->n_kv_heads, m->head_dim, m->ffn, m->vocab,
                           m->num_code_groups, N, KC, cfg->max_streams);
 }
 
 struct SmemPlan {
-  int RB, proc_warps;
+  int RB, proc_warps, accept_warps, attn_warps, slot_bytes;
   size_t bytes;
 };
 
+constexpr size_t kDynSmemLimit = 216 * 1024;  // dynamic shared memory per CTA (static use is ~7 KB)
+
+// Dynamic shared memory of the frame kernel:
+// [active rows + positions][2 weight-stream slots][union of the phase scratch areas].
 SmemPlan smem_plan(const cp_spec_model* m, int N, int KC, int Bmax) {
   const int NS = N > 2 ? N : 2;
+  const size_t eb = m->dtype == 1 ? 2 : 4;
   const int Kmax = std::max(std::max(m->hidden, m->n_q_heads * m->head_dim), m->ffn);
-  int RB = 8;
-  while (RB > 1 && (size_t)RB * Kmax * 4 > 98304) RB /= 2;
-  const size_t gemv = (size_t)RB * Kmax * 4 + (size_t)cpk::kWarps * 2 * RB * 4;
-  const size_t attn = (size_t)cpk::kWarps * (256 + 64) * 4;
-  const size_t per_warp = ((size_t)m->vocab * 4 + 1024 + (size_t)KC * 8 + 15) / 16 * 16;
-  int pw = (int)std::min<size_t>(cpk::kWarps, std::max<size_t>(1, (size_t)150 * 1024 / per_warp));
-  const size_t proc = per_warp * pw;
-  const size_t acc = (size_t)cpk::kWarps * sizeof(cpk::StreamState);
-  const size_t uni = std::max(std::max(gemv, attn), std::max(proc, acc));
-  const size_t rows = ((size_t)Bmax * NS * 4 + 15) / 16 * 16;
-  return SmemPlan{RB, pw, rows + uni};
+  const size_t rows = ((size_t)Bmax * NS * 8 + 127) / 128 * 128;
+  const size_t pair = ((2 * (size_t)Kmax * eb) + 127) / 128 * 128;
+  size_t slot = std::max<size_t>(pair, 56 * 1024);
+  const size_t per_attn = ((size_t)33 * m->head_dim + 64) * 4;
+  const size_t per_acc = cpk::accept_scratch_bytes(NS, KC);
+  const size_t proc = ((size_t)m->vocab * 4 + 15) / 16 * 16 + 128 + (size_t)KC * 8;
+  SmemPlan best{0, 1, 0, 0, 0, 0};
+  for (; slot >= pair; slot -= 8 * 1024) {
+    if (rows + 2 * slot >= kDynSmemLimit) continue;
+    const size_t budget = kDynSmemLimit - rows - 2 * slot;
+    int RB = 8;
+    auto gemv = [&](int rb) {
+      return (size_t)rb * Kmax * 4 + (size_t)cpk::kWarps * 2 * rb * 4 + (size_t)rb * (m->head_dim / 2) * 8;
+    };
+    while (RB > 1 && gemv(RB) > budget) RB /= 2;
+    const int tw = (int)std::min<size_t>(cpk::kWarps, budget / per_attn);
+    const int aw = (int)std::min<size_t>(cpk::kWarps, budget / per_acc);
+    if (gemv(RB) > budget || tw < 1 || aw < 1 || proc > budget) continue;
+    const size_t uni = std::max(std::max(gemv(RB), per_attn * tw), std::max(proc, per_acc * aw));
+    best = SmemPlan{RB, 1, aw, tw, (int)slot, rows + 2 * slot + uni};
+    break;
+  }
+  return best;
 }
 
 template <typename T>
@@ -180,15 +204,29 @@ cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* w
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   if (e != cudaSuccess) return check_cuda(nullptr, e, "device query");
   if (!coop) return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "device does not support cooperative launches");
-  const int KC = config->top_k < model->vocab ? config->top_k : model->vocab;
+  const int KC = list_capacity(model, config);
   const SmemPlan sp = smem_plan(model, N, KC, config->max_streams);
+  {
+    // a GEMV task keeps at most 8 warps x 32 lanes x 4 chunks of 16 bytes of a row in registers
+    const int epc = model->dtype == 1 ? 8 : 4;
+    const int kmax = std::max(std::max(model->hidden, model->n_q_heads * model->head_dim), model->ffn);
+    if (kmax > cpk::kWarps * 32 * 4 * epc)
+      return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "input width %d above %d for this weight dtype", kmax,
+                  cpk::kWarps * 32 * 4 * epc);
+  }
+  if (sp.bytes == 0)
+    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "shapes do not fit the frame kernel's shared memory (top_k %d, window %d)",
+                config->top_k, config->verify_window);
+  if (sp.accept_warps < 1)
+    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "top_k %d too large for verify window %d (accept lists exceed shared memory)",
+                config->top_k, config->verify_window);
   int maxb = 0;
   e = cpk_host::frame_kernel_config(model->dtype, sp.bytes, &maxb);
   if (e != cudaSuccess) return check_cuda(nullptr, e, "frame kernel attributes");
   if (maxb < 1) return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "frame kernel needs %zu bytes of shared memory per CTA", sp.bytes);
   const int NS = N > 2 ? N : 2;
-  if ((long long)config->max_streams > (long long)sms * cpk::kWarps)
-    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "max_streams above %d (one accept warp per stream)", sms * cpk::kWarps);
+  if ((long long)config->max_streams > (long long)sms * sp.accept_warps)
+    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "max_streams above %d (one accept warp per stream)", sms * sp.accept_warps);
 
   cp_spec_ctx* c = new (std::nothrow) cp_spec_ctx();
   if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "host allocation failed");
@@ -210,6 +248,9 @@ cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* w
   P.F = model->ffn; P.V = model->vocab; P.G = model->num_code_groups; P.dtype = model->dtype;
   P.eps = model->rms_eps;
   P.N = N; P.NS = NS; P.ND = N > 1 ? N - 1 : 0; P.KC = KC; P.RB = sp.RB; P.proc_warps = sp.proc_warps;
+  P.accept_warps = sp.accept_warps;
+  P.attn_warps = sp.attn_warps;
+  P.slot_bytes = sp.slot_bytes;
   P.seed = config->seed;
   P.timeout_ns = kBarrierTimeoutNs;
   const long long eb = model->dtype == 1 ? 2 : 4;
@@ -258,7 +299,8 @@ cp_spec_status cp_spec_set_stream_sampling(cp_spec_ctx* c, int32_t n, const int3
   if (n < 1 || n > c->config.max_streams || !h_top_k || !h_temp)
     return fail(c, CP_SPEC_E_INVALID, "n must be in [1, max_streams] with non-null arrays");
   for (int i = 0; i < n; ++i) {
-    if (h_top_k[i] < 1 || h_top_k[i] > c->base.KC) return fail(c, CP_SPEC_E_INVALID, "stream %d: top_k out of [1, %d]", i, c->base.KC);
+    if (h_top_k[i] < 1 || h_top_k[i] > c->config.top_k)
+      return fail(c, CP_SPEC_E_INVALID, "stream %d: top_k out of [1, %d]", i, c->config.top_k);
     const float T = h_temp[i];
     if (!(T == 0.0f || (T >= 1e-3f && T <= 100.0f))) return fail(c, CP_SPEC_E_INVALID, "stream %d: bad temperature", i);
   }
@@ -395,6 +437,7 @@ cp_spec_status cp_spec_read_stats(cp_spec_ctx* c, cp_spec_stats* out, void* stre
   out->weight_bytes = ctl.weight_bytes;
   out->kv_bytes = ctl.kv_bytes;
   out->heads_applied = ctl.heads_applied;
+  for (int i = 0; i < 8; ++i) out->phase_ns[i] = ctl.phase_ns[i];
   delete[] hs;
   return CP_SPEC_OK;
 }
@@ -404,7 +447,7 @@ cp_spec_status cp_spec_reset_stats(cp_spec_ctx* c, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(c->base.sstats, 0, sizeof(cpk::StreamStats) * c->config.max_streams, s);
   if (e == cudaSuccess)
-    e = cudaMemsetAsync(&c->base.ctl->weight_bytes, 0, 4 * sizeof(long long), s);
+    e = cudaMemsetAsync(&c->base.ctl->weight_bytes, 0, 12 * sizeof(long long), s);
   return check_cuda(c, e, "reset stats");
 }
 
