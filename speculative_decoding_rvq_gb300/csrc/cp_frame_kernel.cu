@@ -69,6 +69,9 @@ struct CtaShared {
   int cur_w, cur_t;     // next tile to issue: launch-relative weight phase, tile within it
   int pass;             // pass being run (launch-relative)
   int wok;              // verdict of the last slot wait
+  // per-kind tile geometry of this CTA (QKV, O, gate/up, down, lm_heads):
+  // pair range [tp0, tp1), pairs per tile, tiles; computed once (lm_heads once per pass)
+  int tp0[5], tp1[5], tppt[5], tnt[5];
 };
 
 // Pair p of a GEMV phase -> the two weight rows it reads.
@@ -129,8 +132,9 @@ __device__ __forceinline__ int gemv_K(const FrameParams& P, int kind) {
 }
 
 __device__ __forceinline__ void cta_pair_range(int np, int& p0, int& p1) {
-  p0 = (int)(((long long)np * blockIdx.x) / gridDim.x);
-  p1 = (int)(((long long)np * (blockIdx.x + 1)) / gridDim.x);
+  // np * gridDim.x stays far below 2^32 for every supported shape
+  p0 = (int)(((unsigned)np * blockIdx.x) / gridDim.x);
+  p1 = (int)(((unsigned)np * (blockIdx.x + 1)) / gridDim.x);
 }
 
 // ------------------------------------------------------- weight stream
@@ -148,25 +152,27 @@ __device__ __forceinline__ int pair_row_bytes(const FrameParams& P, int kind) {
 }
 
 template <typename WT>
-__device__ __forceinline__ int pairs_per_tile(const FrameParams& P, int kind) {
+__device__ __forceinline__ int pairs_per_tile_calc(const FrameParams& P, int kind) {
   return max(1, P.slot_bytes / (2 * pair_row_bytes<WT>(P, kind)));
 }
 
+// Fill the tile table entry of `kind` (thread 0).
 template <typename WT>
-__device__ __forceinline__ int phase_tiles(const FrameParams& P, const CtaShared& cs, int kind) {
+__device__ __noinline__ void tile_table_fill(const FrameParams& P, CtaShared& cs, int kind) {
   int p0, p1;
   cta_pair_range(gemv_pairs(P, kind, cs), p0, p1);
-  const int ppt = pairs_per_tile<WT>(P, kind);
-  return p1 > p0 ? (p1 - p0 + ppt - 1) / ppt : 0;
+  const int ppt = pairs_per_tile_calc<WT>(P, kind);
+  cs.tp0[kind] = p0;
+  cs.tp1[kind] = p1;
+  cs.tppt[kind] = ppt;
+  cs.tnt[kind] = p1 > p0 ? (p1 - p0 + ppt - 1) / ppt : 0;
 }
 
-template <typename WT>
-__device__ __forceinline__ void tile_pairs(const FrameParams& P, const CtaShared& cs, int kind, int t, int& pa, int& pb) {
-  int p0, p1;
-  cta_pair_range(gemv_pairs(P, kind, cs), p0, p1);
-  const int ppt = pairs_per_tile<WT>(P, kind);
-  pa = p0 + t * ppt;
-  pb = min(p1, pa + ppt);
+__device__ __forceinline__ int pairs_per_tile(const CtaShared& cs, int kind) { return cs.tppt[kind]; }
+__device__ __forceinline__ int phase_tiles(const CtaShared& cs, int kind) { return cs.tnt[kind]; }
+__device__ __forceinline__ void tile_pairs(const CtaShared& cs, int kind, int t, int& pa, int& pb) {
+  pa = cs.tp0[kind] + t * cs.tppt[kind];
+  pb = min(cs.tp1[kind], pa + cs.tppt[kind]);
 }
 
 __device__ __forceinline__ void weight_phase_of(const FrameParams& P, int w, int& kind, int& l) {
@@ -184,7 +190,7 @@ template <typename WT>
 __device__ __noinline__ void issue_tile(const FrameParams& P, CtaShared& cs, unsigned char* slots, int slot, int kind,
                                         int l, int t) {
   int pa, pb;
-  tile_pairs<WT>(P, cs, kind, t, pa, pb);
+  tile_pairs(cs, kind, t, pa, pb);
   const int n = pb - pa;
   const size_t K = (size_t)gemv_K(P, kind);
   const uint32_t rb = (uint32_t)(K * sizeof(WT));
@@ -241,7 +247,7 @@ __device__ __noinline__ void refill_slots(const FrameParams& P, CtaShared& cs, u
     int kind, l;
     weight_phase_of(P, cs.cur_w, kind, l);
     if (kind == kHeads && cs.cur_w / per_pass != cs.pass) break;
-    const int nt = phase_tiles<WT>(P, cs, kind);
+    const int nt = phase_tiles(cs, kind);
     if (cs.cur_t >= nt) { cs.cur_w += 1; cs.cur_t = 0; continue; }
     issue_tile<WT>(P, cs, slots, cs.issued & 1, kind, l, cs.cur_t);
     cs.issued += 1;
@@ -257,7 +263,8 @@ __device__ __noinline__ void refill_slots(const FrameParams& P, CtaShared& cs, u
 // Must be called by the whole CTA.
 template <typename WT>
 __device__ void stage_rows(const FrameParams& P, const float* src, int ld, int K, const float* gain,
-                           const int* rows, int nr, float* xs) {
+                           const int* rows, int nr, float* xs, uint64_t* wbar = nullptr, uint32_t wpar = 0,
+                           int* wok = nullptr) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr bool split = WTraits<WT>::EPC == 8;
   const int n4 = K >> 2;
@@ -266,6 +273,9 @@ __device__ void stage_rows(const FrameParams& P, const float* src, int ld, int K
     float* dst = xs + (size_t)r * K + (split ? ((k & 7) >> 2) * (K >> 1) + 4 * (k >> 3) : k);
     cp_async16(dst, src + (size_t)rows[r] * ld + k);
   }
+  // optionally, thread 0 waits (bounded) for a weight tile while the copies fly;
+  // the barrier below publishes its verdict
+  if (wbar && threadIdx.x == 0) *wok = mbar_wait_bounded(wbar, wpar, &P.ctl->status, P.timeout_ns) ? 1 : 0;
   cp_async_wait_all();
   __syncthreads();
   if (gain) {
@@ -319,9 +329,12 @@ __device__ __forceinline__ void gemv_load_task(const WT* r0, const WT* r1, int c
   }
 }
 
-// Dot products of the task's chunks with staged rows 0..nr-1 (runtime loop,
-// fixed (chunk, element) accumulation order), reduced over the warp; lane 0
-// stores the two sums of row r at red[r] and red[RBS + r].
+// Dot products of the task's chunks with staged rows 0..nr-1, four rows at
+// a time with two partial sums per output (16 independent FMA chains per
+// lane), reduced over the warp; lane 0 stores the two sums of row r at
+// red[r] and red[RBS + r].  The accumulation order is fixed: per lane, even
+// chunks and odd chunks separately, each in (chunk, element) order, then
+// even + odd, then a butterfly over the lanes.
 template <typename WT>
 __device__ __noinline__ void gemv_task_rows(const uint4 (&u0)[kU], const uint4 (&u1)[kU], int cb, int ce,
                                             const float* xs, int K, int nr, float* red, int RBS) {
@@ -331,30 +344,47 @@ __device__ __noinline__ void gemv_task_rows(const uint4 (&u0)[kU], const uint4 (
 #pragma unroll
   for (int j = 0; j < kU; ++j) { WTraits<WT>::unpack(u0[j], f0[j]); WTraits<WT>::unpack(u1[j], f1[j]); }
 #pragma unroll 1
-  for (int r = 0; r < nr; ++r) {
-    const float* xr = xs + (size_t)r * K;
-    float s0 = 0.0f, s1 = 0.0f;
+  for (int r0 = 0; r0 < nr; r0 += 4) {
+    float a[4][2][2];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) { a[q][0][0] = a[q][0][1] = a[q][1][0] = a[q][1][1] = 0.0f; }
+    const float* xr[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) xr[q] = xs + (size_t)min(r0 + q, nr - 1) * K;
 #pragma unroll
     for (int j = 0; j < kU; ++j) {
       const int c = cb + lane + 32 * j;
       if (c < ce) {
-        if (EPC == 8) {
-          const float4 x0 = *reinterpret_cast<const float4*>(xr + 4 * c);
-          const float4 x1 = *reinterpret_cast<const float4*>(xr + K / 2 + 4 * c);
-          const float x[8] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w};
 #pragma unroll
-          for (int e = 0; e < 8; ++e) { s0 = fmaf(f0[j][e], x[e], s0); s1 = fmaf(f1[j][e], x[e], s1); }
-        } else {
-          const float4 x0 = *reinterpret_cast<const float4*>(xr + 4 * c);
-          const float x[4] = {x0.x, x0.y, x0.z, x0.w};
+        for (int q = 0; q < 4; ++q) {
+          float x[EPC];
+          const float4 x0 = *reinterpret_cast<const float4*>(xr[q] + 4 * c);
+          x[0] = x0.x; x[1] = x0.y; x[2] = x0.z; x[3] = x0.w;
+          if (EPC == 8) {
+            const float4 x1 = *reinterpret_cast<const float4*>(xr[q] + K / 2 + 4 * c);
+            x[EPC - 4] = x1.x; x[EPC - 3] = x1.y; x[EPC - 2] = x1.z; x[EPC - 1] = x1.w;
+          }
 #pragma unroll
-          for (int e = 0; e < EPC; ++e) { s0 = fmaf(f0[j][e], x[e], s0); s1 = fmaf(f1[j][e], x[e], s1); }
+          for (int e = 0; e < EPC; ++e) {
+            a[q][0][j & 1] = fmaf(f0[j][e], x[e], a[q][0][j & 1]);
+            a[q][1][j & 1] = fmaf(f1[j][e], x[e], a[q][1][j & 1]);
+          }
         }
       }
     }
-    s0 = warp_sum(s0);
-    s1 = warp_sum(s1);
-    if (lane == 0) { red[r] = s0; red[RBS + r] = s1; }
+    float v[8];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) { v[2 * q] = a[q][0][0] + a[q][0][1]; v[2 * q + 1] = a[q][1][0] + a[q][1][1]; }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], o);
+    }
+    if (lane == 0) {
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (r0 + q < nr) { red[r0 + q] = v[2 * q]; red[RBS + r0 + q] = v[2 * q + 1]; }
+    }
   }
 }
 
@@ -423,7 +453,7 @@ __device__ __noinline__ int gemv_phase(const FrameParams& P, CtaShared& cs, cons
                                        unsigned char* slots, int consumed) {
   const int kind = cs.kind, l = cs.layer;
   const int K = gemv_K(P, kind);
-  const int nt = phase_tiles<WT>(P, cs, kind);
+  const int nt = phase_tiles(cs, kind);
   if (nt == 0) return consumed;
   const float* src;
   int ld;
@@ -438,12 +468,12 @@ __device__ __noinline__ int gemv_phase(const FrameParams& P, CtaShared& cs, cons
   constexpr int EPC = WTraits<WT>::EPC;
   const int nch = K / EPC;
   const bool split = (kind == kQKV || kind == kGU);
-  const int KS = gemv_ksplit(nch, pairs_per_tile<WT>(P, kind));
+  const int KS = gemv_ksplit(nch, pairs_per_tile(cs, kind));
   const int ppr = kWarps / KS;  // pairs per round
   const int RB = P.RB;
   float* xs = uni;
-  float* red = uni + (size_t)RB * K;  // [kWarps][2][RB]
-  float2* srope = reinterpret_cast<float2*>(red + (size_t)kWarps * 2 * RB);  // [RB][d/2]
+  float* red = uni + (size_t)RB * K;  // [2 rounds][kWarps][2][RB]
+  float2* srope = reinterpret_cast<float2*>(red + (size_t)2 * kWarps * 2 * RB);  // [RB][d/2]
   const int half = P.d / 2;
   const int warp = threadIdx.x >> 5;
   const int ks = warp % KS;
@@ -452,34 +482,35 @@ __device__ __noinline__ int gemv_phase(const FrameParams& P, CtaShared& cs, cons
   int staged = -1;
   for (int t = 0; t < nt; ++t) {
     int pa, pb;
-    tile_pairs<WT>(P, cs, kind, t, pa, pb);
+    tile_pairs(cs, kind, t, pa, pb);
     const int npt = pb - pa;
     const int slot = consumed & 1;
+    const uint32_t par = (uint32_t)((consumed >> 1) & 1);
     const WT* tile = reinterpret_cast<const WT*>(slot_base(P, slots, slot));
     for (int ch = 0; ch < nchunks; ++ch) {
       const int rb0 = ch * RB, nr = min(RB, cs.nrows - rb0);
       if (staged != ch) {
-        __syncthreads();  // the previous chunk is done with xs / srope
+        __syncthreads();  // the previous chunk is done with xs / srope / red
         if (kind == kQKV)
           for (int i = threadIdx.x; i < nr * (half / 2); i += kThreads) {
             const int r = i / (half / 2), c = i - r * (half / 2);
             cp_async16(srope + (size_t)r * half + 2 * c, P.rope + (size_t)cs.rpos[rb0 + r] * half + 2 * c);
           }
-        stage_rows<WT>(P, src, ld, K, gain, rows + rb0, nr, xs);
+        // thread 0 also waits (bounded) for this tile; stage_rows' barriers publish the verdict
+        stage_rows<WT>(P, src, ld, K, gain, rows + rb0, nr, xs, ch == 0 ? &cs.wbar[slot] : nullptr, par, &cs.wok);
         staged = ch;
-      }
-      if (ch == 0) {
-        // thread 0 waits (bounded) and publishes the verdict so every thread takes the same path;
-        // the others then observe the completed phase themselves (acquire of the TMA writes)
-        const uint32_t par = (uint32_t)((consumed >> 1) & 1);
+      } else if (ch == 0) {
         if (threadIdx.x == 0) cs.wok = mbar_wait_bounded(&cs.wbar[slot], par, &P.ctl->status, P.timeout_ns) ? 1 : 0;
         __syncthreads();
+      }
+      if (ch == 0) {
         if (!cs.wok) return -1;
-        while (!mbar_try_wait(&cs.wbar[slot], par)) {
+        while (!mbar_try_wait(&cs.wbar[slot], par)) {  // completed: every thread acquires the TMA writes
         }
       }
       const int rounds = (npt + ppr - 1) / ppr;
       for (int rd = 0; rd < rounds; ++rd) {
+        float* rbuf = red + (size_t)(rd & 1) * kWarps * 2 * RB;
         const int g = rd * ppr + warp / KS;  // pair within the tile
         if (g < npt) {
           const WT *r0, *r1;
@@ -487,9 +518,9 @@ __device__ __noinline__ int gemv_phase(const FrameParams& P, CtaShared& cs, cons
           else { r0 = tile + (size_t)(2 * g) * K; r1 = r0 + K; }
           uint4 u0[kU], u1[kU];
           gemv_load_task<WT>(r0, r1, cb, ce, u0, u1);
-          gemv_task_rows<WT>(u0, u1, cb, ce, xs, K, nr, red + (size_t)warp * 2 * RB, RB);
+          gemv_task_rows<WT>(u0, u1, cb, ce, xs, K, nr, rbuf + (size_t)warp * 2 * RB, RB);
         }
-        __syncthreads();
+        __syncthreads();  // rbuf complete; the other buffer is free for the next round
         // finish: sum the K-split partials in order, then the epilogue
         for (int i = threadIdx.x; i < ppr * nr; i += kThreads) {
           const int gi = i / nr, r = i - gi * nr;
@@ -497,13 +528,13 @@ __device__ __noinline__ int gemv_phase(const FrameParams& P, CtaShared& cs, cons
           if (gg >= npt) continue;
           float y0 = 0.0f, y1 = 0.0f;
           for (int j = 0; j < KS; ++j) {
-            y0 += red[((gi * KS + j) * 2 + 0) * RB + r];
-            y1 += red[((gi * KS + j) * 2 + 1) * RB + r];
+            y0 += rbuf[((gi * KS + j) * 2 + 0) * RB + r];
+            y1 += rbuf[((gi * KS + j) * 2 + 1) * RB + r];
           }
           gemv_epilogue<WT>(P, kind, l, pa + gg, rows[rb0 + r], cs.rpos[rb0 + r], srope + (size_t)r * half, y0, y1, cs);
         }
-        __syncthreads();
       }
+      __syncthreads();  // tile rows and xs no longer read
     }
     // the slot is free: refill it with the next tile of the sequence
     ++consumed;
@@ -1268,6 +1299,8 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
     mbar_init(&cs.wbar[1], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     cs.issued = 0; cs.cur_w = 0; cs.cur_t = 0; cs.pass = -1; cs.nheads = 0;
+    for (int kind = kQKV; kind <= kDown; ++kind) tile_table_fill<WT>(P, cs, kind);
+    tile_table_fill<WT>(P, cs, kHeads);  // no heads until the first pass
   }
   __syncthreads();
   refill_slots<WT>(P, cs, slots, consumed);  // layer-0 weights stream during the setup
@@ -1291,7 +1324,10 @@ __global__ void __launch_bounds__(kThreads, 1) frame_kernel(const __grid_constan
       }
       const int parity = (pass_base + pass) & 1;
       build_pass_lists(P, parity, cs, rows, rpos);
-      if (threadIdx.x == 0) cs.pass = pass;
+      if (threadIdx.x == 0) {
+        tile_table_fill<WT>(P, cs, kHeads);
+        cs.pass = pass;
+      }
       refill_slots<WT>(P, cs, slots, consumed);
       if (blockIdx.x == 0 && threadIdx.x == 0) {
         ctl->head_mask[parity ^ 1] = 0ull;

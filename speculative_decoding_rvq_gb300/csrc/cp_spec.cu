@@ -141,7 +141,7 @@ SmemPlan smem_plan(const cp_spec_model* m, int N, int KC, int Bmax) {
     const size_t budget = kDynSmemLimit - rows - 2 * slot;
     int RB = 8;
     auto gemv = [&](int rb) {
-      return (size_t)rb * Kmax * 4 + (size_t)cpk::kWarps * 2 * rb * 4 + (size_t)rb * (m->head_dim / 2) * 8;
+      return (size_t)rb * Kmax * 4 + (size_t)2 * cpk::kWarps * 2 * rb * 4 + (size_t)rb * (m->head_dim / 2) * 8;
     };
     while (RB > 1 && gemv(RB) > budget) RB /= 2;
     const int tw = (int)std::min<size_t>(cpk::kWarps, budget / per_attn);
