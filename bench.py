@@ -105,25 +105,46 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
+FRAME_KERNEL_SOURCES = ("cp_common.cuh", "cp_sampling.cuh", "cp_frame.cuh", "cp_frame_kernel.cu")
+
+
 def kernel_source_hash():
+    """Hash of the sources the frame kernel is compiled from (host-side files excluded)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_rvq_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
-        if fn.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, fn), "rb").read())
+    for fn in FRAME_KERNEL_SOURCES:
+        h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic():
-    """DRAM bytes per launch of the frame kernel from the committed ncu summary, if it
-    was taken on the current kernel sources (else None)."""
+    """DRAM bytes per decoder pass of the frame kernel from the committed ncu summary,
+    if it was taken on the current kernel sources (else None).  Every pass streams the
+    same weights, so a launch's traffic scales with its number of passes."""
     p = os.path.join(ROOT, "profiles", "frame_kernel_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     if d.get("kernel_source_hash") != kernel_source_hash():
         return None
-    return d.get("dram_bytes_per_frame")
+    return d.get("dram_bytes_per_pass")
+
+
+# ------------------------------------------------------------- multi-rank
+def job_throughput(units_local: float, ms_local: float, world: int):
+    """Whole-job throughput: the units every rank processed over the slowest rank's time.
+
+    Returns (units per second, max ms over ranks).  At world size 1 no process group is used."""
+    if world <= 1:
+        return units_local / (ms_local / 1e3), ms_local
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    u = torch.tensor([units_local], dtype=torch.float64, device=dev)
+    t = torch.tensor([ms_local], dtype=torch.float64, device=dev)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(u.item()) / (float(t.item()) / 1e3), float(t.item())
 
 
 # ------------------------------------------------------------------ GPU arm
@@ -175,24 +196,20 @@ def run_gpu(args, rank, world):
     st = cp.stats()
     cp.status()
     codes_total = args.steps * frames * (spec.num_code_groups - 1)
-    if world > 1:
-        t = torch.tensor([total_ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    value = codes_total * world / (total_ms / 1e3)
+    value, total_ms = job_throughput(codes_total, total_ms, world)
 
     peak, peak_kind = measured_peaks()
     per_launch_bytes = (st["weight_bytes"] + st["kv_bytes"]) / args.steps
     mean_launch_s = statistics.mean(launch_ms) / 1e3
     achieved = per_launch_bytes / mean_launch_s / 1e9
-    traffic_pf = recorded_traffic()
+    traffic_pp = recorded_traffic()
+    passes = st["passes"] / args.steps
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                "traffic": (round(traffic_pf * frames) if traffic_pf else None),
+                "traffic": (round(traffic_pp * passes) if traffic_pp else None),
                 "kernel": "frame_kernel<bf16> (one cooperative launch per step)",
                 "algorithmic_bytes_per_launch": int(per_launch_bytes),
                 "mean_launch_ms": round(statistics.mean(launch_ms), 3)}
-    passes = st["passes"] / args.steps
     rounds = st["rounds"] / args.steps
     result = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -300,16 +317,23 @@ def accept_microbench(peak):
 
 
 # ------------------------------------------------------------ CPU baselines
-def oracle_codes_per_s(frames: int, window: int):
-    """The CPU oracle (single-threaded C, float64 forward) on `frames` frames of the workload."""
+def oracle_model():
+    """The CPU oracle (single-threaded C, float64 forward) loaded with the workload's weights."""
     from oracle import oracle as O
     from speculative_decoding_rvq_gb300 import synth as S
     spec = S.TTS06B_BF16
-    w = S.gen_weights(spec, 0)
-    m = O.Model(spec, w)
-    x, c0 = S.gen_frames(spec, 1, frames, seed=SEED)
+    return O.Model(spec, S.gen_weights(spec, 0))
+
+
+def oracle_codes_per_s(frames: int, window: int, model=None, first_frame: int = 0):
+    """Codes/s of the CPU oracle on `frames` frames of the workload (frames first_frame..)."""
+    from speculative_decoding_rvq_gb300 import synth as S
+    spec = S.TTS06B_BF16
+    m = model if model is not None else oracle_model()
+    x, c0 = S.gen_frames(spec, 1, first_frame + frames, seed=SEED)
+    x, c0 = x[first_frame:], c0[first_frame:]
     t = time.perf_counter()
-    m.decode_frames(window, TOP_K, TEMP, SEED, x, c0)
+    m.decode_frames(window, TOP_K, TEMP, SEED, x, c0, first_frame=first_frame)
     dt = time.perf_counter() - t
     return frames * (spec.num_code_groups - 1) / dt, dt
 
@@ -322,12 +346,13 @@ def cpu_baseline_entry(frames=3):
 
 def run_reference(args, rank, world):
     spec_frames = max(1, args.ref_frames)
+    model = oracle_model()
     times = []
-    for _ in range(args.warmup if args.warmup < 1 else 1):
-        oracle_codes_per_s(1, WINDOW)
+    for _ in range(min(max(args.warmup, 0), 1)):  # one untimed frame warms caches; more adds nothing
+        oracle_codes_per_s(1, WINDOW, model)
     vals = []
-    for _ in range(args.steps):
-        v, dt = oracle_codes_per_s(spec_frames, WINDOW)
+    for i in range(args.steps):
+        v, dt = oracle_codes_per_s(spec_frames, WINDOW, model, first_frame=i * spec_frames)
         vals.append(v)
         times.append(dt)
     from speculative_decoding_rvq_gb300 import synth as S

@@ -79,9 +79,17 @@ WEIGHT_STD = 0.02
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """Round float32 to bfloat16 (round to nearest, ties to even); returns uint16 bits."""
     a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    rounding = ((u >> 16) & 1) + 0x7FFF
-    return ((u + rounding) >> 16).astype(np.uint16)
+    u = a.view(np.uint32).ravel()
+    out = np.empty(u.shape, np.uint16)
+    step = 1 << 22
+    for i in range(0, u.size, step):  # uint32 arithmetic cannot overflow for finite inputs
+        c = u[i:i + step]
+        r = (c >> np.uint32(16)) & np.uint32(1)
+        r += c
+        r += np.uint32(0x7FFF)
+        r >>= np.uint32(16)
+        out[i:i + step] = r
+    return out.reshape(a.shape)
 
 
 def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
