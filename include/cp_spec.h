@@ -57,6 +57,8 @@ extern "C" {
 #define CP_SPEC_MAX_WINDOW 8
 #define CP_SPEC_MAX_CODE_GROUPS 64
 #define CP_SPEC_MAX_VOCAB 8192
+/* Size of the library-owned scratch of cp_spec_decode_frames_static (8 MiB). */
+#define CP_SPEC_STATIC_SCRATCH_BYTES (8u << 20)
 
 typedef enum {
   CP_SPEC_OK = 0,
@@ -213,6 +215,42 @@ cp_spec_status cp_spec_accept_batch(int32_t R, int32_t N, int32_t V, int32_t top
                                     const float* d_draft, int32_t* d_tokens, int32_t* d_n_accepted,
                                     int32_t* d_drafts, void* stream);
 
+/* Decode without any allocation: cp_spec_decode_frames for a one-off job,
+ * with no context and no caller workspace.  The pages describe no such call;
+ * it exists for callers that cannot allocate device memory when they decode:
+ * a runtime with no device allocator of its own, a host whose memory pool is
+ * frozen after start-up, or one that must keep its device footprint fixed.
+ * The KV cache, activations, sampling lists and stream state live instead in
+ * a library-owned array of CP_SPEC_STATIC_SCRATCH_BYTES in the module's
+ * global memory, reserved by the CUDA runtime when the library's module is
+ * loaded (one copy per device).
+ *
+ * Arguments are those of cp_spec_init plus cp_spec_decode_frames (same
+ * layouts; streams 0..n_streams-1, n_streams <= config->max_streams).  The
+ * workspace it needs is cp_spec_workspace_bytes(model, config); above
+ * CP_SPEC_STATIC_SCRATCH_BYTES the call returns CP_SPEC_E_WORKSPACE and
+ * enqueues nothing (lower max_streams).  d_status (optional, device, one
+ * int32) receives the device status word after the decode: CP_SPEC_OK,
+ * CP_SPEC_E_DEVICE_TIMEOUT or CP_SPEC_E_DEVICE.
+ *
+ * Every call clears the scratch, resets it to the state cp_spec_init leaves
+ * (on `stream`, before the decode) and decodes: results equal those of a
+ * fresh context with the same config, bit for bit.  Per-stream sampling
+ * overrides and counters are not available.  Asynchronous; returns
+ * CP_SPEC_W_AR_FALLBACK under the same condition as cp_spec_init.
+ *
+ * The first call on each device looks up the scratch address
+ * (cudaGetSymbolAddress, which may load the module) and caches it; make that
+ * first call before any stream capture begins.  All calls on one device share
+ * the one scratch array: calls whose work overlaps in time (different
+ * streams, or threads without ordering) race on it and give wrong results.
+ * Order them on one stream.  Launches count in the context-free counter of
+ * cp_spec_launch_count(NULL). */
+cp_spec_status cp_spec_decode_frames_static(const cp_spec_model* model, const cp_spec_weights* weights,
+                                            const cp_spec_config* config, int32_t n_streams, int32_t n_frames,
+                                            int32_t first_frame, const float* d_x, const int32_t* d_c0,
+                                            int32_t* d_codes, int32_t* d_status, void* stream);
+
 /* Synchronise `stream` and return the device status word of the context:
  * CP_SPEC_OK, CP_SPEC_E_DEVICE_TIMEOUT or CP_SPEC_E_DEVICE.  Clears it. */
 cp_spec_status cp_spec_status_word(cp_spec_ctx* ctx, void* stream);
@@ -222,7 +260,8 @@ cp_spec_status cp_spec_read_stats(cp_spec_ctx* ctx, cp_spec_stats* h_stats, void
 cp_spec_status cp_spec_reset_stats(cp_spec_ctx* ctx, void* stream);
 
 /* Number of kernel launches the library has enqueued on this context
- * (cp_spec_accept_batch counts in a process-wide counter, ctx = NULL). */
+ * (cp_spec_accept_batch and cp_spec_decode_frames_static count in a
+ * process-wide counter, ctx = NULL). */
 int64_t cp_spec_launch_count(const cp_spec_ctx* ctx);
 
 /* Last error message of the context (or of the last context-free call when

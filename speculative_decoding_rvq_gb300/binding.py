@@ -25,7 +25,7 @@ E_INVALID, E_UNSUPPORTED, E_CUDA, E_WORKSPACE, E_DEVICE_TIMEOUT, E_STATE, E_DEVI
 EXPORTS = ("cp_spec_workspace_bytes", "cp_spec_init", "cp_spec_set_stream_sampling", "cp_spec_decode_frames",
            "cp_spec_begin_frame", "cp_spec_round", "cp_spec_teacher_logits", "cp_spec_accept_batch",
            "cp_spec_status_word", "cp_spec_read_stats", "cp_spec_reset_stats", "cp_spec_launch_count",
-           "cp_spec_last_error", "cp_spec_destroy")
+           "cp_spec_last_error", "cp_spec_destroy", "cp_spec_decode_frames_static")
 
 
 class CpSpecError(RuntimeError):
@@ -85,6 +85,7 @@ def load():
     L.cp_spec_round.argtypes = [vp, vp, vp, vp]
     L.cp_spec_teacher_logits.argtypes = [vp, i32, i32, vp, vp, vp, vp, vp]
     L.cp_spec_accept_batch.argtypes = [i32, i32, i32, i32, f32, u64, i32, vp, vp, vp, vp, vp, vp]
+    L.cp_spec_decode_frames_static.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
     L.cp_spec_status_word.argtypes = [vp, vp]
     L.cp_spec_read_stats.argtypes = [vp, vp, vp]
     L.cp_spec_reset_stats.argtypes = [vp, vp]
@@ -96,7 +97,7 @@ def load():
     L.cp_spec_destroy.restype = None
     for name in ("cp_spec_init", "cp_spec_set_stream_sampling", "cp_spec_decode_frames", "cp_spec_begin_frame",
                  "cp_spec_round", "cp_spec_teacher_logits", "cp_spec_accept_batch", "cp_spec_status_word",
-                 "cp_spec_read_stats", "cp_spec_reset_stats"):
+                 "cp_spec_read_stats", "cp_spec_reset_stats", "cp_spec_decode_frames_static"):
         getattr(L, name).restype = C.c_int
     _lib = L
     return L
@@ -240,3 +241,25 @@ def accept_batch(target, draft, top_k: int, temperature: float, seed: int, mode:
     _check(lib.cp_spec_accept_batch(R, N, V, top_k, temperature, seed, mode, _ptr(target), _ptr(draft), _ptr(tok),
                                     _ptr(na), _ptr(dr), _stream()))
     return tok, na, dr
+
+
+def decode_frames_static(spec: synth.ModelSpec, device_weights: dict, verify_window: int, top_k: int,
+                         temperature: float, seed: int, x, c0, codes=None, first_frame: int = 0, max_streams=None,
+                         status=None):
+    """cp_spec_decode_frames_static: one decode in the library's static scratch, no context.
+
+    x [F, B, H] float32 cuda, c0 [F, B] int32 cuda -> codes [F, B, G] int32 (asynchronous).
+    status (optional) is a 1-element int32 cuda tensor that receives the device status word.
+    Returns (codes, rc) with rc OK or W_AR_FALLBACK."""
+    import torch
+    lib = load()
+    F, B, _ = x.shape
+    if codes is None:
+        codes = torch.empty((F, B, spec.num_code_groups), dtype=torch.int32, device=x.device)
+    model = model_struct(spec)
+    weights = weights_struct(device_weights)
+    config = Config(verify_window, top_k, temperature, seed, B if max_streams is None else max_streams)
+    rc = lib.cp_spec_decode_frames_static(C.byref(model), C.byref(weights), C.byref(config), B, F, first_frame,
+                                          _ptr(x), _ptr(c0), _ptr(codes), _ptr(status), _stream())
+    _check(rc, None, allow=(OK, W_AR_FALLBACK))
+    return codes, rc

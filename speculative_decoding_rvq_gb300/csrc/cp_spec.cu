@@ -10,6 +10,7 @@
 #include <algorithm>
 #include <atomic>
 #include <cmath>
+#include <mutex>
 #include <new>
 #include <string>
 
@@ -157,47 +158,30 @@ SmemPlan smem_plan(const cp_spec_model* m, int N, int KC, int Bmax) {
 template <typename T>
 T* at(unsigned char* base, size_t off) { return reinterpret_cast<T*>(base + off); }
 
-cp_spec_status enqueue_frame(cp_spec_ctx* c, const cpk::FrameParams& P, bool clear_masks, cudaStream_t s) {
-  cpk::Control* ctl = at<cpk::Control>(c->ws, c->lay.ctl);
-  cudaError_t e = cudaMemsetAsync(ctl, 0, clear_masks ? 3 * sizeof(unsigned long long) : sizeof(unsigned long long), s);
-  if (e != cudaSuccess) return check_cuda(c, e, "cudaMemsetAsync(control)");
-  e = cpk_host::launch_frame_kernel(P, c->grid, c->smem, s);
-  if (e != cudaSuccess) return check_cuda(c, e, "frame kernel launch");
-  c->launches += 1;
-  return CP_SPEC_OK;
-}
-
-}  // namespace
-
-extern "C" {
-
-size_t cp_spec_workspace_bytes(const cp_spec_model* model, const cp_spec_config* config) {
-  if (validate(model, config, nullptr) != CP_SPEC_OK) return 0;
-  return layout_for(model, config, effective_window(model, config)).total;
-}
-
-cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* weights, const cp_spec_config* config,
-                            void* d_workspace, size_t workspace_bytes, cp_spec_ctx** out) {
-  if (!out) return fail(nullptr, CP_SPEC_E_INVALID, "out is null");
-  *out = nullptr;
-  cp_spec_status v = validate(model, config, nullptr);
-  if (v != CP_SPEC_OK) return v;
+cp_spec_status check_weights(const cp_spec_model* model, const cp_spec_weights* weights) {
   if (!weights) return fail(nullptr, CP_SPEC_E_INVALID, "weights is null");
-  const int L = model->n_layers;
   const void* ptrs[] = {weights->embed, weights->lm_head, weights->final_norm};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return fail(nullptr, CP_SPEC_E_INVALID, "embed/lm_head/final_norm null or not 16-byte aligned");
-  for (int l = 0; l < L; ++l) {
+  for (int l = 0; l < model->n_layers; ++l) {
     const void* lp[] = {weights->attn_norm[l], weights->wq[l], weights->wk[l], weights->wv[l], weights->wo[l],
                         weights->ffn_norm[l], weights->w_gate[l], weights->w_up[l], weights->w_down[l]};
     for (const void* p : lp)
       if (!p || !aligned16(p)) return fail(nullptr, CP_SPEC_E_INVALID, "layer %d weight null or not 16-byte aligned", l);
   }
-  if (!d_workspace || !aligned16(d_workspace)) return fail(nullptr, CP_SPEC_E_INVALID, "workspace null or not 16-byte aligned");
-  const int N = effective_window(model, config);
-  const cpk::Layout lay = layout_for(model, config, N);
-  if (workspace_bytes < lay.total)
-    return fail(nullptr, CP_SPEC_E_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes, lay.total);
+  return CP_SPEC_OK;
+}
+
+// Device facts and the shared-memory plan of one frame-kernel configuration.
+struct DevicePlan {
+  int dev, sms, KC;
+  SmemPlan sp;
+};
+
+// Queries the current device and checks that the configuration fits the
+// frame kernel (cooperative launch, register-held rows, shared memory, one
+// accept warp per stream).  Sets the kernel's shared-memory attribute.
+cp_spec_status plan_device(const cp_spec_model* model, const cp_spec_config* config, int N, DevicePlan* dp) {
   int dev = 0, sms = 0, coop = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -224,33 +208,27 @@ cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* w
   e = cpk_host::frame_kernel_config(model->dtype, sp.bytes, &maxb);
   if (e != cudaSuccess) return check_cuda(nullptr, e, "frame kernel attributes");
   if (maxb < 1) return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "frame kernel needs %zu bytes of shared memory per CTA", sp.bytes);
-  const int NS = N > 2 ? N : 2;
   if ((long long)config->max_streams > (long long)sms * sp.accept_warps)
     return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "max_streams above %d (one accept warp per stream)", sms * sp.accept_warps);
+  *dp = DevicePlan{dev, sms, KC, sp};
+  return CP_SPEC_OK;
+}
 
-  cp_spec_ctx* c = new (std::nothrow) cp_spec_ctx();
-  if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "host allocation failed");
-  c->model = *model;
-  c->weights = *weights;
-  c->config = *config;
-  c->N = N;
-  c->device = dev;
-  c->grid = sms;
-  c->smem = sp.bytes;
-  c->lay = lay;
-  c->ws = static_cast<unsigned char*>(d_workspace);
-  c->launches = 0;
-  c->staged = c->need_setup = false;
-
-  cpk::FrameParams& P = c->base;
+// Fills the launch-invariant part of the frame kernel's parameters: model
+// shape, plan, weight pointers and the carve-up of the workspace at `ws`.
+void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, const cp_spec_config* config, int N,
+                 const DevicePlan& dp, const cpk::Layout& lay, unsigned char* ws, cpk::FrameParams* out) {
+  cpk::FrameParams& P = *out;
   memset(&P, 0, sizeof P);
+  const int L = model->n_layers;
+  const int NS = N > 2 ? N : 2;
   P.H = model->hidden; P.L = L; P.nq = model->n_q_heads; P.nkv = model->n_kv_heads; P.d = model->head_dim;
   P.F = model->ffn; P.V = model->vocab; P.G = model->num_code_groups; P.dtype = model->dtype;
   P.eps = model->rms_eps;
-  P.N = N; P.NS = NS; P.ND = N > 1 ? N - 1 : 0; P.KC = KC; P.RB = sp.RB; P.proc_warps = sp.proc_warps;
-  P.accept_warps = sp.accept_warps;
-  P.attn_warps = sp.attn_warps;
-  P.slot_bytes = sp.slot_bytes;
+  P.N = N; P.NS = NS; P.ND = N > 1 ? N - 1 : 0; P.KC = dp.KC; P.RB = dp.sp.RB; P.proc_warps = dp.sp.proc_warps;
+  P.accept_warps = dp.sp.accept_warps;
+  P.attn_warps = dp.sp.attn_warps;
+  P.slot_bytes = dp.sp.slot_bytes;
   P.seed = config->seed;
   P.timeout_ns = kBarrierTimeoutNs;
   const long long eb = model->dtype == 1 ? 2 : 4;
@@ -264,7 +242,6 @@ cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* w
     P.wv[l] = weights->wv[l]; P.wo[l] = weights->wo[l]; P.ffn_norm[l] = weights->ffn_norm[l];
     P.w_gate[l] = weights->w_gate[l]; P.w_up[l] = weights->w_up[l]; P.w_down[l] = weights->w_down[l];
   }
-  unsigned char* ws = c->ws;
   P.kv = at<float>(ws, lay.kv); P.h = at<float>(ws, lay.h); P.qbuf = at<float>(ws, lay.qbuf);
   P.obuf = at<float>(ws, lay.obuf); P.act = at<float>(ws, lay.act); P.logits = at<float>(ws, lay.logits);
   P.lidx = at<int>(ws, lay.lidx); P.lprob = at<float>(ws, lay.lprob); P.lcount = at<int>(ws, lay.lcount);
@@ -272,10 +249,90 @@ cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* w
   P.row_pos = at<int>(ws, lay.row_pos); P.st = at<cpk::StreamState>(ws, lay.st);
   P.sstats = at<cpk::StreamStats>(ws, lay.sstats); P.rope = at<float2>(ws, lay.rope);
   P.top_k = at<int>(ws, lay.top_k); P.temp = at<float>(ws, lay.temp); P.ctl = at<cpk::Control>(ws, lay.ctl);
+}
 
-  e = cudaMemset(ws, 0, lay.total);
+cp_spec_status enqueue_frame(cp_spec_ctx* c, const cpk::FrameParams& P, bool clear_masks, cudaStream_t s) {
+  cpk::Control* ctl = at<cpk::Control>(c->ws, c->lay.ctl);
+  cudaError_t e = cudaMemsetAsync(ctl, 0, clear_masks ? 3 * sizeof(unsigned long long) : sizeof(unsigned long long), s);
+  if (e != cudaSuccess) return check_cuda(c, e, "cudaMemsetAsync(control)");
+  e = cpk_host::launch_frame_kernel(P, c->grid, c->smem, s);
+  if (e != cudaSuccess) return check_cuda(c, e, "frame kernel launch");
+  c->launches += 1;
+  return CP_SPEC_OK;
+}
+
+// Scratch of cp_spec_decode_frames_static: a fixed array in this module's
+// global memory, reserved by the CUDA runtime when the module is loaded on a
+// device (one copy per device), so the call itself reserves nothing.
+__device__ __align__(256) unsigned char g_static_scratch[CP_SPEC_STATIC_SCRATCH_BYTES];
+
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_mu;
+unsigned char* g_static_addr[kMaxStaticDevices] = {};
+
+// Address of g_static_scratch on device `dev` (the current device), looked up
+// on the first call for that device and cached.
+cp_spec_status static_scratch(int dev, unsigned char** out) {
+  if (dev < 0 || dev >= kMaxStaticDevices)
+    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "device ordinal %d above %d", dev, kMaxStaticDevices - 1);
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (!g_static_addr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess) return check_cuda(nullptr, e, "cudaGetSymbolAddress(static scratch)");
+    if (!p || !aligned16(p)) return fail(nullptr, CP_SPEC_E_CUDA, "static scratch address not 16-byte aligned");
+    g_static_addr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = g_static_addr[dev];
+  return CP_SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t cp_spec_workspace_bytes(const cp_spec_model* model, const cp_spec_config* config) {
+  if (validate(model, config, nullptr) != CP_SPEC_OK) return 0;
+  return layout_for(model, config, effective_window(model, config)).total;
+}
+
+cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* weights, const cp_spec_config* config,
+                            void* d_workspace, size_t workspace_bytes, cp_spec_ctx** out) {
+  if (!out) return fail(nullptr, CP_SPEC_E_INVALID, "out is null");
+  *out = nullptr;
+  cp_spec_status v = validate(model, config, nullptr);
+  if (v != CP_SPEC_OK) return v;
+  v = check_weights(model, weights);
+  if (v != CP_SPEC_OK) return v;
+  if (!d_workspace || !aligned16(d_workspace)) return fail(nullptr, CP_SPEC_E_INVALID, "workspace null or not 16-byte aligned");
+  const int N = effective_window(model, config);
+  const cpk::Layout lay = layout_for(model, config, N);
+  if (workspace_bytes < lay.total)
+    return fail(nullptr, CP_SPEC_E_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes, lay.total);
+  DevicePlan dp;
+  v = plan_device(model, config, N, &dp);
+  if (v != CP_SPEC_OK) return v;
+
+  cp_spec_ctx* c = new (std::nothrow) cp_spec_ctx();
+  if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "host allocation failed");
+  c->model = *model;
+  c->weights = *weights;
+  c->config = *config;
+  c->N = N;
+  c->device = dp.dev;
+  c->grid = dp.sms;
+  c->smem = dp.sp.bytes;
+  c->lay = lay;
+  c->ws = static_cast<unsigned char*>(d_workspace);
+  c->launches = 0;
+  c->staged = c->need_setup = false;
+
+  cpk::FrameParams& P = c->base;
+  fill_params(model, weights, config, N, dp, lay, c->ws, &P);
+
+  cudaError_t e = cudaMemset(c->ws, 0, lay.total);
   if (e == cudaSuccess)
-    e = cudaMemset(P.row_pos, 0xFF, sizeof(int) * (size_t)config->max_streams * NS);
+    e = cudaMemset(P.row_pos, 0xFF, sizeof(int) * (size_t)config->max_streams * P.NS);
   if (e == cudaSuccess)
     e = cpk_host::launch_init_tables(P.rope, P.G, P.d, (double)model->rope_theta, P.top_k, P.temp, config->max_streams,
                                      config->top_k, config->temperature, 0);
@@ -399,6 +456,63 @@ cp_spec_status cp_spec_accept_batch(int32_t R, int32_t N, int32_t V, int32_t top
                                                 d_n_accepted, d_drafts, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return check_cuda(nullptr, e, "accept kernel launch");
   g_free_launches.fetch_add(1);
+  return CP_SPEC_OK;
+}
+
+cp_spec_status cp_spec_decode_frames_static(const cp_spec_model* model, const cp_spec_weights* weights,
+                                            const cp_spec_config* config, int32_t n_streams, int32_t n_frames,
+                                            int32_t first_frame, const float* d_x, const int32_t* d_c0,
+                                            int32_t* d_codes, int32_t* d_status, void* stream) {
+  cp_spec_status v = validate(model, config, nullptr);
+  if (v != CP_SPEC_OK) return v;
+  v = check_weights(model, weights);
+  if (v != CP_SPEC_OK) return v;
+  if (n_streams < 1 || n_streams > config->max_streams)
+    return fail(nullptr, CP_SPEC_E_INVALID, "n_streams out of [1, max_streams]");
+  if (n_frames < 0 || first_frame < 0) return fail(nullptr, CP_SPEC_E_INVALID, "negative n_frames or first_frame");
+  const int N = effective_window(model, config);
+  const cpk::Layout lay = layout_for(model, config, N);
+  if (lay.total > (size_t)CP_SPEC_STATIC_SCRATCH_BYTES)
+    return fail(nullptr, CP_SPEC_E_WORKSPACE, "needs %zu bytes of scratch, above the static maximum %zu (lower max_streams)",
+                lay.total, (size_t)CP_SPEC_STATIC_SCRATCH_BYTES);
+  if (n_frames == 0) return CP_SPEC_OK;
+  if (!d_x || !d_c0 || !d_codes || !aligned16(d_x) || !aligned16(d_c0) || !aligned16(d_codes) ||
+      (d_status && !aligned16(d_status)))
+    return fail(nullptr, CP_SPEC_E_INVALID, "x/c0/codes null, or a pointer not 16-byte aligned");
+  DevicePlan dp;
+  v = plan_device(model, config, N, &dp);
+  if (v != CP_SPEC_OK) return v;
+  unsigned char* ws = nullptr;
+  v = static_scratch(dp.dev, &ws);
+  if (v != CP_SPEC_OK) return v;
+
+  cpk::FrameParams P;
+  fill_params(model, weights, config, N, dp, lay, ws, &P);
+  P.mode = cpk::kModeDecode;
+  P.B = n_streams; P.n_frames = n_frames; P.first_frame = first_frame;
+  P.max_passes = 0; P.do_setup = 1;
+  P.x = d_x; P.c0 = d_c0; P.codes_out = d_codes; P.committed_out = nullptr;
+
+  // Same starting state as a fresh cp_spec_init, enqueued on the caller's stream.
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(ws, 0, lay.total, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(P.row_pos, 0xFF, sizeof(int) * (size_t)config->max_streams * P.NS, s);
+  if (e == cudaSuccess)
+    e = cpk_host::launch_init_tables(P.rope, P.G, P.d, (double)model->rope_theta, P.top_k, P.temp, config->max_streams,
+                                     config->top_k, config->temperature, s);
+  if (e != cudaSuccess) return check_cuda(nullptr, e, "static scratch initialisation");
+  e = cpk_host::launch_frame_kernel(P, dp.sms, dp.sp.bytes, s);
+  if (e != cudaSuccess) return check_cuda(nullptr, e, "frame kernel launch");
+  if (d_status) {
+    e = cudaMemcpyAsync(d_status, &P.ctl->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
+    if (e != cudaSuccess) return check_cuda(nullptr, e, "status copy");
+  }
+  g_free_launches.fetch_add(2);
+  if (N != window_of(config)) {
+    fail(nullptr, CP_SPEC_W_AR_FALLBACK,
+         "speculation disabled: fewer than 3 code groups leave no draft slot; running the autoregressive loop");
+    return CP_SPEC_W_AR_FALLBACK;
+  }
   return CP_SPEC_OK;
 }
 
