@@ -32,14 +32,14 @@ __global__ void __launch_bounds__(kAcceptWarps * 32) accept_batch_kernel(int R, 
   float* lprob = reinterpret_cast<float*>(lidx + (size_t)nrows * KC);
   int* lcnt = reinterpret_cast<int*>(lprob + (size_t)nrows * KC);
   const size_t lists_bytes = ((size_t)nrows * KC * 8 + (size_t)nrows * 4 + 15) / 16 * 16;
-  // per-warp scratch: [keys: V uint32, 16-byte padded][hist: 256 uint32][ebuf: KC doubles]
+  // per-warp scratch: [keys: V uint32, 16-byte padded][hist: 256 uint32][ebuf: KC floats]
   const size_t keys_bytes = ((size_t)V * 4 + 15) / 16 * 16;
-  const size_t per_warp = (keys_bytes + 1024 + (size_t)KC * 8 + 15) / 16 * 16;
+  const size_t per_warp = (keys_bytes + 1024 + (size_t)KC * 4 + 15) / 16 * 16;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   unsigned char* wb = smem + lists_bytes + (size_t)warp * per_warp;
   uint32_t* keys = reinterpret_cast<uint32_t*>(wb);
   uint32_t* hist = reinterpret_cast<uint32_t*>(wb + keys_bytes);
-  double* ebuf = reinterpret_cast<double*>(wb + keys_bytes + 1024);
+  float* ebuf = reinterpret_cast<float*>(wb + keys_bytes + 1024);
   for (int r = blockIdx.x; r < R; r += gridDim.x) {
     const float* trow = tgt + (size_t)r * N * V;
     const float* drow = drf + (size_t)r * ND * V;
@@ -113,7 +113,7 @@ size_t accept_batch_smem(int N, int V, int k) {
   const int nrows = 2 * N - 1;
   const size_t lists_bytes = ((size_t)nrows * KC * 8 + (size_t)nrows * 4 + 15) / 16 * 16;
   const size_t keys_bytes = ((size_t)V * 4 + 15) / 16 * 16;
-  const size_t per_warp = (keys_bytes + 1024 + (size_t)KC * 8 + 15) / 16 * 16;
+  const size_t per_warp = (keys_bytes + 1024 + (size_t)KC * 4 + 15) / 16 * 16;
   return lists_bytes + per_warp * cpk::kAcceptWarps;
 }
 

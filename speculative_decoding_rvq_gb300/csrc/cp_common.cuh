@@ -87,11 +87,23 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
 
-// 1-D bulk copy global -> shared by the TMA unit; completion is signalled on
-// `bar` as transaction bytes.  dst, src and bytes must be multiples of 16.
-__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+// An L2 policy under which the lines a copy brings in are the first to be
+// evicted.  Weights are read once per pass and the pass streams more bytes
+// than L2 holds, so they must not push out what is reused within a pass
+// (exchange buffers, KV cache, code).
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// 1-D bulk copy global -> shared by the TMA unit under L2 policy `policy`;
+// completion is signalled on `bar` as transaction bytes.  dst, src and bytes
+// must be multiples of 16.
+__device__ __forceinline__ void bulk_copy_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                              uint64_t policy) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+               ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
                : "memory");
 }
 
@@ -105,6 +117,18 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// try_wait with a suspend-time hint: the thread sleeps until the phase
+// completes or about `hint_ns` passed, instead of spinning.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Wait for phase `parity` of `bar` to complete, bounded by timeout_ns of
 // %globaltimer; returns false (after raising the status word) on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status, uint64_t timeout_ns) {
@@ -114,6 +138,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     if (globaltimer_ns() - t0 > timeout_ns) { atomicCAS(status, 0, -5); return false; }
   }
   return true;
+}
+
+// Plain arrival (no transaction bytes).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
 // Inverse of float_key.
@@ -162,40 +191,55 @@ enum : int { kStatusOk = 0, kStatusTimeout = -5, kStatusDevice = -7 };
 
 __device__ __forceinline__ void raise_status(int* status, int code) { atomicCAS(status, 0, code); }
 
-// Grid-wide barrier for a cooperative launch.  `counter` is zeroed before the
-// launch; generation g completes when it reaches g * gridDim.x.  Every wait
-// is bounded by `timeout_ns` of %globaltimer and by the status word: on
-// timeout the status is set and the function returns false so the caller
-// can leave the kernel; nothing spins forever.
-__device__ __forceinline__ bool grid_barrier(unsigned long long* counter, int* status,
-                                             unsigned long long& gen, uint64_t timeout_ns) {
-  __syncthreads();
-  bool ok = true;
-  if (threadIdx.x == 0) {
-    ++gen;
-    const unsigned long long target = gen * (unsigned long long)gridDim.x;
-    __threadfence();
-    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(counter) : "memory");
-    uint64_t t0 = globaltimer_ns();
-    uint32_t spins = 0;
-    while (ld_acquire_u64(counter) < target) {
-      ++spins;
-      if ((spins & 63u) == 0) {
-        const uint64_t now = globaltimer_ns();
-        // bounded twice over: by the global timer and by an iteration count
-        if (now - t0 > timeout_ns || spins > (1u << 30)) { raise_status(status, kStatusTimeout); ok = false; break; }
-        if (ld_relaxed_i32(status) != 0) { ok = false; break; }
-      }
-      if (spins > 4096u) __nanosleep(256);
-    }
-  } else {
-    ++gen;
-  }
-  // broadcast the verdict through shared memory
-  __shared__ int s_ok;
-  if (threadIdx.x == 0) s_ok = ok ? 1 : 0;
-  __syncthreads();
-  return s_ok != 0;
+// ------------------------------------------------------ exchange elements
+// 64-bit words {value, flag}: the writer stores both halves with one 64-bit
+// access, so a reader that sees the expected flag also sees the value.
+__device__ __forceinline__ void xel_store(unsigned long long* p, float v, uint32_t flag) {
+  const unsigned long long w = ((unsigned long long)flag << 32) | (unsigned long long)__float_as_uint(v);
+  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
+}
+
+// Two consecutive exchange elements (16-byte aligned) from L2.
+__device__ __forceinline__ void xel_load2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p));
+}
+
+__device__ __forceinline__ float xel_value(unsigned long long w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ uint32_t xel_flag(unsigned long long w) { return (uint32_t)(w >> 32); }
+
+// ------------------------------------------------------------ arithmetic
+// e^d for d <= 0 in float32, the softmax exponential of the sampling path,
+// written from the mathematics: Cody-Waite range reduction (Cody and Waite,
+// "Software Manual for the Elementary Functions", 1980), n = rint(d log2 e),
+// r = d - n ln 2 with ln 2 split into an exact-product high part and a low
+// part, the degree-7 Taylor polynomial of e^r by Horner with fused
+// multiply-adds, and an exact scaling by 2^n; defined as 0 below d = -87.
+// Each step is one IEEE float32 operation (no contraction, no flush to zero),
+// so the CPU restatement of the same sequence gives the same bits.
+__device__ __forceinline__ float cp_expf(float d) {
+  if (!(d >= -87.0f)) return 0.0f;
+  const float n = rintf(__fmul_rn(d, 0x1.715476p+0f));
+  float r = fmaf(-n, 0x1.62e4p-1f, d);
+  r = fmaf(-n, 0x1.7f7d1cp-20f, r);
+  float p = 0x1.a01a02p-13f;
+  p = fmaf(p, r, 0x1.6c16c2p-10f);
+  p = fmaf(p, r, 0x1.111112p-7f);
+  p = fmaf(p, r, 0x1.555556p-5f);
+  p = fmaf(p, r, 0x1.555556p-3f);
+  p = fmaf(p, r, 0.5f);
+  p = fmaf(p, r, 1.0f);
+  p = fmaf(p, r, 1.0f);
+  return __fmul_rn(p, __uint_as_float((uint32_t)((int)n + 127) << 23));
+}
+
+// Two independent float32 fused multiply-adds in one instruction:
+// (c.x + a.x * b.x, c.y + a.y * b.y), each rounded once.
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  asm("{\n .reg .b64 ra, rb, rc;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n mov.b64 rc, {%0, %1};\n"
+      " fma.rn.f32x2 rc, ra, rb, rc;\n mov.b64 {%0, %1}, rc;\n}"
+      : "+f"(c.x), "+f"(c.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return c;
 }
 
 }  // namespace cpk

@@ -6,8 +6,8 @@
 //  * processing: T == 0 -> one-hot argmax (lowest index on ties).  Else
 //    z = fl32(logit / T); keep exactly min(k, V) entries by (z desc, index
 //    asc) -- one MSB-first radix select over order-preserving keys, cost
-//    independent of k; p_i = fl32(exp(z_i - zmax) / S) with S the float64
-//    sum over the kept set in ascending index order.
+//    independent of k; e_i = cp_expf(fl32(z_i - zmax)), S the sequential
+//    float32 sum of the kept e_i in ascending index order, p_i = fl32(e_i / S).
 //  * a processed row is a list (idx ascending, prob) of its support.
 //  * categorical draw: sequential float32 prefix sums S_j over entries with
 //    prob > 0 in index order; t = fl32(u * S_last); first j with S_j > t,
@@ -58,11 +58,11 @@ __device__ __forceinline__ void warp_stage_row(float* dst, const float* __restri
 
 // Processes one row of V float32 logits with one warp.  keys: warp-private
 // scratch of V uint32 (the row is staged there, then replaced by its keys);
-// hist: warp-private 256 uint32; ebuf: warp-private min(k, V) doubles;
+// hist: warp-private 256 uint32; ebuf: warp-private min(k, V) floats;
 // out_idx / out_prob: capacity min(k, V) (1 when T == 0).
 // Returns the list length (all lanes).
 static __device__ __noinline__ int warp_process_row(const float* __restrict__ logits, int V, int k, float T,
-                                                    uint32_t* keys, uint32_t* hist, double* ebuf, int* out_idx,
+                                                    uint32_t* keys, uint32_t* hist, float* ebuf, int* out_idx,
                                                     float* out_prob) {
   const int lane = threadIdx.x & 31;
   float* row = reinterpret_cast<float*>(keys);
@@ -142,8 +142,8 @@ static __device__ __noinline__ int warp_process_row(const float* __restrict__ lo
     __syncwarp();
   }
   // compaction in ascending index order (strided layout: index = j*32 + lane);
-  // each kept entry's exp(z - zmax) is computed in float64 on the way
-  const double zmax = (double)key_float(kmax);
+  // each kept entry's e = cp_expf(z - zmax) is computed on the way
+  const float zmax = key_float(kmax);
   int base = 0, eq_seen = 0;
   const unsigned lt = (1u << lane) - 1u;
   for (int j0 = 0; j0 < V; j0 += 32) {
@@ -163,17 +163,17 @@ static __device__ __noinline__ int warp_process_row(const float* __restrict__ lo
     if (sel) {
       const int pos = base + __popc(selb & lt);
       out_idx[pos] = i;
-      ebuf[pos] = exp((double)key_float(key) - zmax);
+      ebuf[pos] = cp_expf(__fsub_rn(key_float(key), zmax));
     }
     base += __popc(selb);
   }
   __syncwarp();
-  // softmax normalisation: sequential float64 sum in index order
-  double S = 0.0;
+  // softmax normalisation: sequential float32 sum in index order
+  float S = 0.0f;
   if (lane == 0)
-    for (int p = 0; p < kk; ++p) S = __dadd_rn(S, ebuf[p]);
+    for (int p = 0; p < kk; ++p) S = __fadd_rn(S, ebuf[p]);
   S = __shfl_sync(0xffffffffu, S, 0);
-  for (int p = lane; p < kk; p += 32) out_prob[p] = __double2float_rn(__ddiv_rn(ebuf[p], S));
+  for (int p = lane; p < kk; p += 32) out_prob[p] = __fdiv_rn(ebuf[p], S);
   __syncwarp();
   return kk;
 }

@@ -74,13 +74,14 @@ int window_of(const cp_spec_config* cfg) { return cfg->verify_window; }
 cp_spec_status validate(const cp_spec_model* m, const cp_spec_config* cfg, cp_spec_ctx* c) {
   if (!m || !cfg) return fail(c, CP_SPEC_E_INVALID, "null model or config");
   if (m->dtype != 0 && m->dtype != 1) return fail(c, CP_SPEC_E_INVALID, "dtype must be 0 (fp32) or 1 (bf16)");
-  if (m->hidden <= 0 || m->hidden % 8) return fail(c, CP_SPEC_E_UNSUPPORTED, "hidden must be a positive multiple of 8");
-  if (m->ffn <= 0 || m->ffn % 8) return fail(c, CP_SPEC_E_UNSUPPORTED, "ffn must be a positive multiple of 8");
+  if (m->hidden <= 0 || m->hidden % 16) return fail(c, CP_SPEC_E_UNSUPPORTED, "hidden must be a positive multiple of 16");
+  if (m->ffn <= 0 || m->ffn % 16) return fail(c, CP_SPEC_E_UNSUPPORTED, "ffn must be a positive multiple of 16");
   if (m->head_dim <= 0 || m->head_dim % 8 || m->head_dim > 256)
     return fail(c, CP_SPEC_E_UNSUPPORTED, "head_dim must be a multiple of 8 in [8, 256]");
   if (m->n_q_heads <= 0 || m->n_kv_heads <= 0 || m->n_q_heads % m->n_kv_heads)
     return fail(c, CP_SPEC_E_UNSUPPORTED, "n_q_heads must be a positive multiple of n_kv_heads");
-  if ((m->n_q_heads * m->head_dim) % 8) return fail(c, CP_SPEC_E_UNSUPPORTED, "n_q_heads*head_dim must be a multiple of 8");
+  if ((m->n_q_heads * m->head_dim) % 16)
+    return fail(c, CP_SPEC_E_UNSUPPORTED, "n_q_heads*head_dim must be a multiple of 16");
   if (m->n_layers < 1 || m->n_layers > CP_SPEC_MAX_LAYERS) return fail(c, CP_SPEC_E_UNSUPPORTED, "n_layers must be in [1, 64]");
   if (m->num_code_groups < 2 || m->num_code_groups > CP_SPEC_MAX_CODE_GROUPS)
     return fail(c, CP_SPEC_E_INVALID, "num_code_groups must be in [2, 64]");
@@ -118,39 +119,87 @@ cpk::Layout layout_for(const cp_spec_model* m, const cp_spec_config* cfg, int N)
 }
 
 struct SmemPlan {
-  int RB, proc_warps, accept_warps, attn_warps, slot_bytes;
+  int nslots, slot_bytes, accept_warps, uni_floats, red_floats, hown_cap;
+  int off_ring, off_uni, off_red, off_hown, off_rope;
   size_t bytes;
 };
 
-constexpr size_t kDynSmemLimit = 216 * 1024;  // dynamic shared memory per CTA (static use is ~7 KB)
+// Dynamic shared memory per CTA; the static part (parameter copy, CTA
+// state, top-k histogram) is about 9.6 KB of the 227 KB an SM offers.
+constexpr size_t kDynSmemLimit = 216 * 1024;
+constexpr size_t kMaxSlotBytes = 32 * 1024;
+constexpr size_t kMaxRingBytes = 160 * 1024;
+constexpr size_t kMaxRopeBytes = 16 * 1024;
+constexpr int kKPartHost = 512;  // input elements per GEMV task part (matches the kernel)
+constexpr int kMaxTileRowsHost = 64;
 
 // Dynamic shared memory of the frame kernel:
-// [active rows + positions][2 weight-stream slots][union of the phase scratch areas].
-SmemPlan smem_plan(const cp_spec_model* m, int N, int KC, int Bmax) {
+// [row lists][owned residual rows][RoPE table][weight ring][GEMV partial sums][phase scratch].
+SmemPlan smem_plan(const cp_spec_model* m, int N, int KC, int Bmax, int grid) {
   const int NS = N > 2 ? N : 2;
   const size_t eb = m->dtype == 1 ? 2 : 4;
-  const int Kmax = std::max(std::max(m->hidden, m->n_q_heads * m->head_dim), m->ffn);
-  const size_t rows = ((size_t)Bmax * NS * 8 + 127) / 128 * 128;
-  const size_t pair = ((2 * (size_t)Kmax * eb) + 127) / 128 * 128;
-  size_t slot = std::max<size_t>(pair, 56 * 1024);
-  const size_t per_attn = ((size_t)33 * m->head_dim + 64) * 4;
+  const int H = m->hidden, F = m->ffn, QD = m->n_q_heads * m->head_dim, V = m->vocab, G = m->num_code_groups;
+  const int d = m->head_dim;
+  auto kstride = [&](int K) { return m->dtype == 1 ? (K + 255) / 256 * 256 : K; };
+  const int KSmax = std::max(std::max(kstride(H), kstride(QD)), kstride(F));
+  const size_t max_unit = (size_t)std::max(std::max(2 * H, QD), F) * eb;
+  const size_t max_row = (size_t)std::max(std::max(H, QD), F) * eb;
+  const int rows = Bmax * NS;
+  const size_t rows_b = ((size_t)rows * 12 + 127) / 128 * 128;
+  const int hown_cap = (H + grid - 1) / grid + 1;
+  const size_t hown_b = ((size_t)rows * hown_cap * 4 + 127) / 128 * 128;
+  const size_t rope_raw = (size_t)G * (d / 2) * 8;
+  const size_t rope_b = rope_raw <= kMaxRopeBytes ? (rope_raw + 127) / 128 * 128 : 0;
   const size_t per_acc = cpk::accept_scratch_bytes(NS, KC);
-  const size_t proc = ((size_t)m->vocab * 4 + 15) / 16 * 16 + 128 + (size_t)KC * 8;
-  SmemPlan best{0, 1, 0, 0, 0, 0};
-  for (; slot >= pair; slot -= 8 * 1024) {
-    if (rows + 2 * slot >= kDynSmemLimit) continue;
-    const size_t budget = kDynSmemLimit - rows - 2 * slot;
-    int RB = 8;
-    auto gemv = [&](int rb) {
-      return (size_t)rb * Kmax * 4 + (size_t)2 * cpk::kWarps * 2 * rb * 4 + (size_t)rb * (m->head_dim / 2) * 8;
-    };
-    while (RB > 1 && gemv(RB) > budget) RB /= 2;
-    const int tw = (int)std::min<size_t>(cpk::kWarps, budget / per_attn);
-    const int aw = (int)std::min<size_t>(cpk::kWarps, budget / per_acc);
-    if (gemv(RB) > budget || tw < 1 || aw < 1 || proc > budget) continue;
-    const size_t uni = std::max(std::max(gemv(RB), per_attn * tw), std::max(proc, per_acc * aw));
-    best = SmemPlan{RB, 1, aw, tw, (int)slot, rows + 2 * slot + uni};
-    break;
+  const size_t topk_b = ((size_t)V * 4 + 15) / 16 * 16 + (size_t)cpk::kWarps * 1024 + ((size_t)KC * 4 + 15) / 16 * 16 + 256;
+  const size_t attn_b = ((size_t)64 + (size_t)G * d) * 4;
+  // GEMV tasks read up to kRB - 1 rows past a tile's end: the scratch after the ring covers that
+  const size_t uni_fixed = std::max(std::max(std::max(topk_b, per_acc), attn_b), (size_t)(cpk::kRB - 1) * max_row);
+  const int QGmax = (std::min(rows, 16) + 3) / 4;  // staged row groups never exceed 16 rows
+  SmemPlan best{};
+  // staged input rows: every row of a single-stream pass when that leaves a
+  // ring of at least three 32 KB slots, else four
+  const int want_rows[2] = {std::min(rows, 8), std::min(rows, 4)};
+  for (int a = 0; a < 2 && best.bytes == 0; ++a) {
+    const size_t uni = std::max(uni_fixed, (size_t)want_rows[a] * KSmax * 4);
+    for (size_t slot = kMaxSlotBytes; slot >= max_unit && best.bytes == 0; slot -= 4096) {
+      // partial sums of one wave of tiles: (8-row batches x input parts x row groups) x 32 per tile
+      size_t tmax = 0;
+      auto tstride_of = [&](int K, int rpu) {
+        const int upt = std::max(1, std::min((int)(slot / ((size_t)rpu * K * eb)), kMaxTileRowsHost / rpu));
+        const int KP = (K + kKPartHost - 1) / kKPartHost;
+        tmax = std::max(tmax, (size_t)((upt * rpu + cpk::kRB - 1) / cpk::kRB) * KP * QGmax * cpk::kRedPerTask);
+      };
+      tstride_of(H, 2);
+      tstride_of(QD, 1);
+      tstride_of(F, 1);
+      tstride_of(H, 1);
+      for (int ns = cpk::kMaxSlots; ns >= (a == 0 ? 3 : 2); --ns) {
+        if ((size_t)ns * slot > kMaxRingBytes) continue;
+        const size_t red_floats = (size_t)std::max(1, ns - 2) * tmax;
+        const size_t red_b = (red_floats * 4 + 127) / 128 * 128;
+        const size_t fixed = rows_b + hown_b + rope_b + red_b;
+        if (fixed + (size_t)ns * slot + uni > kDynSmemLimit) continue;
+        // GEMV tasks read up to kRB - 1 rows past a tile's end: keep that much after the ring
+        if (red_b + uni < (size_t)(cpk::kRB - 1) * max_row) continue;
+        SmemPlan p{};
+        p.nslots = ns;
+        p.slot_bytes = (int)slot;
+        p.hown_cap = hown_cap;
+        p.red_floats = (int)red_floats;
+        p.off_hown = (int)rows_b;
+        p.off_rope = rope_b ? (int)(rows_b + hown_b) : -1;
+        p.off_ring = (int)(rows_b + hown_b + rope_b);
+        p.off_red = (int)(p.off_ring + (size_t)ns * slot);
+        p.off_uni = (int)(p.off_red + red_b);
+        const size_t uni_all = (kDynSmemLimit - fixed - (size_t)ns * slot) / 16 * 16;
+        p.uni_floats = (int)(uni_all / 4);
+        p.accept_warps = (int)std::min<size_t>(cpk::kWarps, uni_all / per_acc);
+        p.bytes = (size_t)p.off_uni + uni_all;
+        best = p;
+        break;
+      }
+    }
   }
   return best;
 }
@@ -189,15 +238,7 @@ cp_spec_status plan_device(const cp_spec_model* model, const cp_spec_config* con
   if (e != cudaSuccess) return check_cuda(nullptr, e, "device query");
   if (!coop) return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "device does not support cooperative launches");
   const int KC = list_capacity(model, config);
-  const SmemPlan sp = smem_plan(model, N, KC, config->max_streams);
-  {
-    // a GEMV task keeps at most 8 warps x 32 lanes x 4 chunks of 16 bytes of a row in registers
-    const int epc = model->dtype == 1 ? 8 : 4;
-    const int kmax = std::max(std::max(model->hidden, model->n_q_heads * model->head_dim), model->ffn);
-    if (kmax > cpk::kWarps * 32 * 4 * epc)
-      return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "input width %d above %d for this weight dtype", kmax,
-                  cpk::kWarps * 32 * 4 * epc);
-  }
+  const SmemPlan sp = smem_plan(model, N, KC, config->max_streams, sms);
   if (sp.bytes == 0)
     return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "shapes do not fit the frame kernel's shared memory (top_k %d, window %d)",
                 config->top_k, config->verify_window);
@@ -225,10 +266,16 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
   P.H = model->hidden; P.L = L; P.nq = model->n_q_heads; P.nkv = model->n_kv_heads; P.d = model->head_dim;
   P.F = model->ffn; P.V = model->vocab; P.G = model->num_code_groups; P.dtype = model->dtype;
   P.eps = model->rms_eps;
-  P.N = N; P.NS = NS; P.ND = N > 1 ? N - 1 : 0; P.KC = dp.KC; P.RB = dp.sp.RB; P.proc_warps = dp.sp.proc_warps;
-  P.accept_warps = dp.sp.accept_warps;
-  P.attn_warps = dp.sp.attn_warps;
+  P.N = N; P.NS = NS; P.ND = N > 1 ? N - 1 : 0; P.KC = dp.KC;
+  P.Bmax = config->max_streams;
+  P.nslots = dp.sp.nslots;
   P.slot_bytes = dp.sp.slot_bytes;
+  P.accept_warps = dp.sp.accept_warps;
+  P.off_ring = dp.sp.off_ring; P.off_uni = dp.sp.off_uni; P.off_red = dp.sp.off_red; P.off_hown = dp.sp.off_hown;
+  P.off_rope = dp.sp.off_rope;
+  P.uni_floats = dp.sp.uni_floats;
+  P.red_floats = dp.sp.red_floats;
+  P.hown_cap = dp.sp.hown_cap;
   P.seed = config->seed;
   P.timeout_ns = kBarrierTimeoutNs;
   const long long eb = model->dtype == 1 ? 2 : 4;
@@ -242,11 +289,12 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
     P.wv[l] = weights->wv[l]; P.wo[l] = weights->wo[l]; P.ffn_norm[l] = weights->ffn_norm[l];
     P.w_gate[l] = weights->w_gate[l]; P.w_up[l] = weights->w_up[l]; P.w_down[l] = weights->w_down[l];
   }
-  P.kv = at<float>(ws, lay.kv); P.h = at<float>(ws, lay.h); P.qbuf = at<float>(ws, lay.qbuf);
-  P.obuf = at<float>(ws, lay.obuf); P.act = at<float>(ws, lay.act); P.logits = at<float>(ws, lay.logits);
-  P.lidx = at<int>(ws, lay.lidx); P.lprob = at<float>(ws, lay.lprob); P.lcount = at<int>(ws, lay.lcount);
+  P.hpub = at<cpk::xel>(ws, lay.hpub); P.qpub = at<cpk::xel>(ws, lay.qpub); P.opub = at<cpk::xel>(ws, lay.opub);
+  P.apub = at<cpk::xel>(ws, lay.apub); P.kv = at<cpk::xel>(ws, lay.kv); P.logits = at<cpk::xel>(ws, lay.logits);
+  P.lidx = at<int>(ws, lay.lidx); P.lprob = at<float>(ws, lay.lprob);
+  P.lflag = at<unsigned long long>(ws, lay.lflag);
   P.qidx = at<int>(ws, lay.qidx); P.qprob = at<float>(ws, lay.qprob); P.qcount = at<int>(ws, lay.qcount);
-  P.row_pos = at<int>(ws, lay.row_pos); P.st = at<cpk::StreamState>(ws, lay.st);
+  P.row_pos = at<int>(ws, lay.row_pos); P.row_code = at<int>(ws, lay.row_code); P.st = at<cpk::StreamState>(ws, lay.st);
   P.sstats = at<cpk::StreamStats>(ws, lay.sstats); P.rope = at<float2>(ws, lay.rope);
   P.top_k = at<int>(ws, lay.top_k); P.temp = at<float>(ws, lay.temp); P.ctl = at<cpk::Control>(ws, lay.ctl);
 }
