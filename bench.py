@@ -105,23 +105,23 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-FRAME_KERNEL_SOURCES = ("cp_common.cuh", "cp_sampling.cuh", "cp_frame.cuh", "cp_frame_kernel.cu")
+PASS_KERNEL_SOURCES = ("cp_common.cuh", "cp_sampling.cuh", "cp_frame.cuh", "cp_pass_kernels.cu")
 
 
 def kernel_source_hash():
-    """Hash of the sources the frame kernel is compiled from (host-side files excluded)."""
+    """Hash of the sources the pass kernels are compiled from."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "speculative_decoding_rvq_gb300", "csrc")
-    for fn in FRAME_KERNEL_SOURCES:
+    for fn in PASS_KERNEL_SOURCES:
         h.update(open(os.path.join(csrc, fn), "rb").read())
     return h.hexdigest()[:16]
 
 
 def recorded_traffic():
-    """DRAM bytes per decoder pass of the frame kernel from the committed ncu summary,
-    if it was taken on the current kernel sources (else None).  Every pass streams the
-    same weights, so a launch's traffic scales with its number of passes."""
-    p = os.path.join(ROOT, "profiles", "frame_kernel_traffic.json")
+    """DRAM bytes per decoder pass (the pass's kernels summed) from the committed ncu
+    summary, if it was taken on the current kernel sources (else None).  Every pass
+    streams the same weights, so a step's traffic scales with its number of passes."""
+    p = os.path.join(ROOT, "profiles", "pass_kernels_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
@@ -173,7 +173,6 @@ def run_gpu(args, rank, world):
     torch.cuda.synchronize()
     cp.status()
     cp.reset_stats()
-    l0 = cp.launch_count()
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     if world > 1:
         torch.distributed.barrier()
@@ -192,7 +191,6 @@ def run_gpu(args, rank, world):
         torch.distributed.barrier()
     total_ms = t0.elapsed_time(t1)
     launch_ms = [a.elapsed_time(b) for a, b in ev]
-    launches = cp.launch_count() - l0
     st = cp.stats()
     cp.status()
     codes_total = args.steps * frames * (spec.num_code_groups - 1)
@@ -207,7 +205,8 @@ def run_gpu(args, rank, world):
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                 "traffic": (round(traffic_pp * passes) if traffic_pp else None),
-                "kernel": "frame_kernel<bf16> (one cooperative launch per step)",
+                "kernel": "verify pass: the call graph's pass kernels (5 per layer + lm_heads, top-k, accept), "
+                          "timed per step; GEMV kernels are 21 of the 28 per pass",
                 "algorithmic_bytes_per_launch": int(per_launch_bytes),
                 "mean_launch_ms": round(statistics.mean(launch_ms), 3)}
     rounds = st["rounds"] / args.steps
@@ -216,7 +215,7 @@ def run_gpu(args, rank, world):
         "warmup": args.warmup, "ms_per_step": round(total_ms / args.steps, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": dict(workload_config(spec, frames, 1, args.window), parallelism=f"replicas x{world}"),
-        "roofline": roofline, "gpu_launches": int(launches),
+        "roofline": roofline, "gpu_launches": int(st["kernel_launches"] + args.steps),
         "decode": {"passes_per_frame": round(passes / frames, 3),
                    "codes_per_round": round((frames * (spec.num_code_groups - 2)) / max(rounds, 1), 3),
                    "accepted_by_offset": st["accepted_by_offset"][1:args.window],
@@ -368,6 +367,34 @@ def run_reference(args, rank, world):
     }
 
 
+def profile_rounds(args):
+    """Profiling case for ncu: the default workload's model, one stream, `args.profile_rounds`
+    decoder passes through the step-wise API (cp_spec_round launches the pass kernels
+    directly, so a profiler sees each kernel launch; inside the call graph the pass
+    kernels run under a device-side loop).  Prints one status line."""
+    import torch
+    from speculative_decoding_rvq_gb300 import binding, synth as S
+    spec = S.TTS06B_BF16
+    dw = binding.weights_to_device(spec, S.gen_weights(spec, 0))
+    x, c0 = S.gen_frames(spec, 1, 8, seed=1)
+    xd, cd = torch.from_numpy(x).cuda(), torch.from_numpy(c0).cuda()
+    cp = binding.CpSpec(spec, dw, args.window, TOP_K, TEMP, SEED, 1)
+    codes = torch.zeros((1, spec.num_code_groups), dtype=torch.int32, device="cuda")
+    done, f = 0, 0
+    while done < args.profile_rounds:
+        cp.begin_frame(xd[f].clone(), cd[f].clone(), f)
+        for _ in range(spec.num_code_groups - 1):
+            cp.round(codes)
+            done += 1
+            if done >= args.profile_rounds:
+                break
+        f = (f + 1) % 8
+    torch.cuda.synchronize()
+    cp.status()
+    st = cp.stats()
+    print(json.dumps({"profile_rounds": done, "passes": st["passes"], "kernel_launches": st["kernel_launches"]}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -379,7 +406,12 @@ def main():
     ap.add_argument("--ref-frames", type=int, default=2)
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-rounds", type=int, default=0,
+                    help="run this many step-wise passes (direct kernel launches, for a profiler) and exit")
     args = ap.parse_args()
+    if args.profile_rounds > 0:
+        profile_rounds(args)
+        return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":

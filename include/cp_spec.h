@@ -33,8 +33,8 @@
  *  - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *    stream).  Calls enqueue work on it and return without synchronising,
  *    except where stated.  Argument errors are returned synchronously and
- *    enqueue nothing.  Device-side errors (bad code index, a grid barrier
- *    that timed out) are recorded in a device status word and reported by
+ *    enqueue nothing.  Device-side errors (bad code index, a weight tile
+ *    copy that did not land in time) are recorded in a device status word and reported by
  *    cp_spec_status_word() or by the next call on the same context.
  *  - Randomness is Philox4x32-10 (Salmon et al., SC'11) with counter
  *    (stream id, frame index, depth, purpose) and key = (seed mod 2^32,
@@ -133,11 +133,10 @@ typedef struct {
   int64_t drafted_by_offset[9];
   int64_t accepted_by_offset[9];
   int64_t weight_bytes, kv_bytes, heads_applied;
-  /* Critical-path nanoseconds per pass phase, measured on the GPU between
-   * grid barriers: [0] QKV+RoPE+KV append, [1] attention, [2] O projection,
-   * [3] RMSNorm+gate/up+SwiGLU, [4] down projection, [5] lm_heads,
-   * [6] top-k/softmax, [7] accept/commit/stage. */
-  int64_t phase_ns[8];
+  /* Pass kernels executed on the device (5 per layer + lm_heads, top-k and
+   * accept, per pass; counted by the accept kernel). */
+  int64_t kernel_launches;
+  int64_t reserved[7];
 } cp_spec_stats;
 
 typedef struct cp_spec_ctx cp_spec_ctx;
@@ -168,8 +167,11 @@ cp_spec_status cp_spec_set_stream_sampling(cp_spec_ctx* ctx, int32_t n, const in
  * d_x: [n_frames][n_streams][H] float32 talker hiddens; d_c0: [n_frames][n_streams]
  * int32 first codes; d_codes (out): [n_frames][n_streams][G] int32, with
  * d_codes[f][b][0] = c_0.  Frame f uses Philox frame index first_frame + f.
- * One launch on `stream`; streams advance through their frames independently.
- * Asynchronous. */
+ * One launch of the context's call graph on `stream` (a setup kernel, then
+ * a device-controlled loop of decoder passes, 5 L + 3 kernels each, until
+ * every stream has finished its frames; the graph is built and instantiated
+ * on the first call, in host memory); streams advance through their frames
+ * independently.  Asynchronous. */
 cp_spec_status cp_spec_decode_frames(cp_spec_ctx* ctx, int32_t n_streams, int32_t n_frames,
                                      int32_t first_frame, const float* d_x, const int32_t* d_c0,
                                      int32_t* d_codes, void* stream);
@@ -241,7 +243,10 @@ cp_spec_status cp_spec_accept_batch(int32_t R, int32_t N, int32_t V, int32_t top
  *
  * The first call on each device looks up the scratch address
  * (cudaGetSymbolAddress, which may load the module) and caches it; make that
- * first call before any stream capture begins.  All calls on one device share
+ * first call before any stream capture begins.  The decode runs as a call
+ * graph (host objects, no device allocation by the library) that is cached
+ * per device and rebuilt, after a device synchronisation, when the model,
+ * weights or configuration change.  All calls on one device share
  * the one scratch array: calls whose work overlaps in time (different
  * streams, or threads without ordering) race on it and give wrong results.
  * Order them on one stream.  Launches count in the context-free counter of
@@ -259,9 +264,11 @@ cp_spec_status cp_spec_status_word(cp_spec_ctx* ctx, void* stream);
 cp_spec_status cp_spec_read_stats(cp_spec_ctx* ctx, cp_spec_stats* h_stats, void* stream);
 cp_spec_status cp_spec_reset_stats(cp_spec_ctx* ctx, void* stream);
 
-/* Number of kernel launches the library has enqueued on this context
- * (cp_spec_accept_batch and cp_spec_decode_frames_static count in a
- * process-wide counter, ctx = NULL). */
+/* Number of launches the library has enqueued on this context: kernels
+ * launched directly, plus one per launch of the context's call graph (whose
+ * pass kernels are counted on the device: cp_spec_stats.kernel_launches).
+ * cp_spec_accept_batch and cp_spec_decode_frames_static count in a
+ * process-wide counter, ctx = NULL. */
 int64_t cp_spec_launch_count(const cp_spec_ctx* ctx);
 
 /* Last error message of the context (or of the last context-free call when

@@ -54,11 +54,10 @@ class Config(C.Structure):
 class Stats(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("frames", "passes", "rounds", "committed", "bonus", "rejections")] + [
         ("drafted_by_offset", C.c_int64 * 9), ("accepted_by_offset", C.c_int64 * 9)] + [
-        (n, C.c_int64) for n in ("weight_bytes", "kv_bytes", "heads_applied")] + [("phase_ns", C.c_int64 * 8)]
+        (n, C.c_int64) for n in ("weight_bytes", "kv_bytes", "heads_applied", "kernel_launches")] + [("reserved", C.c_int64 * 7)]
 
     def as_dict(self) -> dict:
-        d = {n: int(getattr(self, n)) for n, _ in self._fields_ if not n.endswith("_offset") and n != "phase_ns"}
-        d["phase_ns"] = [int(v) for v in self.phase_ns]
+        d = {n: int(getattr(self, n)) for n, _ in self._fields_ if not n.endswith("_offset") and n != "reserved"}
         d["drafted_by_offset"] = [int(v) for v in self.drafted_by_offset]
         d["accepted_by_offset"] = [int(v) for v in self.accepted_by_offset]
         return d

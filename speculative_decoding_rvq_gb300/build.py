@@ -17,7 +17,7 @@ INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libcpspec.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["cp_spec.cu", "cp_frame_kernel.cu", "cp_accept_kernel.cu"]
+SOURCES = ["cp_spec.cu", "cp_pass_kernels.cu", "cp_accept_kernel.cu"]
 
 
 def _nvcc() -> str:

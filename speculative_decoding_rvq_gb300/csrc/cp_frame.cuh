@@ -1,5 +1,12 @@
-// cp_frame.cuh -- parameter block and workspace layout of the persistent
-// frame kernel (shared by the kernel and the host-side C ABI).
+// cp_frame.cuh -- parameter block and workspace layout of the pass kernels
+// (shared by the kernels and the host-side C ABI).
+//
+// One decoder pass (the verify forward of every active stream's rows, the
+// lm_heads, top-k and acceptance) is a chain of 5 L + 3 kernels; consecutive
+// kernels overlap through programmatic dependent launch and the chain runs
+// inside a CUDA graph whose while loop repeats passes until every stream is
+// done.  Kernels exchange data through the plain fp32 buffers below; the
+// kernel boundary orders every write before every read of the next kernel.
 #pragma once
 #include <stdint.h>
 
@@ -10,24 +17,17 @@ namespace cpk {
 enum StreamPhase : int { kPhasePrefill = 0, kPhaseAR = 1, kPhaseSpec = 2, kPhaseTeacher = 3, kPhaseDone = 4 };
 enum RunMode : int { kModeDecode = 0, kModeTeacher = 1 };
 
-// A CTA is kWarps consumer warps (all compute, sampling and acceptance) plus
-// one producer warp that only streams weight tiles into shared memory.  Eight
-// warps in all keep two warps per SM sub-partition, so a thread may hold up
-// to 255 registers (nine would cap it at 168 and force spills).
-constexpr int kWarps = 7;
-constexpr int kConsumers = kWarps * 32;
-constexpr int kThreads = kConsumers + 32;
-constexpr int kMaxSlots = 8;        // weight-stream ring depth
-constexpr int kMaxTiles = 40;       // tiles of one GEMV kind per CTA
-constexpr int kKPart = 512;         // input elements per lane group of a GEMV task (16 per lane)
-constexpr int kMaxTileRows = 64;    // weight rows per tile
-constexpr int kRB = 4;              // weight rows per GEMV task (a batch)
-constexpr int kRedPerTask = kRB * 4;  // partial sums a task writes (batch row x input row)
+constexpr int kThreads = 256;               // threads of every pass kernel
+constexpr int kWarps = kThreads / 32;
+constexpr int kSlotBytes = 48 * 1024;       // GEMV weight tile (two slots per CTA)
+constexpr int kRB = 4;                      // weight rows per GEMV batch
+constexpr int kMaxTileRows = 192;           // rows of one weight tile (bounds the partial-sum buffer)
+constexpr int kMaxHeadsPerPass = 64;
 
-// GEMV kinds, in weight-stream order within a layer; kHeads closes a pass.
+// GEMV kinds, in pass order within a layer; kHeads closes a pass.
 enum GemvKind : int { kQKV = 0, kO = 1, kGU = 2, kDown = 3, kHeads = 4 };
 
-// Per-stream device state (one warp owns it in the accept phase).
+// Per-stream device state (one warp owns it in the accept kernel).
 struct StreamState {
   int phase;      // StreamPhase of the pass that is in flight
   int frame;      // frame index within the current launch sequence
@@ -46,23 +46,44 @@ struct StreamStats {
   long long drafted[9], accepted[9];
 };
 
-// Persistent control words (survive across launches, except `bar`).
+// Persistent control words.
 struct Control {
-  unsigned long long bar;            // grid barrier counter, zeroed before each launch
-  unsigned long long head_mask[2];   // lm_heads needed by the next pass (double-buffered by pass parity)
   long long weight_bytes, kv_bytes, heads_applied, passes;
-  long long phase_ns[8];             // ns per phase kind as seen by CTA 0
+  long long phase_ns[8];             // reserved (zero)
+  long long kernels;                 // pass kernels executed
   int active;                        // streams with frames left
-  int pass_global;                   // passes run since init: parity of head_mask, exchange flags
   int status;                        // device status word (cp_spec_status values)
-  int pad;
-  int dbg_pass, dbg_phase, dbg_active, dbg_gen;  // progress record of CTA 0 (diagnostics)
+  int done;                          // CTAs of the current setup/accept kernel that finished (last-CTA election)
+  int pass;                          // passes of the current call
+  int pad[4];
+};
+constexpr int kControlCounters = 13;  // long longs reset by cp_spec_reset_stats, from weight_bytes
+
+// The rows of the pass in flight, compacted, and the lm_heads it applies.
+struct Plan {
+  int nrows;
+  int nheads;
+  int heads[kMaxHeadsPerPass];
 };
 
-// An exchange element: a float32 value in the low word and the flag of the
-// pass that wrote it in the high word, stored with one 64-bit access so a
-// reader that sees the flag sees the value.
-typedef unsigned long long xel;
+// What changes from call to call (in device memory, written before launch).
+struct CallArgs {
+  int mode;        // RunMode
+  int B;           // streams
+  int n_frames;
+  int first_frame;
+  int max_passes;  // 0 = until every stream finished
+  int P;           // teacher positions
+  int pass_cap;    // passes after which the loop stops with a device error
+  int pad;
+  const float* x;        // [n_frames][B][H]
+  const int* c0;         // [n_frames][B]
+  int* codes_out;        // [n_frames][B][G]
+  int* committed_out;    // [B] or null
+  const int* t_codes;    // [B][P-1]
+  float* t_logits;       // [B][P-1][V]
+  float* t_draft;        // [B][P-1][ND][V] or null
+};
 
 struct FrameParams {
   // model
@@ -72,17 +93,10 @@ struct FrameParams {
   int NS;   // row slots per stream = max(N, 2)
   int ND;   // draft logit slots per row = max(N - 1, 0)
   int KC;   // list capacity = min(max top_k, V) rounded up to a multiple of 4
-  // plan (host-computed)
-  int Bmax;          // stream capacity of the workspace (row slots = Bmax * NS)
-  int nslots;        // weight-stream ring depth
-  int slot_bytes;    // bytes per ring slot
-  int accept_warps;  // warps per CTA that own streams in the accept phase
-  int off_ring, off_uni, off_red, off_hown, off_rope;  // dynamic shared memory carve-up (bytes; rope -1 = global)
-  int uni_floats;    // phase scratch capacity (staged activations, top-k, acceptance)
-  int red_floats;    // GEMV partial sums of one phase (floats)
-  int hown_cap;      // owned residual values per active row in shared memory
+  int Bmax; // stream capacity of the workspace (row slots = Bmax * NS)
+  int kernels_per_pass;
   unsigned long long seed;
-  unsigned long long timeout_ns;
+  unsigned long long cond;            // graph conditional handle of the pass loop (0 = none)
   long long layer_bytes, head_bytes;  // algorithmic bytes per layer / per lm_head
   const void* embed;
   const void* head;
@@ -96,45 +110,35 @@ struct FrameParams {
   const void* w_gate[CP_SPEC_MAX_LAYERS];
   const void* w_up[CP_SPEC_MAX_LAYERS];
   const void* w_down[CP_SPEC_MAX_LAYERS];
-  // workspace: exchange buffers (xel) written once per pass, indexed by row slot
-  xel* hpub;       // [L][2][Bmax*NS][H]  residual after O (0) and after down (1)
-  xel* qpub;       // [L][Bmax*NS][nq*d]  query rows after RoPE
-  xel* opub;       // [L][Bmax*NS][nq*d]  attention outputs
-  xel* apub;       // [L][Bmax*NS][F]     SwiGLU activations
-  xel* kv;         // [Bmax][L][2][G][nkv][d]
-  xel* logits;     // [Bmax*NS][1+ND][V]
+  // workspace (row slot r = b * NS + k)
+  float* h;        // [Bmax*NS][H]     residual stream
+  float* qbuf;     // [Bmax*NS][nq*d]  queries after RoPE
+  float* abuf;     // [Bmax*NS][nq*d]  attention outputs
+  float* fbuf;     // [Bmax*NS][F]     SwiGLU activations
+  float* kv;       // [Bmax][L][2][G][nkv][d]
+  float* logits;   // [Bmax*NS][1+ND][V]
   int* lidx;       // [Bmax*NS][1+ND][KC]
   float* lprob;    // [Bmax*NS][1+ND][KC]
-  unsigned long long* lflag;  // [Bmax*NS][1+ND]: count | flag << 32 (release store)
+  int* lcount;     // [Bmax*NS][1+ND]
   int* qidx;       // [Bmax][max(ND,1)][KC]
   float* qprob;    // [Bmax][max(ND,1)][KC]
   int* qcount;     // [Bmax][max(ND,1)]
   int* row_pos;    // [Bmax*NS] position, -1 = inactive
   int* row_code;   // [Bmax*NS] code whose embedding is the row input (frame index at position 0)
+  int* prow;       // [Bmax*NS] the pass's active row slots, ascending
+  int* ppos;       // [Bmax*NS] their positions
+  int* pcode;      // [Bmax*NS] their input codes
+  Plan* plan;
   StreamState* st; // [Bmax]
   StreamStats* sstats;  // [Bmax]
   float2* rope;    // [G][d/2] (cos, sin)
   int* top_k;      // [Bmax]
   float* temp;     // [Bmax]
   Control* ctl;
-  // this launch
-  int mode;        // RunMode
-  int B;           // streams
-  int n_frames;
-  int first_frame;
-  int max_passes;  // 0 = until every stream finished
-  int do_setup;    // stage the first frame / teacher chunk before the first pass
-  const float* x;  // [n_frames][B][H]
-  const int* c0;   // [n_frames][B]
-  int* codes_out;  // [n_frames][B][G]
-  int* committed_out;  // [B] or null
-  int P;                 // teacher positions
-  const int* t_codes;    // [B][P-1]
-  float* t_logits;       // [B][P-1][V]
-  float* t_draft;        // [B][P-1][ND][V] or null
+  CallArgs* call;
 };
 
-// Per-warp shared scratch of the accept phase: the stream state plus 2*NS
+// Per-warp shared scratch of the accept kernel: the stream state plus 2*NS
 // staged probability lists (index and probability arrays of capacity KC)
 // and their lengths.
 inline __host__ __device__ size_t accept_scratch_bytes(int NS, int KC) {
@@ -143,8 +147,8 @@ inline __host__ __device__ size_t accept_scratch_bytes(int NS, int KC) {
 
 // Workspace carve-up, computed identically by the host for sizing.
 struct Layout {
-  size_t hpub, qpub, opub, apub, kv, logits, lidx, lprob, lflag, qidx, qprob, qcount, row_pos, row_code, st,
-      sstats, rope, top_k, temp, ctl, total;
+  size_t h, qbuf, abuf, fbuf, kv, logits, lidx, lprob, lcount, qidx, qprob, qcount, row_pos, row_code, prow, ppos,
+      pcode, plan, st, sstats, rope, top_k, temp, ctl, call, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -152,30 +156,34 @@ inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 inline Layout make_layout(int H, int L, int nq, int nkv, int d, int F, int V, int G, int N, int KC, int Bmax) {
   const int NS = N > 2 ? N : 2, ND = N > 1 ? N - 1 : 0, NDq = ND > 0 ? ND : 1;
   const size_t rows = (size_t)Bmax * NS;
-  const size_t X = sizeof(xel);
   Layout o{};
   size_t off = 0;
   auto take = [&](size_t bytes) { size_t at = off; off = align_up(off + bytes, 256); return at; };
-  o.hpub = take(X * L * 2 * rows * H);
-  o.qpub = take(X * L * rows * nq * d);
-  o.opub = take(X * L * rows * nq * d);
-  o.apub = take(X * L * rows * F);
-  o.kv = take(X * (size_t)Bmax * L * 2 * G * nkv * d);
-  o.logits = take(X * rows * (1 + ND) * V);
+  o.h = take(4 * rows * H);
+  o.qbuf = take(4 * rows * nq * d);
+  o.abuf = take(4 * rows * nq * d);
+  o.fbuf = take(4 * rows * F);
+  o.kv = take(4 * (size_t)Bmax * L * 2 * G * nkv * d);
+  o.logits = take(4 * rows * (1 + ND) * V);
   o.lidx = take(sizeof(int) * rows * (1 + ND) * KC);
   o.lprob = take(sizeof(float) * rows * (1 + ND) * KC);
-  o.lflag = take(8 * rows * (1 + ND));
+  o.lcount = take(sizeof(int) * rows * (1 + ND));
   o.qidx = take(sizeof(int) * (size_t)Bmax * NDq * KC);
   o.qprob = take(sizeof(float) * (size_t)Bmax * NDq * KC);
   o.qcount = take(sizeof(int) * (size_t)Bmax * NDq);
   o.row_pos = take(sizeof(int) * rows);
   o.row_code = take(sizeof(int) * rows);
+  o.prow = take(sizeof(int) * rows);
+  o.ppos = take(sizeof(int) * rows);
+  o.pcode = take(sizeof(int) * rows);
+  o.plan = take(sizeof(Plan));
   o.st = take(sizeof(StreamState) * (size_t)Bmax);
   o.sstats = take(sizeof(StreamStats) * (size_t)Bmax);
   o.rope = take(sizeof(float) * 2 * (size_t)G * (d / 2));
   o.top_k = take(sizeof(int) * (size_t)Bmax);
   o.temp = take(sizeof(float) * (size_t)Bmax);
   o.ctl = take(sizeof(Control));
+  o.call = take(sizeof(CallArgs));
   o.total = off;
   return o;
 }

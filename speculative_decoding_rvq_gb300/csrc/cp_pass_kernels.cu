@@ -1,0 +1,1547 @@
+// cp_pass_kernels.cu -- the kernels of one decoder pass and their launches.
+//
+// A pass ("CodePredictor Speculative Decoding", "How a round works") is, for
+// every active stream, one causal CodePredictor forward over its rows (the
+// committed position plus the drafted ones) against the stream's KV cache,
+// the lm_heads of those rows (the target heads and, on the row at the
+// committed depth, the draft heads head_{s+1..s+N-1}: "Why the draft is
+// free"), top-k / temperature processing of every logit row, and the exact
+// acceptance that commits codes and stages the next pass.  It runs as
+//
+//   per layer: QKV GEMV (RMSNorm, RoPE, KV append) -> attention -> O GEMV
+//              (residual) -> gate/up GEMV (RMSNorm, SwiGLU) -> down GEMV
+//              (residual)
+//   then:      lm_head GEMV (final RMSNorm) -> top-k -> accept
+//
+// one kernel each.  Every kernel after the first is launched as a
+// programmatic dependent and lets its own successor start as soon as it
+// begins (griddepcontrol.launch_dependents): a kernel's CTAs start while its
+// predecessor still runs, issue the bulk copies of their weight tiles and
+// copy what the pass plan, the call arguments, the RoPE table and the norm
+// gains hold, and only then wait (griddepcontrol.wait) for the
+// predecessor's results.  Nothing read before the wait is written inside
+// the pass: the plan and the call arguments are written before the pass's
+// first kernel starts, and that kernel is a full dependent of earlier work.
+//
+// Numerics: bf16 (or fp32) weights, fp32 activations, KV cache and
+// accumulation.  Every reduction has a fixed order that depends only on the
+// model shape (per thread in element order, a butterfly over the warp, warps
+// in index order), never on which rows share the pass, so greedy speculative
+// decoding reproduces greedy autoregressive decoding exactly.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "cp_common.cuh"
+#include "cp_frame.cuh"
+#include "cp_sampling.cuh"
+
+namespace cpk {
+
+// ------------------------------------------------------------ weight types
+// One 16-byte chunk of a weight row in shared memory: loaded raw, then
+// converted to float2 pairs.
+template <typename WT> struct WTraits;
+template <> struct WTraits<float> {
+  static constexpr int EB = 4;   // bytes per element
+  static constexpr int EPC = 4;  // elements per 16-byte chunk
+  typedef float4 Raw;
+  __device__ __forceinline__ static Raw ld_raw(const unsigned char* p) { return *reinterpret_cast<const float4*>(p); }
+  __device__ __forceinline__ static void cvt(const Raw& v, float2 (&w)[2]) {
+    w[0] = make_float2(v.x, v.y);
+    w[1] = make_float2(v.z, v.w);
+  }
+  __device__ __forceinline__ static float load1(const void* base, size_t i) {
+    return __ldg(static_cast<const float*>(base) + i);
+  }
+};
+template <> struct WTraits<__nv_bfloat16> {
+  static constexpr int EB = 2;
+  static constexpr int EPC = 8;
+  typedef uint4 Raw;
+  __device__ __forceinline__ static Raw ld_raw(const unsigned char* p) { return *reinterpret_cast<const uint4*>(p); }
+  __device__ __forceinline__ static void cvt(const Raw& v, float2 (&w)[4]) {
+    w[0] = bf16x2_to_f2(v.x);
+    w[1] = bf16x2_to_f2(v.y);
+    w[2] = bf16x2_to_f2(v.z);
+    w[3] = bf16x2_to_f2(v.w);
+  }
+  __device__ __forceinline__ static float load1(const void* base, size_t i) {
+    const unsigned short u = __ldg(static_cast<const unsigned short*>(base) + i);
+    return __uint_as_float((uint32_t)u << 16);
+  }
+};
+
+// -------------------------------------------------- programmatic launches
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// ------------------------------------------------------------ GEMV shapes
+// Output units of a GEMV kind: QKV = RoPE pair (e, e + d/2) of a head;
+// O, down = output row; gate/up = feature (gate row + up row);
+// lm_heads = (head of the pass, vocabulary row).
+__host__ __device__ __forceinline__ int rows_per_unit(int kind) { return (kind == kQKV || kind == kGU) ? 2 : 1; }
+
+__device__ __forceinline__ int gemv_K(const FrameParams& P, int kind) {
+  return kind == kO ? P.nq * P.d : (kind == kDown ? P.F : P.H);
+}
+
+__device__ __forceinline__ int gemv_units(const FrameParams& P, int kind, int nheads) {
+  switch (kind) {
+    case kQKV: return (P.nq + 2 * P.nkv) * (P.d / 2);
+    case kO: case kDown: return P.H;
+    case kGU: return P.F;
+    default: return nheads * P.V;
+  }
+}
+
+struct Tile {
+  int u0, n;  // first output unit and unit count
+};
+constexpr int kMaxTiles = 96;
+constexpr int kRedFloats = 1280;       // GEMV partial sums of two tiles: rows x 4 input rows x warps per row group, per tile
+constexpr int kRopeSmemBytes = 8192;   // RoPE table copied to shared memory up to this size
+constexpr uint64_t kTileTimeoutNs = 2ull * 1000ull * 1000ull * 1000ull;  // a bulk copy that has not landed in 2 s failed
+
+// The two (or one) contiguous byte runs of a tile in global memory: QKV
+// rows e and e + d/2 of one head; gate and up rows; else one run.
+struct TileRuns {
+  const unsigned char* src0;
+  const unsigned char* src1;
+  uint32_t bytes;  // per run
+};
+
+template <typename WT>
+__device__ __forceinline__ TileRuns tile_runs(const FrameParams& P, int kind, int l, const int* heads, Tile t) {
+  constexpr int EB = WTraits<WT>::EB;
+  TileRuns r;
+  r.src1 = nullptr;
+  switch (kind) {
+    case kQKV: {
+      const int half = P.d / 2, hh = t.u0 / half, e = t.u0 - hh * half;
+      const size_t rb = (size_t)P.H * EB;
+      const unsigned char* base;
+      if (hh < P.nq) base = static_cast<const unsigned char*>(P.wq[l]) + (size_t)hh * P.d * rb;
+      else if (hh < P.nq + P.nkv) base = static_cast<const unsigned char*>(P.wk[l]) + (size_t)(hh - P.nq) * P.d * rb;
+      else base = static_cast<const unsigned char*>(P.wv[l]) + (size_t)(hh - P.nq - P.nkv) * P.d * rb;
+      r.src0 = base + (size_t)e * rb;
+      r.src1 = base + (size_t)(e + half) * rb;
+      r.bytes = (uint32_t)(t.n * rb);
+      break;
+    }
+    case kO: {
+      const size_t rb = (size_t)P.nq * P.d * EB;
+      r.src0 = static_cast<const unsigned char*>(P.wo[l]) + (size_t)t.u0 * rb;
+      r.bytes = (uint32_t)(t.n * rb);
+      break;
+    }
+    case kGU: {
+      const size_t rb = (size_t)P.H * EB;
+      r.src0 = static_cast<const unsigned char*>(P.w_gate[l]) + (size_t)t.u0 * rb;
+      r.src1 = static_cast<const unsigned char*>(P.w_up[l]) + (size_t)t.u0 * rb;
+      r.bytes = (uint32_t)(t.n * rb);
+      break;
+    }
+    case kDown: {
+      const size_t rb = (size_t)P.F * EB;
+      r.src0 = static_cast<const unsigned char*>(P.w_down[l]) + (size_t)t.u0 * rb;
+      r.bytes = (uint32_t)(t.n * rb);
+      break;
+    }
+    default: {
+      const size_t rb = (size_t)P.H * EB;
+      const int hi = t.u0 / P.V, v = t.u0 - hi * P.V;
+      r.src0 = static_cast<const unsigned char*>(P.head) + ((size_t)(heads[hi] - 1) * P.V + v) * rb;
+      r.bytes = (uint32_t)(t.n * rb);
+    }
+  }
+  return r;
+}
+
+// Tiles of this CTA's share [U*c/grid, U*(c+1)/grid) of `kind`: at most
+// `upt` units each, none crossing a head boundary (QKV, lm_heads).
+__device__ int make_tiles(int U, int upt, int period, Tile* out) {
+  const int c = blockIdx.x, g = gridDim.x;
+  const int u0 = (int)(((long long)U * c) / g), u1 = (int)(((long long)U * (c + 1)) / g);
+  int n = 0;
+  for (int u = u0; u < u1;) {
+    int e = min(u1, u + upt);
+    if (period > 0) e = min(e, (u / period + 1) * period);
+    if (n >= kMaxTiles) return -1;
+    out[n++] = Tile{u, e - u};
+    u = e;
+  }
+  return n;
+}
+
+// ------------------------------------------------------------ GEMV kernels
+// Butterfly reduce-scatter of NV values over the warp (offsets 16, 8, 4, 2, 1):
+// lane l ends with value l >> (5 - log2 NV) summed over all 32 lanes.  The
+// pairing of lanes is the same for every value and every NV, so a value's
+// rounding does not depend on its index or on how many values travel.
+template <int N, int S>
+__device__ __forceinline__ void rs_step(float* v, int lane) {
+  if constexpr (N >= 2) {
+    constexpr int h = N / 2;
+    const bool up = (lane & S) != 0;
+#pragma unroll
+    for (int i = 0; i < h; ++i) {
+      const float send = up ? v[i] : v[i + h];
+      const float keep = up ? v[i + h] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, S);
+    }
+  } else {
+    v[0] += __shfl_xor_sync(0xffffffffu, v[0], S);
+  }
+}
+
+template <int NV>
+__device__ __forceinline__ float reduce_scatter(float (&v)[NV]) {
+  const int lane = threadIdx.x & 31;
+  rs_step<NV, 16>(v, lane);
+  rs_step<(NV >= 2 ? NV / 2 : 1), 8>(v, lane);
+  rs_step<(NV >= 4 ? NV / 4 : 1), 4>(v, lane);
+  rs_step<(NV >= 8 ? NV / 8 : 1), 2>(v, lane);
+  rs_step<(NV >= 16 ? NV / 16 : 1), 1>(v, lane);
+  return v[0];
+}
+
+// Where a GEMV input row comes from: an fp32 row, or (first layer, positions
+// >= 1) a row of the code embedding in the weight type.
+struct ActRow {
+  const float* f;
+  const void* w;
+};
+
+// How the CTA's threads cover a weight row of nch 16-byte chunks: row groups
+// of TPG threads (a multiple of 32), thread tl of a group owning chunks
+// tl, tl + TPG, ... (CPT of them); group g takes tile rows g, g + RG, ...
+struct RowGeom {
+  int nch, TPG, RG, CPT;
+};
+
+__device__ __forceinline__ RowGeom row_geom(int nch) {
+  RowGeom g;
+  g.nch = nch;
+  g.TPG = min(kThreads, (nch + 31) / 32 * 32);
+  g.RG = kThreads / g.TPG;
+  g.CPT = (nch + g.TPG - 1) / g.TPG;
+  return g;
+}
+
+// Raw input element values k0 .. k0 + EPC - 1 of row `src` (as float2 pairs).
+template <typename WT>
+__device__ __forceinline__ void load_act(const ActRow& src, int k0, float2 (&out)[WTraits<WT>::EPC / 2]) {
+  constexpr int EPC = WTraits<WT>::EPC, PPC = EPC / 2;
+  if (src.f != nullptr) {
+#pragma unroll
+    for (int i = 0; i < EPC; i += 4) {
+      const float4 x = __ldcg(reinterpret_cast<const float4*>(src.f + k0 + i));
+      out[i / 2] = make_float2(x.x, x.y);
+      out[i / 2 + 1] = make_float2(x.z, x.w);
+    }
+  } else {
+    WTraits<WT>::cvt(__ldg(reinterpret_cast<const typename WTraits<WT>::Raw*>(
+                         static_cast<const unsigned char*>(src.w) + (size_t)k0 * WTraits<WT>::EB)),
+                     out);
+  }
+  (void)PPC;
+}
+
+// The pass rows as a GEMV CTA sees them: the plan's arrays, copied to
+// shared memory before the dependency wait (the plan is written before the
+// pass's first kernel starts).
+struct PassRows {
+  const int* prow;
+  const int* ppos;
+  const int* pcode;
+};
+
+// Input row i of the pass (compacted index) for a GEMV kind.
+template <typename WT>
+__device__ __forceinline__ ActRow act_row(const FrameParams& P, const CallArgs& ca, const PassRows& pr, int kind, int l,
+                                          int i) {
+  const int r = pr.prow[i];
+  ActRow a{nullptr, nullptr};
+  switch (kind) {
+    case kQKV:
+      if (l == 0) {
+        const int pos = pr.ppos[i], code = pr.pcode[i], b = r / P.NS;
+        if (pos == 0)
+          a.f = ca.mode == kModeTeacher ? ca.x + (size_t)b * P.H : ca.x + ((size_t)code * ca.B + b) * P.H;
+        else
+          a.w = static_cast<const WT*>(P.embed) + ((size_t)(pos - 1) * P.V + code) * P.H;
+      } else {
+        a.f = P.h + (size_t)r * P.H;
+      }
+      break;
+    case kO: a.f = P.abuf + (size_t)r * P.nq * P.d; break;
+    case kGU: a.f = P.h + (size_t)r * P.H; break;
+    case kDown: a.f = P.fbuf + (size_t)r * P.F; break;
+    default: a.f = P.h + (size_t)r * P.H;
+  }
+  return a;
+}
+
+// Outputs of one unit for pass row gi: RoPE + q / KV append (QKV), residual
+// update (O, down), SwiGLU (gate/up), logits (lm_heads).
+template <int KIND>
+__device__ __forceinline__ void gemv_out(const FrameParams& P, int l, const int* heads, const PassRows& pr,
+                                         const float2* rope, int u, int gi, float y0, float y1, float hold) {
+  const int r = pr.prow[gi], pos = pr.ppos[gi];
+  if (KIND == kQKV) {
+    const int half = P.d / 2, hh = u / half, e = u - hh * half;
+    const int b = r / P.NS;
+    if (hh < P.nq + P.nkv) {
+      const float2 cs2 = rope[(size_t)pos * half + e];
+      const float r0 = y0 * cs2.x - y1 * cs2.y;
+      const float r1 = y1 * cs2.x + y0 * cs2.y;
+      if (hh < P.nq) {
+        float* qd = P.qbuf + (size_t)r * P.nq * P.d + (size_t)hh * P.d;
+        qd[e] = r0;
+        qd[e + half] = r1;
+      } else {
+        float* kd = P.kv + (((((size_t)b * P.L + l) * 2 + 0) * P.G + pos) * P.nkv + (hh - P.nq)) * P.d;
+        kd[e] = r0;
+        kd[e + half] = r1;
+      }
+    } else {
+      float* vd = P.kv + (((((size_t)b * P.L + l) * 2 + 1) * P.G + pos) * P.nkv + (hh - P.nq - P.nkv)) * P.d;
+      vd[e] = y0;
+      vd[e + half] = y1;
+    }
+  } else if (KIND == kO || KIND == kDown) {
+    P.h[(size_t)r * P.H + u] = hold + y0;
+  } else if (KIND == kGU) {
+    P.fbuf[(size_t)r * P.F + u] = y0 / (1.0f + expf(-y0)) * y1;
+  } else {
+    const int hi = u / P.V, v = u - hi * P.V;
+    const int slot = heads[hi] - pos;
+    if (pos >= 1 && slot >= 0 && slot <= P.ND) P.logits[((size_t)r * (1 + P.ND) + slot) * P.V + v] = y0;
+  }
+}
+
+// Shared state of a GEMV CTA.
+struct GemvShared {
+  uint64_t full[2];           // tile landed in slot 0 / 1
+  Tile tiles[kMaxTiles];
+  int ntiles;
+  int heads[kMaxHeadsPerPass];
+  int issued;                 // tiles whose copies were issued
+  ActRow src[4];
+  float ss[kWarps][4];        // RMSNorm partial sums of squares per warp
+};
+
+// Issue the bulk copies of tile t into slot t & 1 (thread 0).
+template <typename WT, int KIND>
+__device__ __forceinline__ void gemv_issue(const FrameParams& P, int l, GemvShared& sh, unsigned char* slots, int t) {
+  const int slot = t & 1;
+  const TileRuns r = tile_runs<WT>(P, KIND, l, sh.heads, sh.tiles[t]);
+  unsigned char* dst = slots + (size_t)slot * kSlotBytes;
+  const uint64_t pol = l2_evict_first_policy();
+  mbar_arrive_expect_tx(&sh.full[slot], r.src1 ? 2 * r.bytes : r.bytes);
+  bulk_copy_g2s(dst, r.src0, r.bytes, &sh.full[slot], pol);
+  if (r.src1) bulk_copy_g2s(dst + r.bytes, r.src1, r.bytes, &sh.full[slot], pol);
+  sh.issued = t + 1;
+}
+
+
+// One input group (rows q0 .. q0 + NQ - 1, rows past nqv repeat row nqv - 1
+// and are discarded) against tiles [ta, tb).  A thread loads its chunks of
+// the group's inputs once; for the normed kinds the sum of squares of each
+// row is taken over row group 0 (per thread over its chunks in order, the
+// warp butterfly, the warps in order) and the values are scaled by
+// inv * gain.  Per tile: all threads wait for the slot, form their partial
+// sums (per (row, input row) a lane accumulates its chunks in order, even and
+// odd elements in the two halves of an f32x2 accumulator; the warp's
+// reduce-scatter adds the lanes), then the epilogue adds the warps of a row
+// group in order and writes the outputs.  With `issue_next`, thread 0 refills
+// a slot with tile t + 2 once every thread is past tile t.
+template <typename WT, int KIND, int CPT, int NQ>
+__device__ __forceinline__ bool gemv_run(const FrameParams& P, const CallArgs& ca, int l, const RowGeom& G,
+                                         GemvShared& sh, const PassRows& pr, const float2* rope, unsigned char* slots,
+                                         float* red, int q0, int nqv, int ta, int tb, bool issue_next,
+                                         const float* gain) {
+  using Raw = typename WTraits<WT>::Raw;
+  constexpr int EPC = WTraits<WT>::EPC, PPC = EPC / 2;
+  constexpr int EB = WTraits<WT>::EB;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int g = tid / G.TPG;
+  const bool active = g < G.RG;  // whole warps: TPG is a multiple of 32
+  const int tl = tid - g * G.TPG, wg = tl >> 5, WPG = G.TPG >> 5;
+  const int K = G.nch * 16 / EB;
+  const int rpu = rows_per_unit(KIND);
+  const size_t row_bytes = (size_t)G.nch * 16;
+  if (tid < 32 * nqv && lane == 0) sh.src[warp] = act_row<WT>(P, ca, pr, KIND, l, q0 + warp);
+  __syncthreads();
+  // gains of this thread's chunks, fetched with the inputs
+  float4 gv[CPT][EPC / 4];
+  if (gain != nullptr) {
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      const int c = tl + j * G.TPG;
+#pragma unroll
+      for (int i = 0; i < EPC; i += 4)
+        gv[j][i / 4] = (active && c < G.nch) ? *reinterpret_cast<const float4*>(gain + c * EPC + i)
+                                             : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  float2 av[CPT][NQ][PPC];
+#pragma unroll
+  for (int j = 0; j < CPT; ++j) {
+    const int c = tl + j * G.TPG;
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      if (active && c < G.nch) {
+        load_act<WT>(sh.src[min(q, nqv - 1)], c * EPC, av[j][q]);
+      } else {
+#pragma unroll
+        for (int p = 0; p < PPC; ++p) av[j][q][p] = make_float2(0.f, 0.f);
+      }
+    }
+  }
+  if (gain != nullptr) {
+    float ss[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      ss[q] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < CPT; ++j)
+#pragma unroll
+        for (int p = 0; p < PPC; ++p) {
+          ss[q] = fmaf(av[j][q][p].x, av[j][q][p].x, ss[q]);
+          ss[q] = fmaf(av[j][q][p].y, av[j][q][p].y, ss[q]);
+        }
+      ss[q] = warp_sum(ss[q]);
+    }
+    if (g == 0 && lane == 0)
+#pragma unroll
+      for (int q = 0; q < NQ; ++q) sh.ss[wg][q] = ss[q];
+    __syncthreads();
+    float inv[NQ];
+#pragma unroll
+    for (int q = 0; q < NQ; ++q) {
+      float t = 0.0f;
+      for (int w = 0; w < WPG; ++w) t += sh.ss[w][q];
+      inv[q] = 1.0f / sqrtf(t / (float)K + P.eps);
+    }
+#pragma unroll
+    for (int j = 0; j < CPT; ++j) {
+      const int c = tl + j * G.TPG;
+      if (!active || c >= G.nch) continue;
+#pragma unroll
+      for (int i = 0; i < EPC; i += 4) {
+        const float4 gg = gv[j][i / 4];
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          float2& a0 = av[j][q][i / 2];
+          float2& a1 = av[j][q][i / 2 + 1];
+          a0.x = a0.x * inv[q] * gg.x;
+          a0.y = a0.y * inv[q] * gg.y;
+          a1.x = a1.x * inv[q] * gg.z;
+          a1.y = a1.y * inv[q] * gg.w;
+        }
+      }
+    }
+  }
+  bool ok = true;
+  // tiles in pairs (one per slot): both computed, then one epilogue
+  for (int t0 = ta; t0 < tb; t0 += 2) {
+    const int nt = min(2, tb - t0);
+    Tile tiles[2];
+    tiles[0] = sh.tiles[t0];
+    tiles[1] = nt > 1 ? sh.tiles[t0 + 1] : Tile{0, 0};
+    const int n_items0 = tiles[0].n * nqv, n_items = n_items0 + tiles[1].n * nqv;
+    // residual values the epilogue adds to (O, down), fetched before the tile is computed
+    constexpr int kHold = 2;
+    float hold[kHold] = {0.0f, 0.0f};
+    if (KIND == kO || KIND == kDown) {
+#pragma unroll
+      for (int m = 0; m < kHold; ++m) {
+        const int it = tid + m * kThreads;
+        if (it < n_items) {
+          const int k = it < n_items0 ? 0 : 1, jt = it - k * n_items0;
+          const int i = jt / nqv, q = jt - i * nqv;
+          hold[m] = __ldcg(P.h + (size_t)pr.prow[q0 + q] * P.H + tiles[k].u0 + i);
+        }
+      }
+    }
+    for (int k = 0; k < nt; ++k) {
+      const int t = t0 + k, slot = t & 1;
+      const int R = tiles[k].n * rpu;
+      float* rk = red + k * (kRedFloats / 2);
+      if (!mbar_wait_bounded(&sh.full[slot], (uint32_t)(t >> 1) & 1u, &P.ctl->status, kTileTimeoutNs)) ok = false;
+      if (!active || !ok) continue;
+      const unsigned char* tp = slots + (size_t)slot * kSlotBytes;
+      const int nrow = (R - g + G.RG - 1) / G.RG;  // rows g, g + RG, ... of the tile
+      for (int i0 = 0; i0 < nrow; i0 += kRB) {
+        int rw[kRB];
+#pragma unroll
+        for (int w = 0; w < kRB; ++w) rw[w] = g + G.RG * min(i0 + w, nrow - 1);
+        float2 acc[kRB][NQ];
+#pragma unroll
+        for (int w = 0; w < kRB; ++w)
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) acc[w][q] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < CPT; ++j) {
+          const int c = tl + j * G.TPG;
+          if (c >= G.nch) continue;
+          Raw raw[kRB];
+#pragma unroll
+          for (int w = 0; w < kRB; ++w) raw[w] = WTraits<WT>::ld_raw(tp + (size_t)rw[w] * row_bytes + (size_t)c * 16);
+#pragma unroll
+          for (int w = 0; w < kRB; ++w) {
+            float2 wv[PPC];
+            WTraits<WT>::cvt(raw[w], wv);
+#pragma unroll
+            for (int q = 0; q < NQ; ++q)
+#pragma unroll
+              for (int p = 0; p < PPC; ++p) acc[w][q] = ffma2(wv[p], av[j][q][p], acc[w][q]);
+          }
+        }
+        float v[kRB * NQ];
+#pragma unroll
+        for (int w = 0; w < kRB; ++w)
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) v[w * NQ + q] = acc[w][q].x + acc[w][q].y;
+        const float sum = reduce_scatter<kRB * NQ>(v);
+        constexpr int NV = kRB * NQ;
+        constexpr int shift = NV >= 32 ? 0 : (NV >= 16 ? 1 : (NV >= 8 ? 2 : (NV >= 4 ? 3 : 4)));
+        if ((lane & ((1 << shift) - 1)) == 0) {
+          const int vi = lane >> shift, w = vi / NQ, q = vi % NQ;
+          if (i0 + w < nrow) rk[((size_t)rw[w] * 4 + q) * WPG + wg] = sum;
+        }
+      }
+    }
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    if (!ok) return false;
+    for (int it = tid, m = 0; it < n_items; it += kThreads, ++m) {
+      const int k = it < n_items0 ? 0 : 1, jt = it - k * n_items0;
+      const int i = jt / nqv, q = jt - i * nqv;
+      const Tile tile = tiles[k];
+      const float* rk = red + k * (kRedFloats / 2);
+      float ys[2] = {0.0f, 0.0f};
+      for (int h = 0; h < rpu; ++h) {
+        const float* rr = rk + ((size_t)(i + h * tile.n) * 4 + q) * WPG;
+        float s = 0.0f;
+        for (int w = 0; w < WPG; ++w) s += rr[w];
+        ys[h] = s;
+      }
+      float ho = 0.0f;
+      if (KIND == kO || KIND == kDown) {
+#pragma unroll
+        for (int mm = 0; mm < kHold; ++mm) if (mm == m) ho = hold[mm];
+        if (m >= kHold) ho = __ldcg(P.h + (size_t)pr.prow[q0 + q] * P.H + tile.u0 + i);
+      }
+      gemv_out<KIND>(P, l, sh.heads, pr, rope, tile.u0 + i, q0 + q, ys[0], ys[1], ho);
+    }
+    __syncthreads();  // red reuse; the slots are free
+    if (issue_next && tid == 0)
+      for (int k = 0; k < nt; ++k)
+        if (t0 + k + 2 < sh.ntiles) gemv_issue<WT, KIND>(P, l, sh, slots, t0 + k + 2);
+  }
+  return true;
+}
+
+// Input rows per group for a geometry (2 when a thread owns 3 chunks, to
+// bound registers).
+__device__ __forceinline__ int group_rows(const RowGeom& G) { return G.CPT >= 3 ? 2 : 4; }
+
+template <typename WT, int KIND>
+__device__ __forceinline__ bool gemv_dispatch(const FrameParams& P, const CallArgs& ca, int l, const RowGeom& G,
+                                              GemvShared& sh, const PassRows& pr, const float2* rope,
+                                              unsigned char* slots, float* red, int q0, int nqv, int ta, int tb,
+                                              bool issue_next, const float* gain) {
+#define CP_RUN(C_, Q_) \
+  gemv_run<WT, KIND, C_, Q_>(P, ca, l, G, sh, pr, rope, slots, red, q0, nqv, ta, tb, issue_next, gain)
+  if (G.CPT == 1) {
+    if (nqv >= 3) return CP_RUN(1, 4);
+    if (nqv == 2) return CP_RUN(1, 2);
+    return CP_RUN(1, 1);
+  }
+  if (G.CPT == 2) {
+    if (nqv >= 3) return CP_RUN(2, 4);
+    if (nqv == 2) return CP_RUN(2, 2);
+    return CP_RUN(2, 1);
+  }
+  if (nqv >= 2) return CP_RUN(3, 2);
+  return CP_RUN(3, 1);
+#undef CP_RUN
+}
+
+// One GEMV kind of one layer for every row of the pass.  The CTA's share of
+// output units is cut into tiles of at most kSlotBytes; tiles stream through
+// two shared-memory slots by TMA bulk copies, the first two issued before the
+// dependency wait.  With one input group (up to 4 rows) or at most two
+// tiles, each group's inputs are loaded once and every tile streams through
+// them; otherwise tile by tile, group by group.
+template <typename WT, int KIND>
+__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ FrameParams P, int l) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  pdl_launch_dependents();
+  __shared__ GemvShared sh;
+  __shared__ CallArgs s_ca;
+  __shared__ int s_nrows;
+  constexpr int EB = WTraits<WT>::EB;
+  const int K = gemv_K(P, KIND);
+  const RowGeom G = row_geom(K * EB / 16);
+  const int rpu = rows_per_unit(KIND);
+  const size_t row_bytes = (size_t)G.nch * 16;
+  const int upt = max(1, min((int)(kSlotBytes / (rpu * row_bytes)), kMaxTileRows / rpu));
+  const int rows_cap = P.Bmax * P.NS;
+  unsigned char* slots = smem;
+  float* red = reinterpret_cast<float*>(smem + 2 * (size_t)kSlotBytes);
+  int* s_rows = reinterpret_cast<int*>(red + kRedFloats);
+  PassRows pr{s_rows, s_rows + rows_cap, s_rows + 2 * rows_cap};
+  const size_t rope_n = (size_t)P.G * (P.d / 2);
+  const bool rope_in_smem = KIND == kQKV && rope_n * sizeof(float2) <= (size_t)kRopeSmemBytes;
+  float2* s_rope = reinterpret_cast<float2*>(s_rows + (3 * rows_cap + 3) / 4 * 4);  // 16-byte aligned
+  // RMSNorm gain (a weight) in shared memory after the RoPE table
+  float* s_gain = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(s_rope) + kRopeSmemBytes);
+  const float* gain_g = KIND == kQKV ? P.attn_norm[l] : (KIND == kGU ? P.ffn_norm[l] : (KIND == kHeads ? P.final_norm : nullptr));
+  // Before the dependency wait: everything that does not come from the
+  // previous kernels of the pass (weight tiles, call arguments, the pass
+  // plan, the RoPE table, the norm gain).
+  if (threadIdx.x == 0) {
+    int nheads = 0;
+    if (KIND == kHeads) {
+      nheads = min(__ldcg(&P.plan->nheads), kMaxHeadsPerPass);
+      for (int i = 0; i < nheads; ++i) sh.heads[i] = __ldcg(&P.plan->heads[i]);
+    }
+    const int period = KIND == kQKV ? P.d / 2 : (KIND == kHeads ? P.V : 0);
+    int n = make_tiles(gemv_units(P, KIND, nheads), upt, period, sh.tiles);
+    if (n < 0) { raise_status(&P.ctl->status, kStatusDevice); n = 0; }
+    sh.ntiles = n;
+    sh.issued = 0;
+    mbar_init(&sh.full[0], 1);
+    mbar_init(&sh.full[1], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    for (int t = 0; t < min(n, 2); ++t) gemv_issue<WT, KIND>(P, l, sh, slots, t);
+    s_ca = *P.call;
+    s_nrows = min(__ldcg(&P.plan->nrows), rows_cap);
+  }
+  __syncthreads();
+  const int nrows = s_nrows;
+  for (int i = threadIdx.x; i < nrows; i += kThreads) {
+    s_rows[i] = __ldcg(P.prow + i);
+    s_rows[rows_cap + i] = __ldcg(P.ppos + i);
+    s_rows[2 * rows_cap + i] = __ldcg(P.pcode + i);
+  }
+  if (rope_in_smem)
+    for (size_t i = threadIdx.x; i < rope_n; i += kThreads) s_rope[i] = __ldg(P.rope + i);
+  if (gain_g != nullptr)
+    for (int i = threadIdx.x; i < K / 4; i += kThreads)
+      reinterpret_cast<float4*>(s_gain)[i] = __ldg(reinterpret_cast<const float4*>(gain_g) + i);
+  __syncthreads();
+  pdl_wait();
+  const CallArgs& ca = s_ca;
+  const float2* rope = rope_in_smem ? s_rope : P.rope;
+  const int ntiles = sh.ntiles;
+  const float* gain = gain_g != nullptr ? s_gain : nullptr;
+  if (KIND == kQKV && l == 0) {
+    // the residual stream starts as the input rows: this CTA's slice of H
+    const int c0 = (int)(((long long)P.H * blockIdx.x) / gridDim.x), c1 = (int)(((long long)P.H * (blockIdx.x + 1)) / gridDim.x);
+    const int w = c1 - c0;
+    for (int it = threadIdx.x; it < nrows * w; it += kThreads) {
+      const int i = it / w, k = c0 + (it - i * w);
+      const ActRow a = act_row<WT>(P, ca, pr, KIND, l, i);
+      P.h[(size_t)pr.prow[i] * P.H + k] = a.f ? __ldcg(a.f + k) : WTraits<WT>::load1(a.w, (size_t)k);
+    }
+  }
+  const int NQG = group_rows(G);
+  const int ngroups = (nrows + NQG - 1) / NQG;
+  bool ok = true;
+  if (ngroups <= 1 || ntiles <= 2) {
+    for (int gq = 0; gq < ngroups && ok; ++gq)
+      ok = gemv_dispatch<WT, KIND>(P, ca, l, G, sh, pr, rope, slots, red, gq * NQG, min(NQG, nrows - gq * NQG), 0,
+                                   ntiles, gq == ngroups - 1, gain);
+  } else {
+    for (int t = 0; t < ntiles && ok; ++t)
+      for (int gq = 0; gq < ngroups && ok; ++gq)
+        ok = gemv_dispatch<WT, KIND>(P, ca, l, G, sh, pr, rope, slots, red, gq * NQG, min(NQG, nrows - gq * NQG), t,
+                                     t + 1, gq == ngroups - 1, gain);
+  }
+  if ((!ok || ngroups == 0) && threadIdx.x == 0) {
+    // no copy may land after the CTA exits: wait (bounded) for the ones in flight
+    for (int t = max(0, sh.issued - 2); t < sh.issued; ++t)
+      mbar_wait_bounded(&sh.full[t & 1], (uint32_t)(t >> 1) & 1u, &P.ctl->status, kTileTimeoutNs);
+  }
+}
+
+// ------------------------------------------------------------- attention
+// Causal GQA attention of one (pass row, query head) per CTA over positions
+// 0..pos of the stream's KV cache (this pass's rows were appended by the QKV
+// kernel): warp w scores positions w, w + kWarps, ... (the dot product split
+// over lanes, reduced by a butterfly) and parks their value rows in shared
+// memory; then each output pair forms the softmax over all positions in
+// index order and sums the values in index order.
+__global__ void __launch_bounds__(kThreads, 2) attention_kernel(const __grid_constant__ FrameParams P, int l) {
+  extern __shared__ __align__(16) float asmem[];
+  pdl_launch_dependents();
+  pdl_wait();
+  const int nrows = __ldcg(&P.plan->nrows);
+  const int i = blockIdx.x / P.nq, hq = blockIdx.x - i * P.nq;
+  if (i >= nrows) return;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int d = P.d, grp = P.nq / P.nkv, lines = d / 2;
+  float* sc = asmem;       // [64] scores
+  float* vs = asmem + 64;  // [G][d] value rows
+  const float scale = 1.0f / sqrtf((float)d);
+  const int r = __ldcg(P.prow + i), pos = __ldcg(P.ppos + i), b = r / P.NS, g = hq / grp;
+  const size_t pstride = (size_t)P.nkv * d;
+  const float* qsrc = P.qbuf + (size_t)r * P.nq * d + (size_t)hq * d;
+  const float* kb = P.kv + ((((size_t)b * P.L + l) * 2 + 0) * P.G) * pstride + (size_t)g * d;
+  const float* vb = P.kv + ((((size_t)b * P.L + l) * 2 + 1) * P.G) * pstride + (size_t)g * d;
+  float2 qv[4];
+#pragma unroll
+  for (int u = 0; u < 4; ++u) {
+    const int ln = lane + 32 * u;
+    qv[u] = ln < lines ? __ldcg(reinterpret_cast<const float2*>(qsrc) + ln) : make_float2(0.f, 0.f);
+  }
+  for (int j = warp; j <= pos; j += kWarps) {
+    float part = 0.0f;
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int ln = lane + 32 * u;
+      if (ln >= lines) continue;
+      const float2 kk = __ldcg(reinterpret_cast<const float2*>(kb + (size_t)j * pstride) + ln);
+      const float2 vv = __ldcg(reinterpret_cast<const float2*>(vb + (size_t)j * pstride) + ln);
+      part = fmaf(qv[u].x, kk.x, part);
+      part = fmaf(qv[u].y, kk.y, part);
+      *reinterpret_cast<float2*>(vs + (size_t)j * d + 2 * ln) = vv;
+    }
+    const float sdot = warp_sum(part) * scale;
+    if (lane == 0) sc[j] = sdot;
+  }
+  __syncthreads();
+  if (tid < lines) {
+    float mx = -INFINITY;
+    for (int j = 0; j <= pos; ++j) mx = fmaxf(mx, sc[j]);
+    float den = 0.0f;
+    for (int j = 0; j <= pos; ++j) den += expf(sc[j] - mx);
+    float2 o = make_float2(0.f, 0.f);
+    for (int j = 0; j <= pos; ++j) {
+      const float w = expf(sc[j] - mx) / den;
+      const float2 v = *reinterpret_cast<const float2*>(vs + (size_t)j * d + 2 * tid);
+      o.x = fmaf(w, v.x, o.x);
+      o.y = fmaf(w, v.y, o.y);
+    }
+    *reinterpret_cast<float2*>(P.abuf + (size_t)r * P.nq * d + (size_t)hq * d + 2 * tid) = o;
+  }
+}
+
+// ------------------------------------------------------------------ top-k
+// One vocabulary row (in shared memory as floats in `keys` on entry)
+// processed by the CTA, with the semantics of the oracle's processing:
+// z = fl32(logit/T), exactly min(k, V) entries kept by (z desc, index asc),
+// e = cp_expf(z - zmax), S = float32 sum of e in ascending index order,
+// p = fl32(e / S); T = 0 is argmax (lowest index).  Thread t owns indices
+// [t*E, t*E + E).  The k-th key is found by an MSB-first 8-bit radix select
+// over warp-private histograms (increments aggregated per bin across the
+// warp, no atomics); one scan of packed (greater, equal) counts places every
+// kept entry in index order.  Scratch: hw [kWarps][256], ebuf [min(k, V)],
+// sx [64].  Returns the length.
+__device__ __noinline__ int block_topk(int V, int k, float T, uint32_t* keys, uint32_t* hw, float* ebuf, int* sx,
+                                       int* out_idx, float* out_prob) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const float* row = reinterpret_cast<const float*>(keys);
+  const int E = (V + kThreads - 1) / kThreads;
+  const int i0 = tid * E, i1 = min(V, i0 + E);
+  if (T == 0.0f) {
+    float best = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int i = i0; i < i1; ++i)
+      if (row[i] > best) { best = row[i]; bi = i; }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, best, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ov > best || (ov == best && oi < bi)) { best = ov; bi = oi; }
+    }
+    float* sbest = reinterpret_cast<float*>(sx);
+    int* sbi = sx + 16;
+    if (lane == 0) { sbest[warp] = best; sbi[warp] = bi; }
+    __syncthreads();
+    if (tid == 0) {
+      float bb = sbest[0];
+      int ix = sbi[0];
+      for (int w = 1; w < kWarps; ++w)
+        if (sbest[w] > bb || (sbest[w] == bb && sbi[w] < ix)) { bb = sbest[w]; ix = sbi[w]; }
+      out_idx[0] = ix;
+      out_prob[0] = 1.0f;
+    }
+    __syncthreads();
+    return 1;
+  }
+  // keys (in place) and the maximum key
+  uint32_t kmax = 0;
+  for (int i = i0; i < i1; ++i) {
+    float z = __fdiv_rn(row[i], T);
+    if (z == 0.0f) z = 0.0f;
+    const uint32_t key = float_key(z);
+    keys[i] = key;
+    kmax = max(kmax, key);
+  }
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  if (lane == 0) sx[warp] = (int)kmax;
+  __syncthreads();
+  kmax = 0;
+  for (int w = 0; w < kWarps; ++w) kmax = max(kmax, (uint32_t)sx[w]);
+  const int kk = k < V ? k : V;
+  uint32_t prefix = 0, mask = 0;
+  int need = kk;
+  bool eq_all = (kk == V);
+  uint32_t* my = hw + warp * 256;
+  for (int shift = 24; shift >= 0 && !eq_all; shift -= 8) {
+    // warp-private histogram, aggregated increments (no atomics: one leader per bin per step)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) my[lane * 8 + j] = 0;
+    __syncwarp();
+    for (int e = 0; e < E; ++e) {
+      const int i = i0 + e;
+      const uint32_t key = i < i1 ? keys[i] : 0u;
+      const bool hit = i < i1 && (key & mask) == prefix;
+      const uint32_t bin = (key >> shift) & 255u;
+      const unsigned grpm = __match_any_sync(0xffffffffu, hit ? bin : 0xFFFFFFFFu);
+      if (hit && lane == __ffs(grpm) - 1) my[bin] += (uint32_t)__popc(grpm);
+      __syncwarp();
+    }
+    __syncthreads();
+    if (warp == 0) {
+      // lane l holds bins 255-8l .. 248-8l (descending), summed over the warps
+      uint32_t cnt[8], chunk = 0;
+#pragma unroll
+      for (int m = 0; m < 8; ++m) {
+        const int bb = 255 - 8 * lane - m;
+        uint32_t c = 0;
+        for (int w = 0; w < kWarps; ++w) c += hw[w * 256 + bb];
+        cnt[m] = c;
+        chunk += c;
+      }
+      uint32_t incl = chunk;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      const uint32_t excl = incl - chunk;
+      if (excl < (uint32_t)need && (uint32_t)need <= incl) {
+        uint32_t acc = excl;
+        for (int m = 0; m < 8; ++m) {
+          if (acc + cnt[m] >= (uint32_t)need) { sx[32] = 255 - 8 * lane - m; sx[33] = (int)acc; sx[34] = (int)cnt[m]; break; }
+          acc += cnt[m];
+        }
+      }
+    }
+    __syncthreads();
+    const uint32_t bin = (uint32_t)sx[32], above = (uint32_t)sx[33], cbin = (uint32_t)sx[34];
+    need -= (int)above;
+    prefix |= bin << shift;
+    mask |= 0xFFu << shift;
+    if ((int)cbin == need) eq_all = true;
+  }
+  // one scan of packed counts (greater | equal << 16), index order
+  int n_gt = 0, n_eq = 0;
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t km = keys[i] & mask;
+    n_gt += km > prefix;
+    n_eq += km == prefix;
+  }
+  const int packed = n_gt | (n_eq << 16);
+  int incl = packed;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int t = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += t;
+  }
+  if (lane == 31) sx[40 + warp] = incl;
+  __syncthreads();
+  int before = incl - packed;
+  for (int w = 0; w < warp; ++w) before += sx[40 + w];
+  int gb = before & 0xFFFF, eb = before >> 16;
+  const float zmax = key_float(kmax);
+  for (int i = i0; i < i1; ++i) {
+    const uint32_t key = keys[i];
+    const uint32_t km = key & mask;
+    int pos = -1;
+    if (km > prefix) { pos = gb + min(eb, need); ++gb; }
+    else if (km == prefix) { if (eq_all || eb < need) pos = gb + eb; ++eb; }
+    if (pos >= 0) { out_idx[pos] = i; ebuf[pos] = cp_expf(__fsub_rn(key_float(key), zmax)); }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    float S = 0.0f;
+    for (int p = 0; p < kk; ++p) S = __fadd_rn(S, ebuf[p]);
+    reinterpret_cast<float*>(sx)[48] = S;
+  }
+  __syncthreads();
+  const float S = reinterpret_cast<float*>(sx)[48];
+  for (int p = tid; p < kk; p += kThreads) out_prob[p] = __fdiv_rn(ebuf[p], S);
+  __syncthreads();
+  return kk;
+}
+
+// Top-k / temperature / softmax of one (pass row, logit slot) per CTA (slot
+// t of the row at position pos holds head pos + t; slots past the last code
+// group are unused).  Decode mode only.
+__global__ void __launch_bounds__(kThreads, 2) topk_kernel(const __grid_constant__ FrameParams P) {
+  extern __shared__ __align__(16) unsigned char tsmem[];
+  pdl_launch_dependents();
+  pdl_wait();
+  if (P.call->mode != kModeDecode) return;
+  const int slots = 1 + P.ND;
+  const int nrows = __ldcg(&P.plan->nrows);
+  const int i = blockIdx.x / slots, t = blockIdx.x - i * slots;
+  if (i >= nrows) return;
+  const int pos = __ldcg(P.ppos + i);
+  if (pos < 1 || pos + t > P.G - 1) return;
+  const int r = __ldcg(P.prow + i), b = r / P.NS;
+  const size_t keys_bytes = ((size_t)P.V * 4 + 15) / 16 * 16;
+  uint32_t* keys = reinterpret_cast<uint32_t*>(tsmem);
+  uint32_t* hw = reinterpret_cast<uint32_t*>(tsmem + keys_bytes);
+  float* ebuf = reinterpret_cast<float*>(tsmem + keys_bytes + kWarps * 1024);
+  int* sx = reinterpret_cast<int*>(tsmem + keys_bytes + kWarps * 1024 + ((size_t)P.KC * 4 + 15) / 16 * 16);
+  const size_t li = (size_t)r * slots + t;
+  const float* src = P.logits + li * P.V;
+  if ((P.V & 3) == 0) {
+    for (int v = threadIdx.x; v < P.V / 4; v += kThreads)
+      reinterpret_cast<float4*>(keys)[v] = __ldcg(reinterpret_cast<const float4*>(src) + v);
+  } else {
+    for (int v = threadIdx.x; v < P.V; v += kThreads) reinterpret_cast<float*>(keys)[v] = __ldcg(src + v);
+  }
+  __syncthreads();
+  const int n = block_topk(P.V, __ldg(P.top_k + b), __ldg(P.temp + b), keys, hw, ebuf, sx, P.lidx + li * P.KC,
+                           P.lprob + li * P.KC);
+  if (threadIdx.x == 0) P.lcount[li] = n;
+}
+
+// ------------------------------------------------------ per-stream logic
+// One warp owns one stream in the setup and accept kernels.
+__device__ __forceinline__ int valid_code(const FrameParams& P, int c) {
+  if (c < 0 || c >= P.V) { raise_status(&P.ctl->status, kStatusDevice); return 0; }
+  return c;
+}
+
+// Record the rows of stream b's next pass (state already updated in S):
+// positions pos0.. and the code whose embedding each row carries (the frame
+// index for the x row at position 0).  Warp-wide.
+template <typename WT>
+__device__ __noinline__ void set_pass_rows(const FrameParams& P, int b, const StreamState& S, const int* codes_in) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  if (lane < P.NS) {
+    const int on = lane < S.m;
+    P.row_pos[b * P.NS + lane] = on ? S.pos0 + lane : -1;
+    P.row_code[b * P.NS + lane] = on ? codes_in[lane] : 0;
+  }
+  if (lane == 0) {
+    const long long kvb = (long long)(S.pos0 + S.m) * P.L * 2 * P.nkv * P.d * (long long)sizeof(float);
+    atomicAdd((unsigned long long*)&P.ctl->kv_bytes, (unsigned long long)kvb);
+    atomicAdd((unsigned long long*)&P.ctl->weight_bytes, (unsigned long long)((long long)S.m * P.H * sizeof(WT)));
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ void retire_stream(const FrameParams& P, int b, StreamState& S) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  if (lane == 0) {
+    S.phase = kPhaseDone;
+    S.m = 0;
+    for (int i = 0; i < P.NS; ++i) P.row_pos[b * P.NS + i] = -1;
+    atomicSub(&P.ctl->active, 1);
+  }
+  __syncwarp();
+}
+
+// Frame start: rows [x, E_0(c_0)] at positions 0, 1.  Scalar state fields
+// are written by lane 0 only; every all-lane read of them follows a __syncwarp().
+template <typename WT>
+__device__ __noinline__ void setup_frame(const FrameParams& P, const CallArgs& ca, int b, StreamState& S, int frame) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  if (lane == 0) {
+    const int c0 = valid_code(P, __ldg(ca.c0 + (size_t)frame * ca.B + b));
+    S.frame = frame;
+    S.frame_abs = ca.first_frame + frame;
+    S.codes[0] = c0;
+    S.s = 0;
+    S.phase = kPhasePrefill;
+    S.pos0 = 0;
+    S.m = 2;
+    S.n_d = 0;
+    ca.codes_out[((size_t)frame * ca.B + b) * P.G] = c0;
+    if (ca.committed_out) ca.committed_out[b] = 1;
+  }
+  __syncwarp();
+  const int codes_in[2] = {frame, S.codes[0]};
+  set_pass_rows<WT>(P, b, S, codes_in);
+}
+
+template <typename WT>
+__device__ __noinline__ void setup_teacher_chunk(const FrameParams& P, const CallArgs& ca, int b, StreamState& S) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  const int pos0 = S.pos0;
+  const int m = min(P.NS, ca.P - pos0);
+  __syncwarp();
+  if (lane == 0) { S.m = m; S.phase = kPhaseTeacher; }
+  __syncwarp();
+  int codes_in[CP_SPEC_MAX_WINDOW];
+  for (int i = 0; i < m; ++i) {
+    const int pos = pos0 + i;
+    codes_in[i] = pos > 0 ? valid_code(P, __ldg(ca.t_codes + (size_t)b * (ca.P - 1) + pos - 1)) : 0;
+  }
+  set_pass_rows<WT>(P, b, S, codes_in);
+}
+
+__device__ __forceinline__ void load_state(const FrameParams& P, int b, StreamState& S) {
+  const int lane = threadIdx.x & 31;
+  const int* src = reinterpret_cast<const int*>(P.st + b);
+  int* dst = reinterpret_cast<int*>(&S);
+  for (int i = lane; i < (int)(sizeof(StreamState) / 4); i += 32) dst[i] = __ldcg(src + i);
+  __syncwarp();
+}
+
+__device__ __forceinline__ void store_state(const FrameParams& P, int b, const StreamState& S) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  int* dst = reinterpret_cast<int*>(P.st + b);
+  const int* src = reinterpret_cast<const int*>(&S);
+  for (int i = lane; i < (int)(sizeof(StreamState) / 4); i += 32) dst[i] = src[i];
+  __syncwarp();
+}
+
+// Per-warp view of the accept scratch (see accept_scratch_bytes).
+struct AcceptScratch {
+  StreamState* S;
+  int* idx;    // [2*NS][KC]
+  float* prob; // [2*NS][KC]
+  int* cnt;    // [2*NS]
+};
+
+__device__ __forceinline__ AcceptScratch accept_scratch(const FrameParams& P, unsigned char* base_all) {
+  const int warp = threadIdx.x >> 5;
+  unsigned char* base = base_all + (size_t)warp * accept_scratch_bytes(P.NS, P.KC);
+  AcceptScratch a;
+  a.S = reinterpret_cast<StreamState*>(base);
+  a.idx = reinterpret_cast<int*>(base + sizeof(StreamState));
+  a.prob = reinterpret_cast<float*>(a.idx + (size_t)2 * P.NS * P.KC);
+  a.cnt = reinterpret_cast<int*>(a.prob + (size_t)2 * P.NS * P.KC);
+  return a;
+}
+
+__device__ __forceinline__ void stage_list_async(const FrameParams& P, AcceptScratch& A, int slot, const int* gidx,
+                                                 const float* gprob) {
+  warp_copy_async(A.idx + (size_t)slot * P.KC, gidx, P.KC * 4);
+  warp_copy_async(A.prob + (size_t)slot * P.KC, gprob, P.KC * 4);
+}
+
+// After codes up to depth s_new are committed: finish the frame or set up
+// the next pass (sampling the drafts from this pass's draft slots).
+template <typename WT>
+__device__ __noinline__ void after_commit(const FrameParams& P, const CallArgs& ca, int b, AcceptScratch& A,
+                                          int s_new, int hrow) {
+  StreamState& S = *A.S;
+  const int lane = threadIdx.x & 31;
+  StreamStats* ss = P.sstats + b;
+  __syncwarp();
+  const int frame = S.frame;
+  __syncwarp();
+  if (s_new >= P.G - 1) {
+    if (lane == 0) { ss->frames += 1; ss->committed += P.G - 1; }
+    const int nf = frame + 1;
+    if (nf < ca.n_frames) setup_frame<WT>(P, ca, b, S, nf);
+    else retire_stream(P, b, S);
+    return;
+  }
+  if (P.N == 0) {
+    if (lane == 0) { S.s = s_new; S.phase = kPhaseAR; S.pos0 = s_new + 1; S.m = 1; S.n_d = 0; }
+    __syncwarp();
+    const int code = S.codes[s_new];
+    set_pass_rows<WT>(P, b, S, &code);
+    return;
+  }
+  const int R = P.G - 1 - s_new;
+  const int n_d = min(P.N - 1, R);
+  const int slots = 1 + P.ND;
+  // The draft distributions q_t = proc(head_{s+t} . h_s), t = 1..n_d, are
+  // this pass's speculative draft slots on the row at position s_new: stage
+  // them, sample the drafts, and keep them for the next pass's acceptance.
+  for (int t = 1; t <= n_d; ++t) {
+    const size_t li = (size_t)hrow * slots + t;
+    stage_list_async(P, A, t - 1, P.lidx + li * P.KC, P.lprob + li * P.KC);
+  }
+  if (lane < n_d) A.cnt[lane] = __ldcg(P.lcount + (size_t)hrow * slots + 1 + lane);
+  cp_async_wait_all();
+  __syncwarp();
+  if (lane == 0) {
+    for (int t = 1; t <= n_d; ++t) {
+      const float u = philox_uniform(P.seed, (uint32_t)b, (uint32_t)S.frame_abs, (uint32_t)(s_new + t), kDraft);
+      S.drafts[t - 1] = valid_code(P, list_sample(A.idx + (size_t)(t - 1) * P.KC, A.prob + (size_t)(t - 1) * P.KC,
+                                                  A.cnt[t - 1], u));
+    }
+    S.s = s_new;
+    S.n_d = n_d;
+    S.m = min(n_d + 1, R);
+    S.pos0 = s_new + 1;
+    S.phase = kPhaseSpec;
+  }
+  // save q_1..q_{n_d} (16-byte stores) for the next pass's acceptance
+  const int kc4 = P.KC >> 2;
+  for (int i = lane; i < n_d * kc4; i += 32) {
+    const int t = i / kc4, c = i - t * kc4;
+    const size_t qi = ((size_t)b * P.ND + t) * P.KC;
+    reinterpret_cast<int4*>(P.qidx + qi)[c] = reinterpret_cast<const int4*>(A.idx + (size_t)t * P.KC)[c];
+    reinterpret_cast<float4*>(P.qprob + qi)[c] = reinterpret_cast<const float4*>(A.prob + (size_t)t * P.KC)[c];
+  }
+  if (lane < n_d) P.qcount[(size_t)b * P.ND + lane] = A.cnt[lane];
+  __syncwarp();
+  int codes_in[CP_SPEC_MAX_WINDOW];
+  const int m = S.m;
+  codes_in[0] = S.codes[s_new];
+  for (int i = 1; i < m; ++i) codes_in[i] = S.drafts[i - 1];
+  set_pass_rows<WT>(P, b, S, codes_in);
+}
+
+// Teacher-forced run: copy this chunk's target (and draft) logits out.
+__device__ void teacher_copy(const FrameParams& P, const CallArgs& ca, int b, const StreamState& S) {
+  const int lane = threadIdx.x & 31;
+  const int slots = 1 + P.ND;
+  for (int i = 0; i < S.m; ++i) {
+    const int row = b * P.NS + i, pos = S.pos0 + i;
+    if (pos < 1) continue;
+    for (int t = 0; t <= (ca.t_draft ? P.ND : 0); ++t) {
+      const bool ok = pos + t <= P.G - 1;
+      float* dst = t == 0 ? ca.t_logits + ((size_t)b * (ca.P - 1) + pos - 1) * P.V
+                          : ca.t_draft + (((size_t)b * (ca.P - 1) + pos - 1) * P.ND + (t - 1)) * P.V;
+      const float* src = P.logits + ((size_t)row * slots + t) * P.V;
+      for (int v = 2 * lane; v < P.V; v += 64)
+        *reinterpret_cast<float2*>(dst + v) = ok ? __ldcg(reinterpret_cast<const float2*>(src + v)) : make_float2(0.f, 0.f);
+    }
+  }
+}
+
+// The acceptance decision of stream b for the pass that just ran ("Speculative
+// Decoding, Beyond Text", section 02; "CodePredictor Speculative Decoding",
+// "How a round works" step 3), then the next pass's rows.
+template <typename WT>
+__device__ void accept_stream(const FrameParams& P, const CallArgs& ca, int b, AcceptScratch& A) {
+  StreamState& S = *A.S;
+  const int lane = threadIdx.x & 31;
+  load_state(P, b, S);
+  if (S.phase == kPhaseDone) return;
+  const int slots = 1 + P.ND;
+  StreamStats* ss = P.sstats + b;
+  if (S.phase == kPhaseTeacher) {
+    teacher_copy(P, ca, b, S);
+    __syncwarp();
+    const int next = S.pos0 + S.m;
+    __syncwarp();
+    if (lane == 0) S.pos0 = next;
+    __syncwarp();
+    if (next >= ca.P) retire_stream(P, b, S);
+    else setup_teacher_chunk<WT>(P, ca, b, S);
+    store_state(P, b, S);
+    return;
+  }
+  // Stage the lists this decision reads: the target rows' slot-0 lists
+  // (p_{s+1..s+m}) and, for a speculative round, the saved draft lists q_t.
+  const bool spec = S.phase == kPhaseSpec;
+  const int nl = spec ? S.m + S.n_d : 1;
+  const int row0 = b * P.NS + (S.phase == kPhasePrefill ? 1 : 0);
+  int cnt = 0;
+  if (spec) {
+    if (lane < S.m) cnt = __ldcg(P.lcount + (size_t)(b * P.NS + lane) * slots);
+    else if (lane < nl) cnt = __ldcg(P.qcount + (size_t)b * P.ND + (lane - S.m));
+    for (int i = 0; i < S.m; ++i) {
+      const size_t li = (size_t)(b * P.NS + i) * slots;
+      stage_list_async(P, A, i, P.lidx + li * P.KC, P.lprob + li * P.KC);
+    }
+    for (int t = 0; t < S.n_d; ++t) {
+      const size_t qi = ((size_t)b * P.ND + t) * P.KC;
+      stage_list_async(P, A, S.m + t, P.qidx + qi, P.qprob + qi);
+    }
+  } else {
+    if (lane == 0) cnt = __ldcg(P.lcount + (size_t)row0 * slots);
+    stage_list_async(P, A, 0, P.lidx + (size_t)row0 * slots * P.KC, P.lprob + (size_t)row0 * slots * P.KC);
+  }
+  if (lane < nl) A.cnt[lane] = cnt;
+  cp_async_wait_all();
+  __syncwarp();
+  const int* Li = A.idx;
+  const float* Lp = A.prob;
+  const int KC = P.KC;
+  int s_new = 0, hrow = 0;
+  if (lane == 0) {
+    const uint32_t fr = (uint32_t)S.frame_abs;
+    const int s = S.s;
+    if (!spec) {
+      const int j = s + 1;  // the pass scored c_j
+      const float u = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)j, kTarget);
+      const int c = valid_code(P, list_sample(Li, Lp, A.cnt[0], u));
+      S.codes[j] = c;
+      ca.codes_out[((size_t)S.frame * ca.B + b) * P.G + j] = c;
+      s_new = j;
+      hrow = row0;
+      ss->passes += 1;
+    } else {  // speculative round: exact left-to-right acceptance
+      const int n_d = S.n_d, m = S.m;
+      int t = 1;
+      bool rejected = false;
+      for (; t <= n_d; ++t) {
+        const int y = S.drafts[t - 1];
+        const int qs = m + t - 1, ps = t - 1;  // scratch slots of q_t and p_{s+t}
+        const float qy = list_lookup(Li + (size_t)qs * KC, Lp + (size_t)qs * KC, A.cnt[qs], y);
+        const float py = list_lookup(Li + (size_t)ps * KC, Lp + (size_t)ps * KC, A.cnt[ps], y);
+        const float ratio = __fdiv_rn(py, qy);
+        ss->drafted[t] += 1;
+        const float ua = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + t), kAccept);
+        if (ua < ratio) {
+          S.codes[s + t] = y;
+          ss->accepted[t] += 1;
+          continue;
+        }
+        const float ut = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + t), kTarget);
+        int c = residual_sample(Li + (size_t)ps * KC, Lp + (size_t)ps * KC, A.cnt[ps], Li + (size_t)qs * KC,
+                                Lp + (size_t)qs * KC, A.cnt[qs], ut);
+        if (c < 0) c = list_sample(Li + (size_t)ps * KC, Lp + (size_t)ps * KC, A.cnt[ps], ut);
+        S.codes[s + t] = valid_code(P, c);
+        rejected = true;
+        break;
+      }
+      if (rejected) {
+        s_new = s + t;
+        ss->rejections += 1;
+      } else if (m > n_d) {
+        const float ut = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + n_d + 1), kTarget);
+        S.codes[s + n_d + 1] =
+            valid_code(P, list_sample(Li + (size_t)n_d * KC, Lp + (size_t)n_d * KC, A.cnt[n_d], ut));
+        ss->bonus += 1;
+        s_new = s + n_d + 1;
+      } else {
+        s_new = s + n_d;
+      }
+      for (int j = s + 1; j <= s_new; ++j) ca.codes_out[((size_t)S.frame * ca.B + b) * P.G + j] = S.codes[j];
+      hrow = b * P.NS + (s_new - s - 1);
+      ss->rounds += 1;
+      ss->passes += 1;
+    }
+    if (ca.committed_out) ca.committed_out[b] = s_new + 1;
+  }
+  s_new = __shfl_sync(0xffffffffu, s_new, 0);
+  hrow = __shfl_sync(0xffffffffu, hrow, 0);
+  __syncwarp();
+  after_commit<WT>(P, ca, b, A, s_new, hrow);
+  store_state(P, b, S);
+}
+
+// The rows of the next pass, compacted, and the lm_heads it needs (head_j
+// for j in [pos, pos + ND] of every row at pos >= 1).  One warp.
+__device__ void build_plan(const FrameParams& P, const CallArgs& ca) {
+  const int lane = threadIdx.x & 31;
+  const unsigned lt = (1u << lane) - 1u;
+  int n = 0;
+  const int total = ca.B * P.NS;
+  unsigned long long mask = 0;
+  for (int j0 = 0; j0 < total; j0 += 32) {
+    const int r = j0 + lane;
+    const int pos = r < total ? __ldcg(P.row_pos + r) : -1;
+    const bool on = pos >= 0;
+    const uint32_t bal = __ballot_sync(0xffffffffu, on);
+    if (on) {
+      const int at = n + __popc(bal & lt);
+      P.prow[at] = r;
+      P.ppos[at] = pos;
+      P.pcode[at] = __ldcg(P.row_code + r);
+      if (pos >= 1)
+        for (int t = 0; t <= P.ND && pos + t <= P.G - 1; ++t) mask |= 1ull << (pos + t);
+    }
+    n += __popc(bal);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mask |= __shfl_xor_sync(0xffffffffu, mask, o);
+  if (lane == 0) {
+    int nh = 0;
+    for (int hd = 1; hd < P.G && hd < 64; ++hd)
+      if ((mask >> hd) & 1ull) P.plan->heads[nh++] = hd;
+    P.plan->nheads = nh;
+    P.plan->nrows = n;
+    if (n > 0) {
+      P.ctl->weight_bytes += (long long)P.L * P.layer_bytes + (long long)nh * P.head_bytes;
+      P.ctl->heads_applied += nh;
+    }
+  }
+  __syncwarp();
+}
+
+// Last-CTA election: true in the CTA that finishes last; its threads then
+// see every other CTA's writes (each CTA fences before counting itself).
+__device__ __forceinline__ bool last_cta(Control* ctl) {
+  __shared__ int s_last;
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) s_last = atomicAdd(&ctl->done, 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (s_last) __threadfence();
+  return s_last != 0;
+}
+
+// Sets the pass loop's condition (inside a graph): continue while streams
+// are active and the pass cap is not reached.
+__device__ __forceinline__ void set_loop(const FrameParams& P, bool go) {
+  if (P.cond != 0) cudaGraphSetConditional((cudaGraphConditionalHandle)P.cond, go ? 1u : 0u);
+}
+
+// Stream setup of a call: frame 0 (decode) or the first teacher chunk; then
+// the first pass's plan.
+template <typename WT>
+__global__ void __launch_bounds__(kThreads, 1) setup_kernel(const __grid_constant__ FrameParams P) {
+  extern __shared__ __align__(16) unsigned char ssmem[];
+  const CallArgs ca = *P.call;
+  const int warp = threadIdx.x >> 5;
+  if (blockIdx.x == 0 && threadIdx.x == 0) { P.ctl->active = ca.B; P.ctl->pass = 0; }
+  const int b = blockIdx.x * kWarps + warp;
+  if (b < ca.B) {
+    AcceptScratch A = accept_scratch(P, ssmem);
+    StreamState& S = *A.S;
+    for (int i = threadIdx.x & 31; i < (int)(sizeof(StreamState) / 4); i += 32) reinterpret_cast<int*>(&S)[i] = 0;
+    __syncwarp();
+    if (ca.mode == kModeTeacher) {
+      if ((threadIdx.x & 31) == 0) { S.frame_abs = ca.first_frame; S.pos0 = 0; }
+      setup_teacher_chunk<WT>(P, ca, b, S);
+    } else {
+      setup_frame<WT>(P, ca, b, S, 0);
+    }
+    store_state(P, b, S);
+  }
+  if (!last_cta(P.ctl)) return;
+  if (warp == 0) build_plan(P, ca);
+  if (threadIdx.x == 0) {
+    P.ctl->done = 0;
+    set_loop(P, __ldcg(&P.plan->nrows) > 0);
+  }
+}
+
+// Acceptance of every stream (warp per stream), then the next pass's plan
+// and the loop condition.
+template <typename WT>
+__global__ void __launch_bounds__(kThreads, 1) accept_kernel(const __grid_constant__ FrameParams P) {
+  extern __shared__ __align__(16) unsigned char ssmem[];
+  pdl_wait();
+  const CallArgs ca = *P.call;
+  const int warp = threadIdx.x >> 5;
+  const int b = blockIdx.x * kWarps + warp;
+  if (b < ca.B) {
+    AcceptScratch A = accept_scratch(P, ssmem);
+    accept_stream<WT>(P, ca, b, A);
+  }
+  if (!last_cta(P.ctl)) return;
+  if (warp == 0) build_plan(P, ca);
+  if (threadIdx.x == 0) {
+    Control* ctl = P.ctl;
+    ctl->done = 0;
+    ctl->passes += 1;
+    ctl->kernels += P.kernels_per_pass;
+    const int pass = ctl->pass + 1;
+    ctl->pass = pass;
+    const bool more = __ldcg(&ctl->active) > 0 && __ldcg(&P.plan->nrows) > 0;
+    const bool capped = pass >= ca.pass_cap;
+    if (more && capped && ca.max_passes == 0) raise_status(&ctl->status, kStatusDevice);
+    set_loop(P, more && !capped && __ldcg(&ctl->status) == 0);
+  }
+}
+
+// ------------------------------------------------------------- init kernel
+__global__ void init_tables_kernel(float2* rope, int G, int d, double theta, int* top_k, float* temp, int Bmax, int k,
+                                   float T) {
+  const int half = d / 2;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < G * half; i += gridDim.x * blockDim.x) {
+    const int pos = i / half, e = i % half;
+    const double inv = pow(theta, -2.0 * e / (double)d);
+    const double ang = (double)pos * inv;
+    rope[i] = make_float2((float)cos(ang), (float)sin(ang));
+  }
+  for (int b = blockIdx.x * blockDim.x + threadIdx.x; b < Bmax; b += gridDim.x * blockDim.x) {
+    top_k[b] = k;
+    temp[b] = T;
+  }
+}
+
+}  // namespace cpk
+
+// ------------------------------------------------------------ host side
+namespace cpk_host {
+
+using cpk::FrameParams;
+
+template <typename WT>
+struct KernelSet {
+  static const void* gemv(int kind) {
+    switch (kind) {
+      case cpk::kQKV: return (const void*)cpk::gemv_kernel<WT, cpk::kQKV>;
+      case cpk::kO: return (const void*)cpk::gemv_kernel<WT, cpk::kO>;
+      case cpk::kGU: return (const void*)cpk::gemv_kernel<WT, cpk::kGU>;
+      case cpk::kDown: return (const void*)cpk::gemv_kernel<WT, cpk::kDown>;
+      default: return (const void*)cpk::gemv_kernel<WT, cpk::kHeads>;
+    }
+  }
+  static const void* setup() { return (const void*)cpk::setup_kernel<WT>; }
+  static const void* accept() { return (const void*)cpk::accept_kernel<WT>; }
+};
+
+const void* gemv_fn(int dtype, int kind) {
+  return dtype == 1 ? KernelSet<__nv_bfloat16>::gemv(kind) : KernelSet<float>::gemv(kind);
+}
+const void* setup_fn(int dtype) { return dtype == 1 ? KernelSet<__nv_bfloat16>::setup() : KernelSet<float>::setup(); }
+const void* accept_fn(int dtype) { return dtype == 1 ? KernelSet<__nv_bfloat16>::accept() : KernelSet<float>::accept(); }
+
+// Dynamic shared memory of each kernel for a parameter block.
+size_t gemv_smem(const FrameParams& P, int kind) {
+  // two weight slots, the partial sums of one tile, the pass rows (3
+  // arrays), then (QKV) the RoPE table and (normed kinds) the gain.  Sized
+  // per kind so that consecutive kernels' CTAs fit on one SM together.
+  size_t b = 2 * (size_t)cpk::kSlotBytes + cpk::kRedFloats * sizeof(float) +
+             ((3 * (size_t)P.Bmax * P.NS + 3) / 4 * 4) * sizeof(int);
+  if (kind == cpk::kQKV || kind == cpk::kGU || kind == cpk::kHeads) b += cpk::kRopeSmemBytes + (size_t)P.H * sizeof(float);
+  return b;
+}
+size_t attention_smem(const FrameParams& P) { return ((size_t)64 + (size_t)P.G * P.d) * sizeof(float); }
+size_t topk_smem(const FrameParams& P) {
+  return ((size_t)P.V * 4 + 15) / 16 * 16 + (size_t)cpk::kWarps * 1024 + ((size_t)P.KC * 4 + 15) / 16 * 16 + 256;
+}
+size_t accept_smem(const FrameParams& P, int warps) { return (size_t)warps * cpk::accept_scratch_bytes(P.NS, P.KC); }
+
+// Raise the dynamic shared-memory limit of every pass kernel of a dtype.
+cudaError_t configure_kernels(const FrameParams& P, int accept_warps) {
+  cudaError_t e = cudaSuccess;
+  // every pass kernel asks for the largest shared-memory carve-out, so the
+  // SM configuration never changes between consecutive kernels and a
+  // dependent's CTA can start beside its predecessor's
+  for (int k = cpk::kQKV; k <= cpk::kHeads && e == cudaSuccess; ++k) {
+    e = cudaFuncSetAttribute(gemv_fn(P.dtype, k), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemv_smem(P, k));
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(gemv_fn(P.dtype, k), cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  }
+  const void* others[] = {(const void*)cpk::attention_kernel, (const void*)cpk::topk_kernel, setup_fn(P.dtype),
+                          accept_fn(P.dtype)};
+  for (const void* f : others)
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute((const void*)cpk::attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)attention_smem(P));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute((const void*)cpk::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)topk_smem(P));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(setup_fn(P.dtype), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)accept_smem(P, accept_warps));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(accept_fn(P.dtype), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)accept_smem(P, accept_warps));
+  return e;
+}
+
+static cudaError_t launch(const void* fn, dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, void** args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// Stream setup of a call (not a programmatic dependent: it follows every
+// earlier piece of work on the stream).
+cudaError_t enqueue_setup(const FrameParams& P, int accept_warps, cudaStream_t s) {
+  void* args[] = {const_cast<FrameParams*>(&P)};
+  const int grid = (P.Bmax + accept_warps - 1) / accept_warps;
+  return launch(setup_fn(P.dtype), dim3(grid), dim3(32 * accept_warps), accept_smem(P, accept_warps), s, false, args);
+}
+
+// One pass: 5 L + 3 kernels; the first is a full dependent of earlier work,
+// the others programmatic dependents of their predecessor.
+cudaError_t enqueue_pass(const FrameParams& P, int sms, int accept_warps, cudaStream_t s) {
+  cudaError_t e = cudaSuccess;
+  bool first = true;
+  int l = 0;
+  void* gargs[] = {const_cast<FrameParams*>(&P), &l};
+  void* pargs[] = {const_cast<FrameParams*>(&P)};
+  const int rows = P.Bmax * P.NS;
+  for (l = 0; l < P.L && e == cudaSuccess; ++l) {
+    e = launch(gemv_fn(P.dtype, cpk::kQKV), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kQKV), s, !first, gargs);
+    first = false;
+    if (e == cudaSuccess)
+      e = launch((const void*)cpk::attention_kernel, dim3(rows * P.nq), dim3(cpk::kThreads), attention_smem(P), s, true,
+                 gargs);
+    if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kO), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kO), s, true, gargs);
+    if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kGU), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kGU), s, true, gargs);
+    if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kDown), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kDown), s, true, gargs);
+  }
+  l = 0;
+  if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kHeads), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kHeads), s, true, gargs);
+  if (e == cudaSuccess)
+    e = launch((const void*)cpk::topk_kernel, dim3(rows * (1 + P.ND)), dim3(cpk::kThreads), topk_smem(P), s, true, pargs);
+  if (e == cudaSuccess) {
+    const int grid = (P.Bmax + accept_warps - 1) / accept_warps;
+    e = launch(accept_fn(P.dtype), dim3(grid), dim3(32 * accept_warps), accept_smem(P, accept_warps), s, true, pargs);
+  }
+  return e;
+}
+
+// The graph of a whole call: the setup kernel, then a while loop whose body
+// is one pass; the accept kernel of each pass sets the loop condition.
+// `P.cond` is filled in here.  `cs` is a non-default stream used for capture.
+cudaError_t build_call_graph(FrameParams P, int sms, int accept_warps, cudaStream_t cs, cudaGraphExec_t* out) {
+  cudaGraph_t g = nullptr;
+  cudaError_t e = cudaGraphCreate(&g, 0);
+  if (e != cudaSuccess) return e;
+  cudaGraphConditionalHandle h;
+  e = cudaGraphConditionalHandleCreate(&h, g, 1, cudaGraphCondAssignDefault);
+  P.cond = (unsigned long long)h;
+  cudaGraphNode_t setup_node = nullptr, loop_node = nullptr;
+  if (e == cudaSuccess) {
+    cudaKernelNodeParams kp = {};
+    void* args[] = {&P};
+    kp.func = const_cast<void*>(setup_fn(P.dtype));
+    kp.gridDim = dim3((P.Bmax + accept_warps - 1) / accept_warps);
+    kp.blockDim = dim3(32 * accept_warps);
+    kp.sharedMemBytes = (unsigned)accept_smem(P, accept_warps);
+    kp.kernelParams = args;
+    e = cudaGraphAddKernelNode(&setup_node, g, nullptr, 0, &kp);
+  }
+  cudaGraphNodeParams cp = {};
+  if (e == cudaSuccess) {
+    cp.type = cudaGraphNodeTypeConditional;
+    cp.conditional.handle = h;
+    cp.conditional.type = cudaGraphCondTypeWhile;
+    cp.conditional.size = 1;
+    e = cudaGraphAddNode(&loop_node, g, &setup_node, nullptr, 1, &cp);
+  }
+  if (e == cudaSuccess) {
+    cudaGraph_t body = cp.conditional.phGraph_out[0];
+    e = cudaStreamBeginCaptureToGraph(cs, body, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal);
+    if (e == cudaSuccess) {
+      const cudaError_t e1 = enqueue_pass(P, sms, accept_warps, cs);
+      const cudaError_t e2 = cudaStreamEndCapture(cs, &body);
+      e = e1 != cudaSuccess ? e1 : e2;
+    }
+  }
+  if (e == cudaSuccess) e = cudaGraphInstantiate(out, g, 0);
+  cudaGraphDestroy(g);
+  return e;
+}
+
+cudaError_t launch_init_tables(float2* rope, int G, int d, double theta, int* top_k, float* temp, int Bmax, int k,
+                               float T, cudaStream_t stream) {
+  cpk::init_tables_kernel<<<8, 256, 0, stream>>>(rope, G, d, theta, top_k, temp, Bmax, k, T);
+  return cudaGetLastError();
+}
+
+}  // namespace cpk_host

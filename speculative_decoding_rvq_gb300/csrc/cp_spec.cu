@@ -18,8 +18,11 @@
 #include "cp_frame.cuh"
 
 namespace cpk_host {
-cudaError_t launch_frame_kernel(const cpk::FrameParams& P, int grid, size_t smem, cudaStream_t stream);
-cudaError_t frame_kernel_config(int dtype, size_t smem, int* max_blocks_per_sm);
+cudaError_t configure_kernels(const cpk::FrameParams& P, int accept_warps);
+cudaError_t enqueue_setup(const cpk::FrameParams& P, int accept_warps, cudaStream_t s);
+cudaError_t enqueue_pass(const cpk::FrameParams& P, int sms, int accept_warps, cudaStream_t s);
+cudaError_t build_call_graph(cpk::FrameParams P, int sms, int accept_warps, cudaStream_t cs, cudaGraphExec_t* out);
+size_t accept_smem(const cpk::FrameParams& P, int warps);
 cudaError_t launch_init_tables(float2* rope, int G, int d, double theta, int* top_k, float* temp, int Bmax, int k,
                                float T, cudaStream_t stream);
 cudaError_t launch_accept_batch(int R, int N, int V, int k, float T, unsigned long long seed, int mode,
@@ -32,13 +35,15 @@ struct cp_spec_ctx {
   cp_spec_weights weights;
   cp_spec_config config;
   int N;  // effective window (0 after an AR fallback)
-  int device, grid;
-  size_t smem;
+  int device, sms, accept_warps;
   cpk::Layout lay;
   unsigned char* ws;
   cpk::FrameParams base;
   long long launches;
   std::string err;
+  // the call graph (setup + pass loop), built on the first whole-call decode
+  cudaGraphExec_t graph;
+  cudaStream_t capture;
   // step-wise API
   bool staged, need_setup;
   int staged_B, staged_frame;
@@ -50,7 +55,6 @@ namespace {
 
 std::string g_err = "";
 std::atomic<long long> g_free_launches{0};
-constexpr unsigned long long kBarrierTimeoutNs = 20ull * 1000ull * 1000ull * 1000ull;  // 20 s per wait
 
 cp_spec_status fail(cp_spec_ctx* c, cp_spec_status s, const char* fmt, ...) {
   char buf[512];
@@ -118,92 +122,6 @@ cpk::Layout layout_for(const cp_spec_model* m, const cp_spec_config* cfg, int N)
                           m->num_code_groups, N, KC, cfg->max_streams);
 }
 
-struct SmemPlan {
-  int nslots, slot_bytes, accept_warps, uni_floats, red_floats, hown_cap;
-  int off_ring, off_uni, off_red, off_hown, off_rope;
-  size_t bytes;
-};
-
-// Dynamic shared memory per CTA; the static part (parameter copy, CTA
-// state, top-k histogram) is about 9.6 KB of the 227 KB an SM offers.
-constexpr size_t kDynSmemLimit = 216 * 1024;
-constexpr size_t kMaxSlotBytes = 32 * 1024;
-constexpr size_t kMaxRingBytes = 160 * 1024;
-constexpr size_t kMaxRopeBytes = 16 * 1024;
-constexpr int kKPartHost = 512;  // input elements per GEMV task part (matches the kernel)
-constexpr int kMaxTileRowsHost = 64;
-
-// Dynamic shared memory of the frame kernel:
-// [row lists][owned residual rows][RoPE table][weight ring][GEMV partial sums][phase scratch].
-SmemPlan smem_plan(const cp_spec_model* m, int N, int KC, int Bmax, int grid) {
-  const int NS = N > 2 ? N : 2;
-  const size_t eb = m->dtype == 1 ? 2 : 4;
-  const int H = m->hidden, F = m->ffn, QD = m->n_q_heads * m->head_dim, V = m->vocab, G = m->num_code_groups;
-  const int d = m->head_dim;
-  auto kstride = [&](int K) { return m->dtype == 1 ? (K + 255) / 256 * 256 : K; };
-  const int KSmax = std::max(std::max(kstride(H), kstride(QD)), kstride(F));
-  const size_t max_unit = (size_t)std::max(std::max(2 * H, QD), F) * eb;
-  const size_t max_row = (size_t)std::max(std::max(H, QD), F) * eb;
-  const int rows = Bmax * NS;
-  const size_t rows_b = ((size_t)rows * 12 + 127) / 128 * 128;
-  const int hown_cap = (H + grid - 1) / grid + 1;
-  const size_t hown_b = ((size_t)rows * hown_cap * 4 + 127) / 128 * 128;
-  const size_t rope_raw = (size_t)G * (d / 2) * 8;
-  const size_t rope_b = rope_raw <= kMaxRopeBytes ? (rope_raw + 127) / 128 * 128 : 0;
-  const size_t per_acc = cpk::accept_scratch_bytes(NS, KC);
-  const size_t topk_b = ((size_t)V * 4 + 15) / 16 * 16 + (size_t)cpk::kWarps * 1024 + ((size_t)KC * 4 + 15) / 16 * 16 + 256;
-  const size_t attn_b = ((size_t)64 + (size_t)G * d) * 4;
-  // GEMV tasks read up to kRB - 1 rows past a tile's end: the scratch after the ring covers that
-  const size_t uni_fixed = std::max(std::max(std::max(topk_b, per_acc), attn_b), (size_t)(cpk::kRB - 1) * max_row);
-  const int QGmax = (std::min(rows, 16) + 3) / 4;  // staged row groups never exceed 16 rows
-  SmemPlan best{};
-  // staged input rows: every row of a single-stream pass when that leaves a
-  // ring of at least three 32 KB slots, else four
-  const int want_rows[2] = {std::min(rows, 8), std::min(rows, 4)};
-  for (int a = 0; a < 2 && best.bytes == 0; ++a) {
-    const size_t uni = std::max(uni_fixed, (size_t)want_rows[a] * KSmax * 4);
-    for (size_t slot = kMaxSlotBytes; slot >= max_unit && best.bytes == 0; slot -= 4096) {
-      // partial sums of one wave of tiles: (8-row batches x input parts x row groups) x 32 per tile
-      size_t tmax = 0;
-      auto tstride_of = [&](int K, int rpu) {
-        const int upt = std::max(1, std::min((int)(slot / ((size_t)rpu * K * eb)), kMaxTileRowsHost / rpu));
-        const int KP = (K + kKPartHost - 1) / kKPartHost;
-        tmax = std::max(tmax, (size_t)((upt * rpu + cpk::kRB - 1) / cpk::kRB) * KP * QGmax * cpk::kRedPerTask);
-      };
-      tstride_of(H, 2);
-      tstride_of(QD, 1);
-      tstride_of(F, 1);
-      tstride_of(H, 1);
-      for (int ns = cpk::kMaxSlots; ns >= (a == 0 ? 3 : 2); --ns) {
-        if ((size_t)ns * slot > kMaxRingBytes) continue;
-        const size_t red_floats = (size_t)std::max(1, ns - 2) * tmax;
-        const size_t red_b = (red_floats * 4 + 127) / 128 * 128;
-        const size_t fixed = rows_b + hown_b + rope_b + red_b;
-        if (fixed + (size_t)ns * slot + uni > kDynSmemLimit) continue;
-        // GEMV tasks read up to kRB - 1 rows past a tile's end: keep that much after the ring
-        if (red_b + uni < (size_t)(cpk::kRB - 1) * max_row) continue;
-        SmemPlan p{};
-        p.nslots = ns;
-        p.slot_bytes = (int)slot;
-        p.hown_cap = hown_cap;
-        p.red_floats = (int)red_floats;
-        p.off_hown = (int)rows_b;
-        p.off_rope = rope_b ? (int)(rows_b + hown_b) : -1;
-        p.off_ring = (int)(rows_b + hown_b + rope_b);
-        p.off_red = (int)(p.off_ring + (size_t)ns * slot);
-        p.off_uni = (int)(p.off_red + red_b);
-        const size_t uni_all = (kDynSmemLimit - fixed - (size_t)ns * slot) / 16 * 16;
-        p.uni_floats = (int)(uni_all / 4);
-        p.accept_warps = (int)std::min<size_t>(cpk::kWarps, uni_all / per_acc);
-        p.bytes = (size_t)p.off_uni + uni_all;
-        best = p;
-        break;
-      }
-    }
-  }
-  return best;
-}
-
 template <typename T>
 T* at(unsigned char* base, size_t off) { return reinterpret_cast<T*>(base + off); }
 
@@ -221,42 +139,68 @@ cp_spec_status check_weights(const cp_spec_model* model, const cp_spec_weights* 
   return CP_SPEC_OK;
 }
 
-// Device facts and the shared-memory plan of one frame-kernel configuration.
-struct DevicePlan {
-  int dev, sms, KC;
-  SmemPlan sp;
-};
+// Shape limits of the pass kernels (checked before anything is launched).
+constexpr size_t kSmemPerSm = 227 * 1024;
+constexpr int kMaxChunksPerRow = 3 * cpk::kThreads;  // a GEMV thread owns at most 3 chunks of a row
+constexpr int kRedFloatsHost = 1280;                 // the GEMV kernel's partial-sum buffer (floats)
 
-// Queries the current device and checks that the configuration fits the
-// frame kernel (cooperative launch, register-held rows, shared memory, one
-// accept warp per stream).  Sets the kernel's shared-memory attribute.
-cp_spec_status plan_device(const cp_spec_model* model, const cp_spec_config* config, int N, DevicePlan* dp) {
-  int dev = 0, sms = 0, coop = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-  if (e != cudaSuccess) return check_cuda(nullptr, e, "device query");
-  if (!coop) return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "device does not support cooperative launches");
-  const int KC = list_capacity(model, config);
-  const SmemPlan sp = smem_plan(model, N, KC, config->max_streams, sms);
-  if (sp.bytes == 0)
-    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "shapes do not fit the frame kernel's shared memory (top_k %d, window %d)",
-                config->top_k, config->verify_window);
-  if (sp.accept_warps < 1)
-    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "top_k %d too large for verify window %d (accept lists exceed shared memory)",
-                config->top_k, config->verify_window);
-  int maxb = 0;
-  e = cpk_host::frame_kernel_config(model->dtype, sp.bytes, &maxb);
-  if (e != cudaSuccess) return check_cuda(nullptr, e, "frame kernel attributes");
-  if (maxb < 1) return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "frame kernel needs %zu bytes of shared memory per CTA", sp.bytes);
-  if ((long long)config->max_streams > (long long)sms * sp.accept_warps)
-    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "max_streams above %d (one accept warp per stream)", sms * sp.accept_warps);
-  *dp = DevicePlan{dev, sms, KC, sp};
+cp_spec_status check_shapes(const cp_spec_model* m, int N, int KC) {
+  const size_t eb = m->dtype == 1 ? 2 : 4;
+  const int H = m->hidden, F = m->ffn, QD = m->n_q_heads * m->head_dim;
+  const size_t unit = std::max(std::max((size_t)2 * H, (size_t)QD), (size_t)F) * eb;
+  if (unit > (size_t)cpk::kSlotBytes)
+    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "a weight row pair of %zu bytes exceeds the %d-byte tile", unit, cpk::kSlotBytes);
+  const size_t maxk = (size_t)std::max(std::max(H, QD), F) * eb / 16;
+  if (maxk > (size_t)kMaxChunksPerRow)
+    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "GEMV width %zu bytes above %d", maxk * 16, kMaxChunksPerRow * 16);
+  if (m->num_code_groups > 64 || (size_t)(64 + m->num_code_groups * m->head_dim) * 4 > kSmemPerSm)
+    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "attention scratch too large");
+  // partial sums of one GEMV tile: rows x 4 input rows x warps per row group
+  // (the kernel's tile and row-group geometry, restated)
+  const int Ks[4] = {H, QD, F, H};
+  const int rpus[4] = {2, 1, 1, 1};
+  for (int i = 0; i < 4; ++i) {
+    const int nch = (int)((size_t)Ks[i] * eb / 16);
+    const int TPG = std::min(cpk::kThreads, (nch + 31) / 32 * 32);
+    const int WPG = TPG / 32;
+    const int rows = std::max(1, std::min((int)(cpk::kSlotBytes / ((size_t)rpus[i] * nch * 16)), cpk::kMaxTileRows / rpus[i])) * rpus[i];
+    if ((size_t)rows * 4 * WPG > (size_t)kRedFloatsHost / 2)  // two tiles' sums at once
+      return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "GEMV partial-sum buffer too small for width %d", Ks[i]);
+  }
+  (void)N;
+  (void)KC;
   return CP_SPEC_OK;
 }
 
-// Fills the launch-invariant part of the frame kernel's parameters: model
-// shape, plan, weight pointers and the carve-up of the workspace at `ws`.
+// Device facts of one configuration.
+struct DevicePlan {
+  int dev, sms, KC, accept_warps;
+};
+
+// Queries the current device and checks that the configuration fits the
+// pass kernels (shared memory of the top-k and accept kernels).
+cp_spec_status plan_device(const cp_spec_model* model, const cp_spec_config* config, int N, DevicePlan* dp) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) return check_cuda(nullptr, e, "device query");
+  const int KC = list_capacity(model, config);
+  cp_spec_status v = check_shapes(model, N, KC);
+  if (v != CP_SPEC_OK) return v;
+  const int NS = N > 2 ? N : 2;
+  const size_t per_warp = cpk::accept_scratch_bytes(NS, KC);
+  const int aw = (int)std::min<size_t>(cpk::kWarps, kSmemPerSm / per_warp);
+  if (aw < 1)
+    return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "top_k %d too large for verify window %d (accept lists exceed shared memory)",
+                config->top_k, config->verify_window);
+  const size_t topk_b = ((size_t)model->vocab * 4 + 15) / 16 * 16 + (size_t)cpk::kWarps * 1024 + ((size_t)KC * 4 + 15) / 16 * 16 + 256;
+  if (topk_b > kSmemPerSm) return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "vocabulary too large for the top-k kernel");
+  *dp = DevicePlan{dev, sms, KC, aw};
+  return CP_SPEC_OK;
+}
+
+// Fills the launch-invariant parameters: model shape, weight pointers and
+// the carve-up of the workspace at `ws`.
 void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, const cp_spec_config* config, int N,
                  const DevicePlan& dp, const cpk::Layout& lay, unsigned char* ws, cpk::FrameParams* out) {
   cpk::FrameParams& P = *out;
@@ -268,16 +212,9 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
   P.eps = model->rms_eps;
   P.N = N; P.NS = NS; P.ND = N > 1 ? N - 1 : 0; P.KC = dp.KC;
   P.Bmax = config->max_streams;
-  P.nslots = dp.sp.nslots;
-  P.slot_bytes = dp.sp.slot_bytes;
-  P.accept_warps = dp.sp.accept_warps;
-  P.off_ring = dp.sp.off_ring; P.off_uni = dp.sp.off_uni; P.off_red = dp.sp.off_red; P.off_hown = dp.sp.off_hown;
-  P.off_rope = dp.sp.off_rope;
-  P.uni_floats = dp.sp.uni_floats;
-  P.red_floats = dp.sp.red_floats;
-  P.hown_cap = dp.sp.hown_cap;
+  P.kernels_per_pass = 5 * L + 3;
   P.seed = config->seed;
-  P.timeout_ns = kBarrierTimeoutNs;
+  P.cond = 0;
   const long long eb = model->dtype == 1 ? 2 : 4;
   const long long H = model->hidden, qd = (long long)model->n_q_heads * model->head_dim,
                   kvd = (long long)model->n_kv_heads * model->head_dim, F = model->ffn;
@@ -289,22 +226,47 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
     P.wv[l] = weights->wv[l]; P.wo[l] = weights->wo[l]; P.ffn_norm[l] = weights->ffn_norm[l];
     P.w_gate[l] = weights->w_gate[l]; P.w_up[l] = weights->w_up[l]; P.w_down[l] = weights->w_down[l];
   }
-  P.hpub = at<cpk::xel>(ws, lay.hpub); P.qpub = at<cpk::xel>(ws, lay.qpub); P.opub = at<cpk::xel>(ws, lay.opub);
-  P.apub = at<cpk::xel>(ws, lay.apub); P.kv = at<cpk::xel>(ws, lay.kv); P.logits = at<cpk::xel>(ws, lay.logits);
-  P.lidx = at<int>(ws, lay.lidx); P.lprob = at<float>(ws, lay.lprob);
-  P.lflag = at<unsigned long long>(ws, lay.lflag);
+  P.h = at<float>(ws, lay.h); P.qbuf = at<float>(ws, lay.qbuf); P.abuf = at<float>(ws, lay.abuf);
+  P.fbuf = at<float>(ws, lay.fbuf); P.kv = at<float>(ws, lay.kv); P.logits = at<float>(ws, lay.logits);
+  P.lidx = at<int>(ws, lay.lidx); P.lprob = at<float>(ws, lay.lprob); P.lcount = at<int>(ws, lay.lcount);
   P.qidx = at<int>(ws, lay.qidx); P.qprob = at<float>(ws, lay.qprob); P.qcount = at<int>(ws, lay.qcount);
-  P.row_pos = at<int>(ws, lay.row_pos); P.row_code = at<int>(ws, lay.row_code); P.st = at<cpk::StreamState>(ws, lay.st);
-  P.sstats = at<cpk::StreamStats>(ws, lay.sstats); P.rope = at<float2>(ws, lay.rope);
+  P.row_pos = at<int>(ws, lay.row_pos); P.row_code = at<int>(ws, lay.row_code);
+  P.prow = at<int>(ws, lay.prow); P.ppos = at<int>(ws, lay.ppos); P.pcode = at<int>(ws, lay.pcode);
+  P.plan = at<cpk::Plan>(ws, lay.plan);
+  P.st = at<cpk::StreamState>(ws, lay.st); P.sstats = at<cpk::StreamStats>(ws, lay.sstats); P.rope = at<float2>(ws, lay.rope);
   P.top_k = at<int>(ws, lay.top_k); P.temp = at<float>(ws, lay.temp); P.ctl = at<cpk::Control>(ws, lay.ctl);
+  P.call = at<cpk::CallArgs>(ws, lay.call);
 }
 
-cp_spec_status enqueue_frame(cp_spec_ctx* c, const cpk::FrameParams& P, bool clear_masks, cudaStream_t s) {
-  cpk::Control* ctl = at<cpk::Control>(c->ws, c->lay.ctl);
-  cudaError_t e = cudaMemsetAsync(ctl, 0, clear_masks ? 3 * sizeof(unsigned long long) : sizeof(unsigned long long), s);
-  if (e != cudaSuccess) return check_cuda(c, e, "cudaMemsetAsync(control)");
-  e = cpk_host::launch_frame_kernel(P, c->grid, c->smem, s);
-  if (e != cudaSuccess) return check_cuda(c, e, "frame kernel launch");
+// Pass cap of a call: every pass commits at least one code of every
+// unfinished stream, so a decode needs at most n_frames * (G - 1) passes and
+// a teacher run ceil(P / NS); anything beyond that is a logic error,
+// reported, not looped.
+int pass_cap_of(const cpk::FrameParams& P, const cpk::CallArgs& ca) {
+  if (ca.max_passes > 0) return ca.max_passes;
+  if (ca.mode == cpk::kModeTeacher) return (ca.P + P.NS - 1) / P.NS + 1;
+  return ca.n_frames * (P.G - 1) + 1;
+}
+
+// Copies the call arguments to the device (ordered on `s`).
+cp_spec_status put_call(cp_spec_ctx* c, const cpk::FrameParams& P, cpk::CallArgs ca, cudaStream_t s) {
+  ca.pass_cap = pass_cap_of(P, ca);
+  cudaError_t e = cudaMemcpyAsync(P.call, &ca, sizeof ca, cudaMemcpyHostToDevice, s);
+  return check_cuda(c, e, "call arguments copy");
+}
+
+// A whole call through the context's graph (built on first use).
+cp_spec_status run_call(cp_spec_ctx* c, const cpk::CallArgs& ca, cudaStream_t s) {
+  if (!c->graph) {
+    cudaError_t e = cudaSuccess;
+    if (!c->capture) e = cudaStreamCreateWithFlags(&c->capture, cudaStreamNonBlocking);
+    if (e == cudaSuccess) e = cpk_host::build_call_graph(c->base, c->sms, c->accept_warps, c->capture, &c->graph);
+    if (e != cudaSuccess) { c->graph = nullptr; return check_cuda(c, e, "call graph"); }
+  }
+  cp_spec_status v = put_call(c, c->base, ca, s);
+  if (v != CP_SPEC_OK) return v;
+  cudaError_t e = cudaGraphLaunch(c->graph, s);
+  if (e != cudaSuccess) return check_cuda(c, e, "graph launch");
   c->launches += 1;
   return CP_SPEC_OK;
 }
@@ -332,6 +294,38 @@ cp_spec_status static_scratch(int dev, unsigned char** out) {
     g_static_addr[dev] = static_cast<unsigned char*>(p);
   }
   *out = g_static_addr[dev];
+  return CP_SPEC_OK;
+}
+
+// The call graph of cp_spec_decode_frames_static, cached per device for the
+// last parameter block it was built for (rebuilt, after a device
+// synchronisation, when the model, weights or configuration change).
+struct StaticGraph {
+  bool valid;
+  cpk::FrameParams P;
+  cudaGraphExec_t exec;
+  cudaStream_t capture;
+};
+StaticGraph g_static_graph[kMaxStaticDevices];
+
+cp_spec_status static_graph(const DevicePlan& dp, const cpk::FrameParams& P, cudaGraphExec_t* out) {
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  StaticGraph& sg = g_static_graph[dp.dev];
+  if (sg.valid && memcmp(&sg.P, &P, sizeof P) == 0) { *out = sg.exec; return CP_SPEC_OK; }
+  cudaError_t e = cudaSuccess;
+  if (sg.valid) {
+    e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaGraphExecDestroy(sg.exec);
+    sg.valid = false;
+    if (e != cudaSuccess) return check_cuda(nullptr, e, "static graph rebuild");
+  }
+  if (!sg.capture) e = cudaStreamCreateWithFlags(&sg.capture, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cpk_host::configure_kernels(P, dp.accept_warps);
+  if (e == cudaSuccess) e = cpk_host::build_call_graph(P, dp.sms, dp.accept_warps, sg.capture, &sg.exec);
+  if (e != cudaSuccess) return check_cuda(nullptr, e, "static call graph");
+  sg.P = P;
+  sg.valid = true;
+  *out = sg.exec;
   return CP_SPEC_OK;
 }
 
@@ -368,17 +362,20 @@ cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* w
   c->config = *config;
   c->N = N;
   c->device = dp.dev;
-  c->grid = dp.sms;
-  c->smem = dp.sp.bytes;
+  c->sms = dp.sms;
+  c->accept_warps = dp.accept_warps;
   c->lay = lay;
   c->ws = static_cast<unsigned char*>(d_workspace);
   c->launches = 0;
+  c->graph = nullptr;
+  c->capture = nullptr;
   c->staged = c->need_setup = false;
 
   cpk::FrameParams& P = c->base;
   fill_params(model, weights, config, N, dp, lay, c->ws, &P);
 
-  cudaError_t e = cudaMemset(c->ws, 0, lay.total);
+  cudaError_t e = cpk_host::configure_kernels(P, dp.accept_warps);
+  if (e == cudaSuccess) e = cudaMemset(c->ws, 0, lay.total);
   if (e == cudaSuccess)
     e = cudaMemset(P.row_pos, 0xFF, sizeof(int) * (size_t)config->max_streams * P.NS);
   if (e == cudaSuccess)
@@ -422,13 +419,13 @@ cp_spec_status cp_spec_decode_frames(cp_spec_ctx* c, int32_t n_streams, int32_t 
   if (n_frames == 0) return CP_SPEC_OK;
   if (!d_x || !d_c0 || !d_codes || !aligned16(d_x) || !aligned16(d_c0) || !aligned16(d_codes))
     return fail(c, CP_SPEC_E_INVALID, "x/c0/codes null or not 16-byte aligned");
-  cpk::FrameParams P = c->base;
-  P.mode = cpk::kModeDecode;
-  P.B = n_streams; P.n_frames = n_frames; P.first_frame = first_frame;
-  P.max_passes = 0; P.do_setup = 1;
-  P.x = d_x; P.c0 = d_c0; P.codes_out = d_codes; P.committed_out = nullptr;
+  cpk::CallArgs ca{};
+  ca.mode = cpk::kModeDecode;
+  ca.B = n_streams; ca.n_frames = n_frames; ca.first_frame = first_frame;
+  ca.max_passes = 0;
+  ca.x = d_x; ca.c0 = d_c0; ca.codes_out = d_codes; ca.committed_out = nullptr;
   c->staged = false;
-  return enqueue_frame(c, P, true, static_cast<cudaStream_t>(stream));
+  return run_call(c, ca, static_cast<cudaStream_t>(stream));
 }
 
 cp_spec_status cp_spec_begin_frame(cp_spec_ctx* c, int32_t n_streams, const float* d_x, const int32_t* d_c0,
@@ -452,14 +449,25 @@ cp_spec_status cp_spec_round(cp_spec_ctx* c, int32_t* d_codes, int32_t* d_commit
   if (!c->staged) return fail(c, CP_SPEC_E_STATE, "cp_spec_round before cp_spec_begin_frame");
   if (!d_codes || !aligned16(d_codes) || (d_committed && !aligned16(d_committed)))
     return fail(c, CP_SPEC_E_INVALID, "codes null or misaligned");
-  cpk::FrameParams P = c->base;
-  P.mode = cpk::kModeDecode;
-  P.B = c->staged_B; P.n_frames = 1; P.first_frame = c->staged_frame;
-  P.max_passes = 1; P.do_setup = c->need_setup ? 1 : 0;
-  P.x = c->staged_x; P.c0 = c->staged_c0; P.codes_out = d_codes; P.committed_out = d_committed;
-  const bool setup = c->need_setup;
-  c->need_setup = false;
-  return enqueue_frame(c, P, setup, static_cast<cudaStream_t>(stream));
+  cpk::CallArgs ca{};
+  ca.mode = cpk::kModeDecode;
+  ca.B = c->staged_B; ca.n_frames = 1; ca.first_frame = c->staged_frame;
+  ca.max_passes = 1;
+  ca.x = c->staged_x; ca.c0 = c->staged_c0; ca.codes_out = d_codes; ca.committed_out = d_committed;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cp_spec_status v = put_call(c, c->base, ca, s);
+  if (v != CP_SPEC_OK) return v;
+  cudaError_t e = cudaSuccess;
+  if (c->need_setup) {
+    e = cpk_host::enqueue_setup(c->base, c->accept_warps, s);
+    if (e != cudaSuccess) return check_cuda(c, e, "setup launch");
+    c->launches += 1;
+    c->need_setup = false;
+  }
+  e = cpk_host::enqueue_pass(c->base, c->sms, c->accept_warps, s);
+  if (e != cudaSuccess) return check_cuda(c, e, "pass launch");
+  c->launches += c->base.kernels_per_pass;
+  return CP_SPEC_OK;
 }
 
 cp_spec_status cp_spec_teacher_logits(cp_spec_ctx* c, int32_t n_streams, int32_t P_, const float* d_x,
@@ -471,14 +479,14 @@ cp_spec_status cp_spec_teacher_logits(cp_spec_ctx* c, int32_t n_streams, int32_t
     return fail(c, CP_SPEC_E_INVALID, "x/codes/logits null or misaligned");
   if (d_draft_logits && (c->N < 2 || !aligned16(d_draft_logits)))
     return fail(c, CP_SPEC_E_INVALID, "draft logits need a speculative window and 16-byte alignment");
-  cpk::FrameParams P = c->base;
-  P.mode = cpk::kModeTeacher;
-  P.B = n_streams; P.n_frames = 1; P.first_frame = 0;
-  P.max_passes = 0; P.do_setup = 1;
-  P.x = d_x; P.c0 = nullptr; P.codes_out = nullptr; P.committed_out = nullptr;
-  P.P = P_; P.t_codes = d_codes; P.t_logits = d_logits; P.t_draft = d_draft_logits;
+  cpk::CallArgs ca{};
+  ca.mode = cpk::kModeTeacher;
+  ca.B = n_streams; ca.n_frames = 1; ca.first_frame = 0;
+  ca.max_passes = 0;
+  ca.x = d_x; ca.c0 = nullptr; ca.codes_out = nullptr; ca.committed_out = nullptr;
+  ca.P = P_; ca.t_codes = d_codes; ca.t_logits = d_logits; ca.t_draft = d_draft_logits;
   c->staged = false;
-  return enqueue_frame(c, P, true, static_cast<cudaStream_t>(stream));
+  return run_call(c, ca, static_cast<cudaStream_t>(stream));
 }
 
 cp_spec_status cp_spec_accept_batch(int32_t R, int32_t N, int32_t V, int32_t top_k, float temperature, uint64_t seed,
@@ -536,10 +544,11 @@ cp_spec_status cp_spec_decode_frames_static(const cp_spec_model* model, const cp
 
   cpk::FrameParams P;
   fill_params(model, weights, config, N, dp, lay, ws, &P);
-  P.mode = cpk::kModeDecode;
-  P.B = n_streams; P.n_frames = n_frames; P.first_frame = first_frame;
-  P.max_passes = 0; P.do_setup = 1;
-  P.x = d_x; P.c0 = d_c0; P.codes_out = d_codes; P.committed_out = nullptr;
+  cpk::CallArgs ca{};
+  ca.mode = cpk::kModeDecode;
+  ca.B = n_streams; ca.n_frames = n_frames; ca.first_frame = first_frame;
+  ca.max_passes = 0;
+  ca.x = d_x; ca.c0 = d_c0; ca.codes_out = d_codes; ca.committed_out = nullptr;
 
   // Same starting state as a fresh cp_spec_init, enqueued on the caller's stream.
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -549,13 +558,18 @@ cp_spec_status cp_spec_decode_frames_static(const cp_spec_model* model, const cp
     e = cpk_host::launch_init_tables(P.rope, P.G, P.d, (double)model->rope_theta, P.top_k, P.temp, config->max_streams,
                                      config->top_k, config->temperature, s);
   if (e != cudaSuccess) return check_cuda(nullptr, e, "static scratch initialisation");
-  e = cpk_host::launch_frame_kernel(P, dp.sms, dp.sp.bytes, s);
-  if (e != cudaSuccess) return check_cuda(nullptr, e, "frame kernel launch");
+  v = put_call(nullptr, P, ca, s);
+  if (v != CP_SPEC_OK) return v;
+  cudaGraphExec_t g = nullptr;
+  v = static_graph(dp, P, &g);
+  if (v != CP_SPEC_OK) return v;
+  e = cudaGraphLaunch(g, s);
+  if (e != cudaSuccess) return check_cuda(nullptr, e, "graph launch");
   if (d_status) {
     e = cudaMemcpyAsync(d_status, &P.ctl->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) return check_cuda(nullptr, e, "status copy");
   }
-  g_free_launches.fetch_add(2);
+  g_free_launches.fetch_add(3);
   if (N != window_of(config)) {
     fail(nullptr, CP_SPEC_W_AR_FALLBACK,
          "speculation disabled: fewer than 3 code groups leave no draft slot; running the autoregressive loop");
@@ -573,7 +587,7 @@ cp_spec_status cp_spec_status_word(cp_spec_ctx* c, void* stream) {
   e = cudaMemcpy(&st, &ctl->status, sizeof(int), cudaMemcpyDeviceToHost);
   if (e == cudaSuccess && st != 0) e = cudaMemset(&ctl->status, 0, sizeof(int));
   if (e != cudaSuccess) return check_cuda(c, e, "status word read");
-  if (st == CP_SPEC_E_DEVICE_TIMEOUT) return fail(c, CP_SPEC_E_DEVICE_TIMEOUT, "a device grid barrier timed out");
+  if (st == CP_SPEC_E_DEVICE_TIMEOUT) return fail(c, CP_SPEC_E_DEVICE_TIMEOUT, "a weight tile copy did not land in time");
   if (st != 0) return fail(c, CP_SPEC_E_DEVICE, "device-side check failed (code out of range)");
   return CP_SPEC_OK;
 }
@@ -599,7 +613,7 @@ cp_spec_status cp_spec_read_stats(cp_spec_ctx* c, cp_spec_stats* out, void* stre
   out->weight_bytes = ctl.weight_bytes;
   out->kv_bytes = ctl.kv_bytes;
   out->heads_applied = ctl.heads_applied;
-  for (int i = 0; i < 8; ++i) out->phase_ns[i] = ctl.phase_ns[i];
+  out->kernel_launches = ctl.kernels;
   delete[] hs;
   return CP_SPEC_OK;
 }
@@ -609,7 +623,7 @@ cp_spec_status cp_spec_reset_stats(cp_spec_ctx* c, void* stream) {
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(c->base.sstats, 0, sizeof(cpk::StreamStats) * c->config.max_streams, s);
   if (e == cudaSuccess)
-    e = cudaMemsetAsync(&c->base.ctl->weight_bytes, 0, 12 * sizeof(long long), s);
+    e = cudaMemsetAsync(&c->base.ctl->weight_bytes, 0, cpk::kControlCounters * sizeof(long long), s);
   return check_cuda(c, e, "reset stats");
 }
 
@@ -619,6 +633,11 @@ int64_t cp_spec_launch_count(const cp_spec_ctx* c) {
 
 const char* cp_spec_last_error(const cp_spec_ctx* c) { return c ? c->err.c_str() : g_err.c_str(); }
 
-void cp_spec_destroy(cp_spec_ctx* c) { delete c; }
+void cp_spec_destroy(cp_spec_ctx* c) {
+  if (!c) return;
+  if (c->graph) cudaGraphExecDestroy(c->graph);
+  if (c->capture) cudaStreamDestroy(c->capture);
+  delete c;
+}
 
 }  // extern "C"
