@@ -138,11 +138,20 @@ struct FrameParams {
   CallArgs* call;
 };
 
-// Per-warp shared scratch of the accept kernel: the stream state plus 2*NS
-// staged probability lists (index and probability arrays of capacity KC)
-// and their lengths.
+// Staged probability lists of one stream in the accept kernel: the target
+// lists of its NS row slots, the ND saved draft lists q_t, and the ND draft
+// slots of each row (the next pass's candidates).
+inline __host__ __device__ int accept_lists(int NS) {
+  const int ND = NS > 2 ? NS - 1 : 1;  // NS = max(N, 2); ND slots per row (at least one list of room)
+  return NS + ND + NS * ND;
+}
+
+// Per-warp shared scratch of the accept kernel: the stream state, the staged
+// lists (index and probability arrays of capacity KC), one list of residual
+// weights, 32 uniforms and the list lengths.
 inline __host__ __device__ size_t accept_scratch_bytes(int NS, int KC) {
-  return (sizeof(StreamState) + (size_t)2 * NS * KC * 8 + (size_t)2 * NS * 4 + 15) / 16 * 16;
+  const size_t n = (size_t)accept_lists(NS);
+  return (sizeof(StreamState) + n * KC * 8 + (size_t)KC * 4 + 32 * 4 + n * 4 + 15) / 16 * 16;
 }
 
 // Workspace carve-up, computed identically by the host for sizing.

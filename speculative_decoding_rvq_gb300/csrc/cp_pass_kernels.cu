@@ -739,9 +739,8 @@ __global__ void __launch_bounds__(kThreads, 2) attention_kernel(const __grid_con
 // e = cp_expf(z - zmax), S = float32 sum of e in ascending index order,
 // p = fl32(e / S); T = 0 is argmax (lowest index).  Thread t owns indices
 // [t*E, t*E + E).  The k-th key is found by an MSB-first 8-bit radix select
-// over warp-private histograms (increments aggregated per bin across the
-// warp, no atomics); one scan of packed (greater, equal) counts places every
-// kept entry in index order.  Scratch: hw [kWarps][256], ebuf [min(k, V)],
+// over warp-private histograms (shared-memory atomic increments); one scan
+// of packed (greater, equal) counts places every kept entry in index order.  Scratch: hw [kWarps][256], ebuf [min(k, V)],
 // sx [64].  Returns the length.
 __device__ __noinline__ int block_topk(int V, int k, float T, uint32_t* keys, uint32_t* hw, float* ebuf, int* sx,
                                        int* out_idx, float* out_prob) {
@@ -795,18 +794,17 @@ __device__ __noinline__ int block_topk(int V, int k, float T, uint32_t* keys, ui
   bool eq_all = (kk == V);
   uint32_t* my = hw + warp * 256;
   for (int shift = 24; shift >= 0 && !eq_all; shift -= 8) {
-    // warp-private histogram, aggregated increments (no atomics: one leader per bin per step)
+    // warp-private histogram (shared-memory atomics; integer counts, so the
+    // result does not depend on their order)
 #pragma unroll
     for (int j = 0; j < 8; ++j) my[lane * 8 + j] = 0;
     __syncwarp();
     for (int e = 0; e < E; ++e) {
       const int i = i0 + e;
-      const uint32_t key = i < i1 ? keys[i] : 0u;
-      const bool hit = i < i1 && (key & mask) == prefix;
-      const uint32_t bin = (key >> shift) & 255u;
-      const unsigned grpm = __match_any_sync(0xffffffffu, hit ? bin : 0xFFFFFFFFu);
-      if (hit && lane == __ffs(grpm) - 1) my[bin] += (uint32_t)__popc(grpm);
-      __syncwarp();
+      if (i < i1) {
+        const uint32_t key = keys[i];
+        if ((key & mask) == prefix) atomicAdd(&my[(key >> shift) & 255u], 1u);
+      }
     }
     __syncthreads();
     if (warp == 0) {
@@ -924,6 +922,20 @@ __device__ __forceinline__ int valid_code(const FrameParams& P, int c) {
   return c;
 }
 
+// When the setup or accept kernel runs as a single CTA, the rows it records
+// are mirrored in shared memory so that its plan is built without a round
+// trip through L2.
+constexpr int kMirrorRows = 64;
+__shared__ int g_mirror_on;
+__shared__ int g_mpos[kMirrorRows];
+__shared__ int g_mcode[kMirrorRows];
+
+__device__ __forceinline__ void mirror_init(const FrameParams& P, const CallArgs& ca) {
+  if (threadIdx.x == 0) g_mirror_on = (gridDim.x == 1 && ca.B * P.NS <= kMirrorRows) ? 1 : 0;
+  for (int i = threadIdx.x; i < kMirrorRows; i += blockDim.x) { g_mpos[i] = -1; g_mcode[i] = 0; }
+  __syncthreads();
+}
+
 // Record the rows of stream b's next pass (state already updated in S):
 // positions pos0.. and the code whose embedding each row carries (the frame
 // index for the x row at position 0).  Warp-wide.
@@ -935,6 +947,10 @@ __device__ __noinline__ void set_pass_rows(const FrameParams& P, int b, const St
     const int on = lane < S.m;
     P.row_pos[b * P.NS + lane] = on ? S.pos0 + lane : -1;
     P.row_code[b * P.NS + lane] = on ? codes_in[lane] : 0;
+    if (g_mirror_on) {
+      g_mpos[b * P.NS + lane] = on ? S.pos0 + lane : -1;
+      g_mcode[b * P.NS + lane] = on ? codes_in[lane] : 0;
+    }
   }
   if (lane == 0) {
     const long long kvb = (long long)(S.pos0 + S.m) * P.L * 2 * P.nkv * P.d * (long long)sizeof(float);
@@ -951,6 +967,8 @@ __device__ __forceinline__ void retire_stream(const FrameParams& P, int b, Strea
     S.phase = kPhaseDone;
     S.m = 0;
     for (int i = 0; i < P.NS; ++i) P.row_pos[b * P.NS + i] = -1;
+    if (g_mirror_on)
+      for (int i = 0; i < P.NS; ++i) g_mpos[b * P.NS + i] = -1;
     atomicSub(&P.ctl->active, 1);
   }
   __syncwarp();
@@ -1014,22 +1032,41 @@ __device__ __forceinline__ void store_state(const FrameParams& P, int b, const S
   __syncwarp();
 }
 
-// Per-warp view of the accept scratch (see accept_scratch_bytes).
+// Counter increment that does not wait for the old value (a reduction in
+// L2): the accept path never reads its counters back.
+__device__ __forceinline__ void bump(long long& c, long long v = 1) {
+  atomicAdd(reinterpret_cast<unsigned long long*>(&c), (unsigned long long)v);
+}
+
+// Per-warp view of the accept scratch (see accept_scratch_bytes).  List
+// slots: target list of row i of the stream at i (i < NS), saved draft list
+// q_t at NS + t - 1, draft slot t of row i at NS + NDr + i * NDr + t - 1.
 struct AcceptScratch {
   StreamState* S;
-  int* idx;    // [2*NS][KC]
-  float* prob; // [2*NS][KC]
-  int* cnt;    // [2*NS]
+  int* idx;    // [lists][KC]
+  float* prob; // [lists][KC]
+  int* cnt;    // [lists]
+  float* r;    // [KC] residual weights
+  float* u;    // [32] Philox uniforms of the decision
+  int NS, NDr;
+  __device__ __forceinline__ int tslot(int i) const { return i; }
+  __device__ __forceinline__ int qslot(int t) const { return NS + t - 1; }
+  __device__ __forceinline__ int dslot(int i, int t) const { return NS + NDr + i * NDr + t - 1; }
 };
 
 __device__ __forceinline__ AcceptScratch accept_scratch(const FrameParams& P, unsigned char* base_all) {
   const int warp = threadIdx.x >> 5;
+  const int n = accept_lists(P.NS);
   unsigned char* base = base_all + (size_t)warp * accept_scratch_bytes(P.NS, P.KC);
   AcceptScratch a;
   a.S = reinterpret_cast<StreamState*>(base);
   a.idx = reinterpret_cast<int*>(base + sizeof(StreamState));
-  a.prob = reinterpret_cast<float*>(a.idx + (size_t)2 * P.NS * P.KC);
-  a.cnt = reinterpret_cast<int*>(a.prob + (size_t)2 * P.NS * P.KC);
+  a.prob = reinterpret_cast<float*>(a.idx + (size_t)n * P.KC);
+  a.r = a.prob + (size_t)n * P.KC;
+  a.u = a.r + P.KC;
+  a.cnt = reinterpret_cast<int*>(a.u + 32);
+  a.NS = P.NS;
+  a.NDr = P.NS > 2 ? P.NS - 1 : 1;
   return a;
 }
 
@@ -1039,8 +1076,58 @@ __device__ __forceinline__ void stage_list_async(const FrameParams& P, AcceptScr
   warp_copy_async(A.prob + (size_t)slot * P.KC, gprob, P.KC * 4);
 }
 
+// Categorical draw from a shared-memory list (idx, w) of n entries (arrays
+// 16-byte aligned, capacity a multiple of 4), one thread, with the semantics
+// of list_sample: sequential float32 prefix sums over entries with w > 0 in
+// index order, t = fl32(u * S), the first entry whose prefix exceeds t, else
+// the last candidate; -1 when no entry is positive.  Loads are issued four at
+// a time ahead of the dependent sums.
+__device__ __forceinline__ int list_sample_s(const int* idx, const float* w, int n, float u) {
+  float S = 0.0f;
+  int last = -1;
+  for (int j = 0; j < n; j += 4) {
+    const float4 p4 = *reinterpret_cast<const float4*>(w + j);
+    const int4 i4 = *reinterpret_cast<const int4*>(idx + j);
+    const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
+    const int iv[4] = {i4.x, i4.y, i4.z, i4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (j + e < n && pv[e] > 0.0f) { S = __fadd_rn(S, pv[e]); last = iv[e]; }
+  }
+  if (last < 0) return -1;
+  const float t = __fmul_rn(u, S);
+  float acc = 0.0f;
+  for (int j = 0; j < n; j += 4) {
+    const float4 p4 = *reinterpret_cast<const float4*>(w + j);
+    const int4 i4 = *reinterpret_cast<const int4*>(idx + j);
+    const float pv[4] = {p4.x, p4.y, p4.z, p4.w};
+    const int iv[4] = {i4.x, i4.y, i4.z, i4.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e)
+      if (j + e < n && pv[e] > 0.0f) {
+        acc = __fadd_rn(acc, pv[e]);
+        if (acc > t) return iv[e];
+      }
+  }
+  return last;
+}
+
+// Residual weights max(0, p - q) on the entries of the p list (index order),
+// the lanes in parallel: outside the p list p = 0, so max(0, -q) = 0 adds
+// nothing to the draw.  Warp-wide; r has the p list's capacity.
+__device__ __forceinline__ void residual_weights(const int* pi, const float* pp, int np, const int* qi,
+                                                 const float* qp, int nq, float* r) {
+  const int lane = threadIdx.x & 31;
+  for (int j = lane; j < np; j += 32) {
+    const float d = __fsub_rn(pp[j], list_lookup(qi, qp, nq, pi[j]));
+    r[j] = d > 0.0f ? d : 0.0f;
+  }
+  __syncwarp();
+}
+
 // After codes up to depth s_new are committed: finish the frame or set up
-// the next pass (sampling the drafts from this pass's draft slots).
+// the next pass (the drafts are drawn from this pass's draft slots on row
+// hrow).  Warp-wide; lane 0 owns the scalar state.
 template <typename WT>
 __device__ __noinline__ void after_commit(const FrameParams& P, const CallArgs& ca, int b, AcceptScratch& A,
                                           int s_new, int hrow) {
@@ -1051,7 +1138,7 @@ __device__ __noinline__ void after_commit(const FrameParams& P, const CallArgs& 
   const int frame = S.frame;
   __syncwarp();
   if (s_new >= P.G - 1) {
-    if (lane == 0) { ss->frames += 1; ss->committed += P.G - 1; }
+    if (lane == 0) { bump(ss->frames); bump(ss->committed, P.G - 1); }
     const int nf = frame + 1;
     if (nf < ca.n_frames) setup_frame<WT>(P, ca, b, S, nf);
     else retire_stream(P, b, S);
@@ -1066,23 +1153,19 @@ __device__ __noinline__ void after_commit(const FrameParams& P, const CallArgs& 
   }
   const int R = P.G - 1 - s_new;
   const int n_d = min(P.N - 1, R);
-  const int slots = 1 + P.ND;
   // The draft distributions q_t = proc(head_{s+t} . h_s), t = 1..n_d, are
-  // this pass's speculative draft slots on the row at position s_new: stage
-  // them, sample the drafts, and keep them for the next pass's acceptance.
-  for (int t = 1; t <= n_d; ++t) {
-    const size_t li = (size_t)hrow * slots + t;
-    stage_list_async(P, A, t - 1, P.lidx + li * P.KC, P.lprob + li * P.KC);
+  // this pass's speculative draft slots on the row at position s_new
+  // (already staged with the target lists): draw the drafts (uniforms one
+  // per lane) and keep the lists for the next pass.
+  const int ih = hrow - b * P.NS;  // the row's index within the stream
+  if (lane < n_d) {
+    // draft t = lane + 1, one lane each
+    const float u = philox_uniform(P.seed, (uint32_t)b, (uint32_t)S.frame_abs, (uint32_t)(s_new + 1 + lane), kDraft);
+    const int ds = A.dslot(ih, lane + 1);
+    S.drafts[lane] = valid_code(P, list_sample_s(A.idx + (size_t)ds * P.KC, A.prob + (size_t)ds * P.KC, A.cnt[ds], u));
   }
-  if (lane < n_d) A.cnt[lane] = __ldcg(P.lcount + (size_t)hrow * slots + 1 + lane);
-  cp_async_wait_all();
   __syncwarp();
   if (lane == 0) {
-    for (int t = 1; t <= n_d; ++t) {
-      const float u = philox_uniform(P.seed, (uint32_t)b, (uint32_t)S.frame_abs, (uint32_t)(s_new + t), kDraft);
-      S.drafts[t - 1] = valid_code(P, list_sample(A.idx + (size_t)(t - 1) * P.KC, A.prob + (size_t)(t - 1) * P.KC,
-                                                  A.cnt[t - 1], u));
-    }
     S.s = s_new;
     S.n_d = n_d;
     S.m = min(n_d + 1, R);
@@ -1094,10 +1177,11 @@ __device__ __noinline__ void after_commit(const FrameParams& P, const CallArgs& 
   for (int i = lane; i < n_d * kc4; i += 32) {
     const int t = i / kc4, c = i - t * kc4;
     const size_t qi = ((size_t)b * P.ND + t) * P.KC;
-    reinterpret_cast<int4*>(P.qidx + qi)[c] = reinterpret_cast<const int4*>(A.idx + (size_t)t * P.KC)[c];
-    reinterpret_cast<float4*>(P.qprob + qi)[c] = reinterpret_cast<const float4*>(A.prob + (size_t)t * P.KC)[c];
+    const int ds = A.dslot(ih, t + 1);
+    reinterpret_cast<int4*>(P.qidx + qi)[c] = reinterpret_cast<const int4*>(A.idx + (size_t)ds * P.KC)[c];
+    reinterpret_cast<float4*>(P.qprob + qi)[c] = reinterpret_cast<const float4*>(A.prob + (size_t)ds * P.KC)[c];
   }
-  if (lane < n_d) P.qcount[(size_t)b * P.ND + lane] = A.cnt[lane];
+  if (lane < n_d) P.qcount[(size_t)b * P.ND + lane] = A.cnt[A.dslot(ih, lane + 1)];
   __syncwarp();
   int codes_in[CP_SPEC_MAX_WINDOW];
   const int m = S.m;
@@ -1124,14 +1208,33 @@ __device__ void teacher_copy(const FrameParams& P, const CallArgs& ca, int b, co
   }
 }
 
+// What the acceptance of stream b reads that no kernel of the pass writes:
+// the stream state and, for a speculative round, the draft lists q_t saved
+// by the previous pass (staged asynchronously).  Before the dependency wait.
+__device__ void accept_prefetch(const FrameParams& P, int b, AcceptScratch& A) {
+  StreamState& S = *A.S;
+  const int lane = threadIdx.x & 31;
+  load_state(P, b, S);
+  if (S.phase != kPhaseSpec) return;
+  const int n_d = S.n_d;
+  for (int t = 1; t <= n_d; ++t) {
+    const size_t qi = ((size_t)b * P.ND + t - 1) * P.KC;
+    stage_list_async(P, A, A.qslot(t), P.qidx + qi, P.qprob + qi);
+  }
+  if (lane < n_d) A.cnt[A.qslot(lane + 1)] = __ldcg(P.qcount + (size_t)b * P.ND + lane);
+  __syncwarp();
+}
+
 // The acceptance decision of stream b for the pass that just ran ("Speculative
 // Decoding, Beyond Text", section 02; "CodePredictor Speculative Decoding",
-// "How a round works" step 3), then the next pass's rows.
+// "How a round works" step 3), then the next pass's rows.  Warp-wide, after
+// accept_prefetch and the dependency wait: the target lists are staged in
+// one round trip, the uniforms of the decision are drawn one per lane
+// meanwhile, and lane 0 runs the left-to-right chain.
 template <typename WT>
 __device__ void accept_stream(const FrameParams& P, const CallArgs& ca, int b, AcceptScratch& A) {
   StreamState& S = *A.S;
   const int lane = threadIdx.x & 31;
-  load_state(P, b, S);
   if (S.phase == kPhaseDone) return;
   const int slots = 1 + P.ND;
   StreamStats* ss = P.sstats + b;
@@ -1147,87 +1250,104 @@ __device__ void accept_stream(const FrameParams& P, const CallArgs& ca, int b, A
     store_state(P, b, S);
     return;
   }
-  // Stage the lists this decision reads: the target rows' slot-0 lists
-  // (p_{s+1..s+m}) and, for a speculative round, the saved draft lists q_t.
+  // Stage the lists this decision reads (the saved draft lists q_t of a
+  // speculative round were staged by accept_prefetch).
   const bool spec = S.phase == kPhaseSpec;
-  const int nl = spec ? S.m + S.n_d : 1;
   const int row0 = b * P.NS + (S.phase == kPhasePrefill ? 1 : 0);
-  int cnt = 0;
-  if (spec) {
-    if (lane < S.m) cnt = __ldcg(P.lcount + (size_t)(b * P.NS + lane) * slots);
-    else if (lane < nl) cnt = __ldcg(P.qcount + (size_t)b * P.ND + (lane - S.m));
-    for (int i = 0; i < S.m; ++i) {
-      const size_t li = (size_t)(b * P.NS + i) * slots;
-      stage_list_async(P, A, i, P.lidx + li * P.KC, P.lprob + li * P.KC);
-    }
-    for (int t = 0; t < S.n_d; ++t) {
-      const size_t qi = ((size_t)b * P.ND + t) * P.KC;
-      stage_list_async(P, A, S.m + t, P.qidx + qi, P.qprob + qi);
-    }
-  } else {
-    if (lane == 0) cnt = __ldcg(P.lcount + (size_t)row0 * slots);
-    stage_list_async(P, A, 0, P.lidx + (size_t)row0 * slots * P.KC, P.lprob + (size_t)row0 * slots * P.KC);
+  const int s = S.s, n_d = S.n_d, m = S.m;
+  const uint32_t fr = (uint32_t)S.frame_abs;
+  // the target lists (slot 0) of the rows the decision reads and, when the
+  // next pass drafts, the draft slots of every row the commit can stop at
+  const int ndn = P.N >= 2 ? P.ND : 0;  // draft slots per row
+  const int r_lo = spec ? 0 : row0 - b * P.NS, r_hi = spec ? m : r_lo + 1;
+  for (int i = r_lo; i < r_hi; ++i) {
+    const size_t li = (size_t)(b * P.NS + i) * slots;
+    stage_list_async(P, A, A.tslot(spec ? i : 0), P.lidx + li * P.KC, P.lprob + li * P.KC);
+    for (int t = 1; t <= ndn; ++t)
+      stage_list_async(P, A, A.dslot(i, t), P.lidx + (li + t) * P.KC, P.lprob + (li + t) * P.KC);
   }
-  if (lane < nl) A.cnt[lane] = cnt;
+  for (int k = lane; k < (r_hi - r_lo) * (1 + ndn); k += 32) {
+    const int i = r_lo + k / (1 + ndn), t = k - (k / (1 + ndn)) * (1 + ndn);
+    const int c = __ldcg(P.lcount + (size_t)(b * P.NS + i) * slots + t);
+    A.cnt[t == 0 ? A.tslot(spec ? i : 0) : A.dslot(i, t)] = c;
+  }
+  // uniforms, one per lane, while the lists land: lane t-1 (t = 1..8) the
+  // ACCEPT draw at depth s + t; lane 8 + t - 1 (t = 1..9) the TARGET draw at
+  // depth s + t (residual at a rejection at t, or the bonus at n_d + 1)
+  if (lane < 8 && lane < n_d) A.u[lane] = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + 1 + lane), kAccept);
+  if (lane >= 8 && lane < 17 && lane - 8 <= n_d)
+    A.u[lane] = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + 1 + lane - 8), kTarget);
   cp_async_wait_all();
   __syncwarp();
   const int* Li = A.idx;
   const float* Lp = A.prob;
   const int KC = P.KC;
-  int s_new = 0, hrow = 0;
+  int s_new = 0, hrow = 0, rej = 0;  // rej = 1 + offset of the rejected draft (0: none)
+  if (spec) {
+    // exact left-to-right acceptance: draft t+1 is accepted iff
+    // u_ACCEPT < fl32(p(y) / q(y)); lane t forms that test for draft t+1 and
+    // the first failing draft is the rejection (later ones are not reached)
+    bool fail = false;
+    if (lane < n_d) {
+      const int y = S.drafts[lane];
+      const int qs = A.qslot(lane + 1), ps = A.tslot(lane);  // scratch slots of q_{t} and p_{s+t}
+      const float qy = list_lookup(Li + (size_t)qs * KC, Lp + (size_t)qs * KC, A.cnt[qs], y);
+      const float py = list_lookup(Li + (size_t)ps * KC, Lp + (size_t)ps * KC, A.cnt[ps], y);
+      fail = !(A.u[lane] < __fdiv_rn(py, qy));
+    }
+    const unsigned fails = __ballot_sync(0xffffffffu, fail);
+    rej = fails ? __ffs(fails) : 0;
+    const int reached = rej ? rej : n_d;  // drafts tested
+    const int acc = rej ? rej - 1 : n_d;  // drafts accepted
+    if (lane < reached) bump(ss->drafted[lane + 1]);
+    if (lane < acc) { bump(ss->accepted[lane + 1]); S.codes[s + 1 + lane] = S.drafts[lane]; }
+    __syncwarp();
+  }
   if (lane == 0) {
-    const uint32_t fr = (uint32_t)S.frame_abs;
-    const int s = S.s;
     if (!spec) {
       const int j = s + 1;  // the pass scored c_j
-      const float u = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)j, kTarget);
-      const int c = valid_code(P, list_sample(Li, Lp, A.cnt[0], u));
+      const int c = valid_code(P, list_sample_s(Li, Lp, A.cnt[0], A.u[8]));
       S.codes[j] = c;
       ca.codes_out[((size_t)S.frame * ca.B + b) * P.G + j] = c;
       s_new = j;
       hrow = row0;
-      ss->passes += 1;
-    } else {  // speculative round: exact left-to-right acceptance
-      const int n_d = S.n_d, m = S.m;
-      int t = 1;
-      bool rejected = false;
-      for (; t <= n_d; ++t) {
-        const int y = S.drafts[t - 1];
-        const int qs = m + t - 1, ps = t - 1;  // scratch slots of q_t and p_{s+t}
-        const float qy = list_lookup(Li + (size_t)qs * KC, Lp + (size_t)qs * KC, A.cnt[qs], y);
-        const float py = list_lookup(Li + (size_t)ps * KC, Lp + (size_t)ps * KC, A.cnt[ps], y);
-        const float ratio = __fdiv_rn(py, qy);
-        ss->drafted[t] += 1;
-        const float ua = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + t), kAccept);
-        if (ua < ratio) {
-          S.codes[s + t] = y;
-          ss->accepted[t] += 1;
-          continue;
+      bump(ss->passes);
+    } else {
+      if (rej == 0) {
+        if (m > n_d) {
+          S.codes[s + n_d + 1] =
+              valid_code(P, list_sample_s(Li + (size_t)A.tslot(n_d) * KC, Lp + (size_t)A.tslot(n_d) * KC,
+                                          A.cnt[A.tslot(n_d)], A.u[8 + n_d]));
+          bump(ss->bonus);
+          s_new = s + n_d + 1;
+        } else {
+          s_new = s + n_d;
         }
-        const float ut = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + t), kTarget);
-        int c = residual_sample(Li + (size_t)ps * KC, Lp + (size_t)ps * KC, A.cnt[ps], Li + (size_t)qs * KC,
-                                Lp + (size_t)qs * KC, A.cnt[qs], ut);
-        if (c < 0) c = list_sample(Li + (size_t)ps * KC, Lp + (size_t)ps * KC, A.cnt[ps], ut);
-        S.codes[s + t] = valid_code(P, c);
-        rejected = true;
-        break;
       }
-      if (rejected) {
-        s_new = s + t;
-        ss->rejections += 1;
-      } else if (m > n_d) {
-        const float ut = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + n_d + 1), kTarget);
-        S.codes[s + n_d + 1] =
-            valid_code(P, list_sample(Li + (size_t)n_d * KC, Lp + (size_t)n_d * KC, A.cnt[n_d], ut));
-        ss->bonus += 1;
-        s_new = s + n_d + 1;
-      } else {
-        s_new = s + n_d;
-      }
+      bump(ss->rounds);
+      bump(ss->passes);
+    }
+  }
+  rej = __shfl_sync(0xffffffffu, rej, 0);
+  if (rej > 0) {
+    // draw from norm(max(0, p - q)) at the rejected offset (from p if the
+    // residual is zero everywhere)
+    const int ps = A.tslot(rej - 1), qs = A.qslot(rej);
+    residual_weights(Li + (size_t)ps * KC, Lp + (size_t)ps * KC, A.cnt[ps], Li + (size_t)qs * KC,
+                     Lp + (size_t)qs * KC, A.cnt[qs], A.r);
+    if (lane == 0) {
+      const float ut = A.u[8 + rej - 1];
+      int c = list_sample_s(Li + (size_t)ps * KC, A.r, A.cnt[ps], ut);
+      if (c < 0) c = list_sample_s(Li + (size_t)ps * KC, Lp + (size_t)ps * KC, A.cnt[ps], ut);
+      S.codes[s + rej] = valid_code(P, c);
+      bump(ss->rejections);
+      s_new = s + rej;
+    }
+  }
+  if (lane == 0) {
+    if (spec) {
       for (int j = s + 1; j <= s_new; ++j) ca.codes_out[((size_t)S.frame * ca.B + b) * P.G + j] = S.codes[j];
       hrow = b * P.NS + (s_new - s - 1);
-      ss->rounds += 1;
-      ss->passes += 1;
     }
     if (ca.committed_out) ca.committed_out[b] = s_new + 1;
   }
@@ -1240,7 +1360,7 @@ __device__ void accept_stream(const FrameParams& P, const CallArgs& ca, int b, A
 
 // The rows of the next pass, compacted, and the lm_heads it needs (head_j
 // for j in [pos, pos + ND] of every row at pos >= 1).  One warp.
-__device__ void build_plan(const FrameParams& P, const CallArgs& ca) {
+__device__ int build_plan(const FrameParams& P, const CallArgs& ca) {
   const int lane = threadIdx.x & 31;
   const unsigned lt = (1u << lane) - 1u;
   int n = 0;
@@ -1248,14 +1368,14 @@ __device__ void build_plan(const FrameParams& P, const CallArgs& ca) {
   unsigned long long mask = 0;
   for (int j0 = 0; j0 < total; j0 += 32) {
     const int r = j0 + lane;
-    const int pos = r < total ? __ldcg(P.row_pos + r) : -1;
+    const int pos = r < total ? (g_mirror_on ? g_mpos[r] : __ldcg(P.row_pos + r)) : -1;
     const bool on = pos >= 0;
     const uint32_t bal = __ballot_sync(0xffffffffu, on);
     if (on) {
       const int at = n + __popc(bal & lt);
       P.prow[at] = r;
       P.ppos[at] = pos;
-      P.pcode[at] = __ldcg(P.row_code + r);
+      P.pcode[at] = g_mirror_on ? g_mcode[r] : __ldcg(P.row_code + r);
       if (pos >= 1)
         for (int t = 0; t <= P.ND && pos + t <= P.G - 1; ++t) mask |= 1ull << (pos + t);
     }
@@ -1270,17 +1390,23 @@ __device__ void build_plan(const FrameParams& P, const CallArgs& ca) {
     P.plan->nheads = nh;
     P.plan->nrows = n;
     if (n > 0) {
-      P.ctl->weight_bytes += (long long)P.L * P.layer_bytes + (long long)nh * P.head_bytes;
-      P.ctl->heads_applied += nh;
+      atomicAdd(reinterpret_cast<unsigned long long*>(&P.ctl->weight_bytes),
+                (unsigned long long)((long long)P.L * P.layer_bytes + (long long)nh * P.head_bytes));
+      atomicAdd(reinterpret_cast<unsigned long long*>(&P.ctl->heads_applied), (unsigned long long)nh);
     }
   }
   __syncwarp();
+  return n;
 }
 
 // Last-CTA election: true in the CTA that finishes last; its threads then
 // see every other CTA's writes (each CTA fences before counting itself).
 __device__ __forceinline__ bool last_cta(Control* ctl) {
   __shared__ int s_last;
+  if (gridDim.x == 1) {  // the block's own writes are visible to it after the barrier
+    __syncthreads();
+    return true;
+  }
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_last = atomicAdd(&ctl->done, 1) == (int)gridDim.x - 1;
@@ -1298,12 +1424,13 @@ __device__ __forceinline__ void set_loop(const FrameParams& P, bool go) {
 // Stream setup of a call: frame 0 (decode) or the first teacher chunk; then
 // the first pass's plan.
 template <typename WT>
-__global__ void __launch_bounds__(kThreads, 1) setup_kernel(const __grid_constant__ FrameParams P) {
+__global__ void __launch_bounds__(kThreads, 2) setup_kernel(const __grid_constant__ FrameParams P) {
   extern __shared__ __align__(16) unsigned char ssmem[];
   const CallArgs ca = *P.call;
   const int warp = threadIdx.x >> 5;
   if (blockIdx.x == 0 && threadIdx.x == 0) { P.ctl->active = ca.B; P.ctl->pass = 0; }
-  const int b = blockIdx.x * kWarps + warp;
+  mirror_init(P, ca);
+  const int b = blockIdx.x * (blockDim.x >> 5) + warp;
   if (b < ca.B) {
     AcceptScratch A = accept_scratch(P, ssmem);
     StreamState& S = *A.S;
@@ -1318,39 +1445,45 @@ __global__ void __launch_bounds__(kThreads, 1) setup_kernel(const __grid_constan
     store_state(P, b, S);
   }
   if (!last_cta(P.ctl)) return;
-  if (warp == 0) build_plan(P, ca);
+  int nrows = 0;
+  if (warp == 0) nrows = build_plan(P, ca);
   if (threadIdx.x == 0) {
-    P.ctl->done = 0;
-    set_loop(P, __ldcg(&P.plan->nrows) > 0);
+    if (gridDim.x > 1) P.ctl->done = 0;
+    set_loop(P, nrows > 0);
   }
 }
 
 // Acceptance of every stream (warp per stream), then the next pass's plan
 // and the loop condition.
 template <typename WT>
-__global__ void __launch_bounds__(kThreads, 1) accept_kernel(const __grid_constant__ FrameParams P) {
+__global__ void __launch_bounds__(kThreads, 2) accept_kernel(const __grid_constant__ FrameParams P) {
   extern __shared__ __align__(16) unsigned char ssmem[];
-  pdl_wait();
   const CallArgs ca = *P.call;
   const int warp = threadIdx.x >> 5;
-  const int b = blockIdx.x * kWarps + warp;
-  if (b < ca.B) {
-    AcceptScratch A = accept_scratch(P, ssmem);
-    accept_stream<WT>(P, ca, b, A);
-  }
+  const int b = blockIdx.x * (blockDim.x >> 5) + warp;
+  // loop bookkeeping words, fetched early (CTA 0 is not necessarily the last)
+  int pass0 = 0, status0 = 0;
+  if (threadIdx.x == 0) { pass0 = __ldcg(&P.ctl->pass); status0 = __ldcg(&P.ctl->status); }
+  mirror_init(P, ca);
+  AcceptScratch A = accept_scratch(P, ssmem);
+  if (b < ca.B) accept_prefetch(P, b, A);
+  pdl_wait();
+  if (b < ca.B) accept_stream<WT>(P, ca, b, A);
   if (!last_cta(P.ctl)) return;
-  if (warp == 0) build_plan(P, ca);
+  int nrows = 0;
+  if (warp == 0) nrows = build_plan(P, ca);
   if (threadIdx.x == 0) {
     Control* ctl = P.ctl;
-    ctl->done = 0;
-    ctl->passes += 1;
-    ctl->kernels += P.kernels_per_pass;
-    const int pass = ctl->pass + 1;
+    if (gridDim.x > 1) { ctl->done = 0; pass0 = __ldcg(&ctl->pass); status0 = __ldcg(&ctl->status); }
+    atomicAdd(reinterpret_cast<unsigned long long*>(&ctl->passes), 1ull);
+    atomicAdd(reinterpret_cast<unsigned long long*>(&ctl->kernels), (unsigned long long)P.kernels_per_pass);
+    const int pass = pass0 + 1;
     ctl->pass = pass;
-    const bool more = __ldcg(&ctl->active) > 0 && __ldcg(&P.plan->nrows) > 0;
+    // every unfinished stream has rows in the next pass
+    const bool more = nrows > 0;
     const bool capped = pass >= ca.pass_cap;
     if (more && capped && ca.max_passes == 0) raise_status(&ctl->status, kStatusDevice);
-    set_loop(P, more && !capped && __ldcg(&ctl->status) == 0);
+    set_loop(P, more && !capped && status0 == 0);
   }
 }
 
