@@ -95,6 +95,7 @@ struct FrameParams {
   int KC;   // list capacity = min(max top_k, V) rounded up to a multiple of 4
   int Bmax; // stream capacity of the workspace (row slots = Bmax * NS)
   int kernels_per_pass;
+  int tc;   // bf16 GEMVs on the tensor-core path (contexts with many rows per pass)
   unsigned long long seed;
   unsigned long long cond;            // graph conditional handle of the pass loop (0 = none)
   long long layer_bytes, head_bytes;  // algorithmic bytes per layer / per lm_head

@@ -375,18 +375,6 @@ __device__ __forceinline__ bool gemv_run(const FrameParams& P, const CallArgs& c
   const size_t row_bytes = (size_t)G.nch * 16;
   if (tid < 32 * nqv && lane == 0) sh.src[warp] = act_row<WT>(P, ca, pr, KIND, l, q0 + warp);
   __syncthreads();
-  // gains of this thread's chunks, fetched with the inputs
-  float4 gv[CPT][EPC / 4];
-  if (gain != nullptr) {
-#pragma unroll
-    for (int j = 0; j < CPT; ++j) {
-      const int c = tl + j * G.TPG;
-#pragma unroll
-      for (int i = 0; i < EPC; i += 4)
-        gv[j][i / 4] = (active && c < G.nch) ? *reinterpret_cast<const float4*>(gain + c * EPC + i)
-                                             : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-  }
   float2 av[CPT][NQ][PPC];
 #pragma unroll
   for (int j = 0; j < CPT; ++j) {
@@ -432,7 +420,7 @@ __device__ __forceinline__ bool gemv_run(const FrameParams& P, const CallArgs& c
       if (!active || c >= G.nch) continue;
 #pragma unroll
       for (int i = 0; i < EPC; i += 4) {
-        const float4 gg = gv[j][i / 4];
+        const float4 gg = *reinterpret_cast<const float4*>(gain + c * EPC + i);  // shared memory
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
           float2& a0 = av[j][q][i / 2];
@@ -545,6 +533,187 @@ __device__ __forceinline__ bool gemv_run(const FrameParams& P, const CallArgs& c
   return true;
 }
 
+
+// --------------------------------------------------- tensor-core GEMV path
+// For contexts with many rows per pass (many streams), the bf16 GEMVs are
+// small GEMMs: mma.sync m16n8k16 (bf16 x bf16 -> f32) with the weight tile
+// in shared memory as the column-major B operand and the input rows as A.
+// The fp32 inputs are split into bf16 hi + lo parts (two MMAs per step), so
+// an input keeps 16 mantissa bits.  Within each 32-element block of K a
+// fixed permutation gives every lane 16 contiguous bytes of a weight row and
+// two float4 of an input row per two k-steps (the same permutation on A and
+// B, so the dot product is unchanged).  Every output element is one warp's
+// MMA chain over K in order: its value does not depend on the other rows
+// of the pass.
+
+__device__ __forceinline__ void mma_bf16_16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// (x0, x1) -> bf16x2 hi and bf16x2 lo with x ~ hi + lo (low half = x0).
+__device__ __forceinline__ void split_bf16x2(float x0, float x1, uint32_t& hi, uint32_t& lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 o = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  hi = *reinterpret_cast<const uint32_t*>(&h);
+  lo = *reinterpret_cast<const uint32_t*>(&o);
+}
+
+// Eight input values k0 .. k0 + 7 of a row (fp32 row or bf16 embedding row).
+__device__ __forceinline__ void load_act8(const ActRow& a, int k0, float (&v)[8]) {
+  if (a.f != nullptr) {
+    const float4 x0 = __ldcg(reinterpret_cast<const float4*>(a.f + k0));
+    const float4 x1 = __ldcg(reinterpret_cast<const float4*>(a.f + k0 + 4));
+    v[0] = x0.x; v[1] = x0.y; v[2] = x0.z; v[3] = x0.w; v[4] = x1.x; v[5] = x1.y; v[6] = x1.z; v[7] = x1.w;
+  } else {
+    float2 w[4];
+    WTraits<__nv_bfloat16>::cvt(__ldg(reinterpret_cast<const uint4*>(static_cast<const __nv_bfloat16*>(a.w) + k0)), w);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) { v[2 * p] = w[p].x; v[2 * p + 1] = w[p].y; }
+  }
+}
+
+constexpr int kTcMaxN = 4;  // n-tiles of 8 weight rows per tile (tiles hold at most 32 rows on this path)
+// per-warp output blocks (16 rows x 32 columns) and 16 row descriptors
+constexpr int kTcYFloats = kWarps * 16 * kTcMaxN * 8 + kWarps * 16 * (int)(sizeof(ActRow) / sizeof(float));
+
+// One tile (R weight rows, K inputs) against pass rows [m0, m0 + 16) by one
+// warp: the MMA chain over K, then the outputs of the tile's units for those
+// rows.  src/inv: the warp's 16 input rows (rows past nrows repeat the last).
+template <int KIND, int NT>
+__device__ __forceinline__ void tc_block(const FrameParams& P, int l, const int* heads, const PassRows& pr,
+                                         const float2* rope, const unsigned char* tile, Tile tl, int R, int K,
+                                         const ActRow* src, const float* inv, const float* gain, int m0, int nrows,
+                                         float* y) {
+  // inv: RMSNorm scales of all pass rows (null when not normed)
+  const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const size_t row_bytes = (size_t)K * 2;
+  float c[NT][4];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
+  const ActRow ra = src[g], rb = src[g + 8];
+  const float ia = inv ? inv[min(m0 + g, nrows - 1)] : 1.0f, ib = inv ? inv[min(m0 + g + 8, nrows - 1)] : 1.0f;
+  const unsigned char* wr[NT];
+#pragma unroll
+  for (int j = 0; j < NT; ++j) wr[j] = tile + (size_t)min(8 * j + g, R - 1) * row_bytes + (size_t)t * 16;
+  for (int kb = 0; kb < K; kb += 32) {
+    const int k0 = kb + 8 * t;
+    float va[8], vb[8];
+    load_act8(ra, k0, va);
+    load_act8(rb, k0, vb);
+    if (gain != nullptr) {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float gk = gain[k0 + e];
+        va[e] = va[e] * ia * gk;
+        vb[e] = vb[e] * ib * gk;
+      }
+    }
+    uint32_t ah[2][4], al[2][4];
+#pragma unroll
+    for (int s = 0; s < 2; ++s) {
+      split_bf16x2(va[4 * s + 0], va[4 * s + 1], ah[s][0], al[s][0]);
+      split_bf16x2(vb[4 * s + 0], vb[4 * s + 1], ah[s][1], al[s][1]);
+      split_bf16x2(va[4 * s + 2], va[4 * s + 3], ah[s][2], al[s][2]);
+      split_bf16x2(vb[4 * s + 2], vb[4 * s + 3], ah[s][3], al[s][3]);
+    }
+#pragma unroll
+    for (int j = 0; j < NT; ++j) {
+      const uint4 w = *reinterpret_cast<const uint4*>(wr[j] + (size_t)kb * 2);
+      mma_bf16_16816(c[j], ah[0][0], ah[0][1], ah[0][2], ah[0][3], w.x, w.y);
+      mma_bf16_16816(c[j], al[0][0], al[0][1], al[0][2], al[0][3], w.x, w.y);
+      mma_bf16_16816(c[j], ah[1][0], ah[1][1], ah[1][2], ah[1][3], w.z, w.w);
+      mma_bf16_16816(c[j], al[1][0], al[1][1], al[1][2], al[1][3], w.z, w.w);
+    }
+  }
+  // C fragment: c[j][0..1] = rows g, cols 8j + 2t, +1; c[j][2..3] = row g + 8
+  const int W = NT * 8;
+#pragma unroll
+  for (int j = 0; j < NT; ++j) {
+    y[g * W + 8 * j + 2 * t] = c[j][0];
+    y[g * W + 8 * j + 2 * t + 1] = c[j][1];
+    y[(g + 8) * W + 8 * j + 2 * t] = c[j][2];
+    y[(g + 8) * W + 8 * j + 2 * t + 1] = c[j][3];
+  }
+  __syncwarp();
+  const int rows = min(16, nrows - m0);
+  const int rpu = rows_per_unit(KIND);
+  for (int it = lane; it < tl.n * rows; it += 32) {
+    const int i = it / rows, q = it - i * rows;
+    const float y0 = y[q * W + i], y1 = rpu == 2 ? y[q * W + i + tl.n] : 0.0f;
+    float ho = 0.0f;
+    if (KIND == kO || KIND == kDown) ho = __ldcg(P.h + (size_t)pr.prow[m0 + q] * P.H + tl.u0 + i);
+    gemv_out<KIND>(P, l, heads, pr, rope, tl.u0 + i, m0 + q, y0, y1, ho);
+  }
+  __syncwarp();
+}
+
+// The tensor-core GEMV of one kind for all rows of the pass (bf16 weights):
+// per tile, warp w takes row blocks w, w + kWarps, ... of 16 rows.
+template <int KIND>
+__device__ __forceinline__ bool gemv_tc(const FrameParams& P, const CallArgs& ca, int l, GemvShared& sh, const PassRows& pr,
+                        const float2* rope, unsigned char* slots, float* ybuf, float* s_inv, int nrows,
+                        const float* gain) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int K = gemv_K(P, KIND);
+  const int rpu = rows_per_unit(KIND);
+  // RMSNorm scales of every row, one warp per row
+  if (gain != nullptr)
+    for (int i = warp; i < nrows; i += kWarps) {
+      const ActRow a = act_row<__nv_bfloat16>(P, ca, pr, KIND, l, i);
+      float ss = 0.0f;
+      for (int k = 8 * lane; k < K; k += 256) {
+        float v[8];
+        load_act8(a, k, v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
+      }
+      ss = warp_sum(ss);
+      if (lane == 0) s_inv[i] = 1.0f / sqrtf(ss / (float)K + P.eps);
+    }
+  __syncthreads();
+  float* y = ybuf + (size_t)warp * 16 * (kTcMaxN * 8);
+  ActRow* src = reinterpret_cast<ActRow*>(ybuf + (size_t)kWarps * 16 * (kTcMaxN * 8)) + warp * 16;  // 16 row descriptors per warp
+  const int nblk = (nrows + 15) / 16;
+  bool ok = true;
+  for (int t = 0; t < sh.ntiles; ++t) {
+    const int slot = t & 1;
+    const Tile tl = sh.tiles[t];
+    const int R = tl.n * rpu;
+    if (!mbar_wait_bounded(&sh.full[slot], (uint32_t)(t >> 1) & 1u, &P.ctl->status, kTileTimeoutNs)) ok = false;
+    if (ok) {
+      const unsigned char* tp = slots + (size_t)slot * kSlotBytes;
+      for (int mb = warp; mb < nblk; mb += kWarps) {
+        const int m0 = mb * 16;
+        if (lane < 16) src[lane] = act_row<__nv_bfloat16>(P, ca, pr, KIND, l, min(m0 + lane, nrows - 1));
+        __syncwarp();
+        const float* inv = gain ? s_inv : nullptr;
+        const int nt = (R + 7) / 8;
+        if (nt <= 1) tc_block<KIND, 1>(P, l, sh.heads, pr, rope, tp, tl, R, K, src, inv, gain, m0, nrows, y);
+        else if (nt == 2) tc_block<KIND, 2>(P, l, sh.heads, pr, rope, tp, tl, R, K, src, inv, gain, m0, nrows, y);
+        else if (nt == 3) tc_block<KIND, 3>(P, l, sh.heads, pr, rope, tp, tl, R, K, src, inv, gain, m0, nrows, y);
+        else tc_block<KIND, 4>(P, l, sh.heads, pr, rope, tp, tl, R, K, src, inv, gain, m0, nrows, y);
+      }
+    }
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    if (!ok) return false;
+    if (threadIdx.x == 0 && t + 2 < sh.ntiles) gemv_issue<__nv_bfloat16, KIND>(P, l, sh, slots, t + 2);
+  }
+  return true;
+}
+
+template <typename WT, int KIND>
+__device__ __forceinline__ bool gemv_tc_any(const FrameParams& P, const CallArgs& ca, int l, GemvShared& sh,
+                                            const PassRows& pr, const float2* rope, unsigned char* slots, float* ybuf,
+                                            float* s_inv, int nrows, const float* gain) {
+  if constexpr (WTraits<WT>::EB == 2) return gemv_tc<KIND>(P, ca, l, sh, pr, rope, slots, ybuf, s_inv, nrows, gain);
+  return false;  // fp32 weights never take the tensor path
+}
+
 // Input rows per group for a geometry (2 when a thread owns 3 chunks, to
 // bound registers).
 __device__ __forceinline__ int group_rows(const RowGeom& G) { return G.CPT >= 3 ? 2 : 4; }
@@ -577,7 +746,7 @@ __device__ __forceinline__ bool gemv_dispatch(const FrameParams& P, const CallAr
 // dependency wait.  With one input group (up to 4 rows) or at most two
 // tiles, each group's inputs are loaded once and every tile streams through
 // them; otherwise tile by tile, group by group.
-template <typename WT, int KIND>
+template <typename WT, int KIND, bool TC>
 __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ FrameParams P, int l) {
   extern __shared__ __align__(128) unsigned char smem[];
   pdl_launch_dependents();
@@ -589,7 +758,8 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
   const RowGeom G = row_geom(K * EB / 16);
   const int rpu = rows_per_unit(KIND);
   const size_t row_bytes = (size_t)G.nch * 16;
-  const int upt = max(1, min((int)(kSlotBytes / (rpu * row_bytes)), kMaxTileRows / rpu));
+  int upt = max(1, min((int)(kSlotBytes / (rpu * row_bytes)), kMaxTileRows / rpu));
+  if (TC) upt = max(1, min(upt, kTcMaxN * 8 / rpu));  // tensor path: at most 32 rows per tile
   const int rows_cap = P.Bmax * P.NS;
   unsigned char* slots = smem;
   float* red = reinterpret_cast<float*>(smem + 2 * (size_t)kSlotBytes);
@@ -598,8 +768,12 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
   const size_t rope_n = (size_t)P.G * (P.d / 2);
   const bool rope_in_smem = KIND == kQKV && rope_n * sizeof(float2) <= (size_t)kRopeSmemBytes;
   float2* s_rope = reinterpret_cast<float2*>(s_rows + (3 * rows_cap + 3) / 4 * 4);  // 16-byte aligned
-  // RMSNorm gain (a weight) in shared memory after the RoPE table
+  // RMSNorm gain (a weight) in shared memory after the RoPE table; then, on
+  // the tensor path, the per-warp output blocks and row descriptors and the
+  // rows' RMSNorm scales
   float* s_gain = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(s_rope) + kRopeSmemBytes);
+  float* s_tcy = s_gain + (P.H + 3) / 4 * 4;
+  float* s_tcinv = s_tcy + kTcYFloats;
   const float* gain_g = KIND == kQKV ? P.attn_norm[l] : (KIND == kGU ? P.ffn_norm[l] : (KIND == kHeads ? P.final_norm : nullptr));
   // Before the dependency wait: everything that does not come from the
   // previous kernels of the pass (weight tiles, call arguments, the pass
@@ -653,7 +827,9 @@ __global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant
   const int NQG = group_rows(G);
   const int ngroups = (nrows + NQG - 1) / NQG;
   bool ok = true;
-  if (ngroups <= 1 || ntiles <= 2) {
+  if constexpr (TC) {
+    if (nrows > 0) ok = gemv_tc_any<WT, KIND>(P, ca, l, sh, pr, rope, slots, s_tcy, s_tcinv, nrows, gain);
+  } else if (ngroups <= 1 || ntiles <= 2) {
     for (int gq = 0; gq < ngroups && ok; ++gq)
       ok = gemv_dispatch<WT, KIND>(P, ca, l, G, sh, pr, rope, slots, red, gq * NQG, min(NQG, nrows - gq * NQG), 0,
                                    ntiles, gq == ngroups - 1, gain);
@@ -1512,21 +1688,24 @@ using cpk::FrameParams;
 
 template <typename WT>
 struct KernelSet {
-  static const void* gemv(int kind) {
+  template <bool TC>
+  static const void* gemv_t(int kind) {
     switch (kind) {
-      case cpk::kQKV: return (const void*)cpk::gemv_kernel<WT, cpk::kQKV>;
-      case cpk::kO: return (const void*)cpk::gemv_kernel<WT, cpk::kO>;
-      case cpk::kGU: return (const void*)cpk::gemv_kernel<WT, cpk::kGU>;
-      case cpk::kDown: return (const void*)cpk::gemv_kernel<WT, cpk::kDown>;
-      default: return (const void*)cpk::gemv_kernel<WT, cpk::kHeads>;
+      case cpk::kQKV: return (const void*)cpk::gemv_kernel<WT, cpk::kQKV, TC>;
+      case cpk::kO: return (const void*)cpk::gemv_kernel<WT, cpk::kO, TC>;
+      case cpk::kGU: return (const void*)cpk::gemv_kernel<WT, cpk::kGU, TC>;
+      case cpk::kDown: return (const void*)cpk::gemv_kernel<WT, cpk::kDown, TC>;
+      default: return (const void*)cpk::gemv_kernel<WT, cpk::kHeads, TC>;
     }
   }
+  static const void* gemv(int kind, bool tc) { return tc ? gemv_t<true>(kind) : gemv_t<false>(kind); }
   static const void* setup() { return (const void*)cpk::setup_kernel<WT>; }
   static const void* accept() { return (const void*)cpk::accept_kernel<WT>; }
 };
 
-const void* gemv_fn(int dtype, int kind) {
-  return dtype == 1 ? KernelSet<__nv_bfloat16>::gemv(kind) : KernelSet<float>::gemv(kind);
+// The tensor path exists for bf16 weights only (the host never sets tc for fp32).
+const void* gemv_fn(int dtype, int kind, bool tc = false) {
+  return dtype == 1 ? KernelSet<__nv_bfloat16>::gemv(kind, tc) : KernelSet<float>::gemv(kind, false);
 }
 const void* setup_fn(int dtype) { return dtype == 1 ? KernelSet<__nv_bfloat16>::setup() : KernelSet<float>::setup(); }
 const void* accept_fn(int dtype) { return dtype == 1 ? KernelSet<__nv_bfloat16>::accept() : KernelSet<float>::accept(); }
@@ -1538,6 +1717,9 @@ size_t gemv_smem(const FrameParams& P, int kind) {
   // per kind so that consecutive kernels' CTAs fit on one SM together.
   size_t b = 2 * (size_t)cpk::kSlotBytes + cpk::kRedFloats * sizeof(float) +
              ((3 * (size_t)P.Bmax * P.NS + 3) / 4 * 4) * sizeof(int);
+  if (P.tc)  // every region, then the tensor path's output blocks and the rows' RMSNorm scales
+    return b + cpk::kRopeSmemBytes + (size_t)(P.H + 3) / 4 * 4 * sizeof(float) + cpk::kTcYFloats * sizeof(float) +
+           (size_t)P.Bmax * P.NS * sizeof(float);
   if (kind == cpk::kQKV || kind == cpk::kGU || kind == cpk::kHeads) b += cpk::kRopeSmemBytes + (size_t)P.H * sizeof(float);
   return b;
 }
@@ -1554,9 +1736,9 @@ cudaError_t configure_kernels(const FrameParams& P, int accept_warps) {
   // SM configuration never changes between consecutive kernels and a
   // dependent's CTA can start beside its predecessor's
   for (int k = cpk::kQKV; k <= cpk::kHeads && e == cudaSuccess; ++k) {
-    e = cudaFuncSetAttribute(gemv_fn(P.dtype, k), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemv_smem(P, k));
+    e = cudaFuncSetAttribute(gemv_fn(P.dtype, k, P.tc != 0), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemv_smem(P, k));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemv_fn(P.dtype, k), cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+      e = cudaFuncSetAttribute(gemv_fn(P.dtype, k, P.tc != 0), cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   }
   const void* others[] = {(const void*)cpk::attention_kernel, (const void*)cpk::topk_kernel, setup_fn(P.dtype),
                           accept_fn(P.dtype)};
@@ -1608,17 +1790,17 @@ cudaError_t enqueue_pass(const FrameParams& P, int sms, int accept_warps, cudaSt
   void* pargs[] = {const_cast<FrameParams*>(&P)};
   const int rows = P.Bmax * P.NS;
   for (l = 0; l < P.L && e == cudaSuccess; ++l) {
-    e = launch(gemv_fn(P.dtype, cpk::kQKV), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kQKV), s, !first, gargs);
+    e = launch(gemv_fn(P.dtype, cpk::kQKV, P.tc != 0), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kQKV), s, !first, gargs);
     first = false;
     if (e == cudaSuccess)
       e = launch((const void*)cpk::attention_kernel, dim3(rows * P.nq), dim3(cpk::kThreads), attention_smem(P), s, true,
                  gargs);
-    if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kO), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kO), s, true, gargs);
-    if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kGU), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kGU), s, true, gargs);
-    if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kDown), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kDown), s, true, gargs);
+    if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kO, P.tc != 0), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kO), s, true, gargs);
+    if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kGU, P.tc != 0), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kGU), s, true, gargs);
+    if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kDown, P.tc != 0), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kDown), s, true, gargs);
   }
   l = 0;
-  if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kHeads), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kHeads), s, true, gargs);
+  if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kHeads, P.tc != 0), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kHeads), s, true, gargs);
   if (e == cudaSuccess)
     e = launch((const void*)cpk::topk_kernel, dim3(rows * (1 + P.ND)), dim3(cpk::kThreads), topk_smem(P), s, true, pargs);
   if (e == cudaSuccess) {

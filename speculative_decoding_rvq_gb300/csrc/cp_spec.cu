@@ -143,6 +143,7 @@ cp_spec_status check_weights(const cp_spec_model* model, const cp_spec_weights* 
 constexpr size_t kSmemPerSm = 227 * 1024;
 constexpr int kMaxChunksPerRow = 3 * cpk::kThreads;  // a GEMV thread owns at most 3 chunks of a row
 constexpr int kRedFloatsHost = 1280;                 // the GEMV kernel's partial-sum buffer (floats)
+constexpr int kTcMinRows = 32;                       // rows per pass (max_streams x row slots) that select the tensor path
 
 cp_spec_status check_shapes(const cp_spec_model* m, int N, int KC) {
   const size_t eb = m->dtype == 1 ? 2 : 4;
@@ -213,6 +214,11 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
   P.N = N; P.NS = NS; P.ND = N > 1 ? N - 1 : 0; P.KC = dp.KC;
   P.Bmax = config->max_streams;
   P.kernels_per_pass = 5 * L + 3;
+  // bf16 contexts with many rows per pass run the GEMVs on tensor cores
+  // (every GEMV width a multiple of 32); the choice depends on the context,
+  // not on the pass, so a stream's results do not depend on its batch-mates
+  P.tc = (model->dtype == 1 && config->max_streams * NS >= kTcMinRows && model->hidden % 32 == 0 &&
+          model->ffn % 32 == 0 && (model->n_q_heads * model->head_dim) % 32 == 0) ? 1 : 0;
   P.seed = config->seed;
   P.cond = 0;
   const long long eb = model->dtype == 1 ? 2 : 4;
