@@ -253,6 +253,7 @@ def run_gpu(args, rank, world):
         result["sweep"] = sweep(cp_factory=lambda n: binding.CpSpec(spec, dw, n, TOP_K, TEMP, SEED, 1),
                                 xd=xd[:200], cd=cd[:200], G=spec.num_code_groups, peak=peak)
         result["accept_microbench"] = accept_microbench(peak)
+        result["batched"] = batched(spec, dw, peak)
     return result
 
 
@@ -282,6 +283,43 @@ def sweep(cp_factory, xd, cd, G, peak):
                         "us_per_pass": round(ms * 1e3 / passes, 2),
                         "hbm_frac": round((st["weight_bytes"] + st["kv_bytes"]) / reps / (ms / 1e3) / 1e9 / peak, 4)}
         cp.close()
+    return out
+
+
+def batched(spec, dw, peak, streams=64, frames=100):
+    """The batched configuration: `streams` concurrent streams (ragged accept counts and KV
+    lengths arise on their own), N=4, half the streams greedy and half top-k 50 / T 0.9,
+    `frames` frames each.  max_streams = streams, so the GEMV kernels take the tensor-core
+    path (bf16, many rows per pass)."""
+    import numpy as np
+    import torch
+    from speculative_decoding_rvq_gb300 import binding, synth as S
+    G = spec.num_code_groups
+    x, c0 = S.gen_frames(spec, streams, frames, seed=3)
+    xd, cd = torch.from_numpy(x).cuda(), torch.from_numpy(c0).cuda()
+    cp = binding.CpSpec(spec, dw, 4, TOP_K, TEMP, SEED, streams)
+    tk = np.full(streams, TOP_K, np.int32)
+    tt = np.full(streams, TEMP, np.float32)
+    tt[: streams // 2] = 0.0
+    cp.set_stream_sampling(tk, tt)
+    codes = torch.empty((frames, streams, G), dtype=torch.int32, device="cuda")
+    cp.decode_frames(xd, cd, codes)
+    torch.cuda.synchronize()
+    cp.reset_stats()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    cp.decode_frames(xd, cd, codes)
+    b.record()
+    torch.cuda.synchronize()
+    cp.status()
+    ms = a.elapsed_time(b)
+    st = cp.stats()
+    out = {"streams": streams, "frames": frames, "verify_window": 4, "greedy_streams": streams // 2,
+           "codes_per_s": round(streams * frames * (G - 1) / (ms / 1e3), 1),
+           "passes": st["passes"], "us_per_pass": round(ms * 1e3 / st["passes"], 2),
+           "hbm_frac": round((st["weight_bytes"] + st["kv_bytes"]) / (ms / 1e3) / 1e9 / peak, 4),
+           "gemv_path": "tensor cores (mma.sync bf16, inputs split hi/lo)"}
+    cp.close()
     return out
 
 
@@ -368,18 +406,20 @@ def run_reference(args, rank, world):
 
 
 def profile_rounds(args):
-    """Profiling case for ncu: the default workload's model, one stream, `args.profile_rounds`
+    """Profiling case for ncu: the default workload's model, `args.profile_streams` streams,
+    `args.profile_rounds`
     decoder passes through the step-wise API (cp_spec_round launches the pass kernels
     directly, so a profiler sees each kernel launch; inside the call graph the pass
     kernels run under a device-side loop).  Prints one status line."""
     import torch
     from speculative_decoding_rvq_gb300 import binding, synth as S
     spec = S.TTS06B_BF16
+    B = args.profile_streams
     dw = binding.weights_to_device(spec, S.gen_weights(spec, 0))
-    x, c0 = S.gen_frames(spec, 1, 8, seed=1)
+    x, c0 = S.gen_frames(spec, B, 8, seed=1)
     xd, cd = torch.from_numpy(x).cuda(), torch.from_numpy(c0).cuda()
-    cp = binding.CpSpec(spec, dw, args.window, TOP_K, TEMP, SEED, 1)
-    codes = torch.zeros((1, spec.num_code_groups), dtype=torch.int32, device="cuda")
+    cp = binding.CpSpec(spec, dw, args.window, TOP_K, TEMP, SEED, B)
+    codes = torch.zeros((B, spec.num_code_groups), dtype=torch.int32, device="cuda")
     done, f = 0, 0
     while done < args.profile_rounds:
         cp.begin_frame(xd[f].clone(), cd[f].clone(), f)
@@ -408,6 +448,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-rounds", type=int, default=0,
                     help="run this many step-wise passes (direct kernel launches, for a profiler) and exit")
+    ap.add_argument("--profile-streams", type=int, default=1, help="streams of the --profile-rounds case")
     args = ap.parse_args()
     if args.profile_rounds > 0:
         profile_rounds(args)

@@ -578,6 +578,7 @@ __device__ __forceinline__ void load_act8(const ActRow& a, int k0, float (&v)[8]
 }
 
 constexpr int kTcMaxN = 4;  // n-tiles of 8 weight rows per tile (tiles hold at most 32 rows on this path)
+constexpr int kTcPipe = 2;  // K blocks of 32 whose inputs are loaded ahead
 // per-warp output blocks (16 rows x 32 columns) and 16 row descriptors
 constexpr int kTcYFloats = kWarps * 16 * kTcMaxN * 8 + kWarps * 16 * (int)(sizeof(ActRow) / sizeof(float));
 
@@ -600,11 +601,25 @@ __device__ __forceinline__ void tc_block(const FrameParams& P, int l, const int*
   const unsigned char* wr[NT];
 #pragma unroll
   for (int j = 0; j < NT; ++j) wr[j] = tile + (size_t)min(8 * j + g, R - 1) * row_bytes + (size_t)t * 16;
-  for (int kb = 0; kb < K; kb += 32) {
+  // K in blocks of 32; the inputs of kTcPipe blocks are loaded before any of
+  // them is used, so that many L2 reads are in flight per warp
+  for (int kb0 = 0; kb0 < K; kb0 += 32 * kTcPipe) {
+  float pa[kTcPipe][8], pb[kTcPipe][8];
+#pragma unroll
+  for (int u = 0; u < kTcPipe; ++u) {
+    const int kb = kb0 + 32 * u;
+    if (kb < K) {
+      load_act8(ra, kb + 8 * t, pa[u]);
+      load_act8(rb, kb + 8 * t, pb[u]);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kTcPipe; ++u) {
+    const int kb = kb0 + 32 * u;
+    if (kb >= K) break;
     const int k0 = kb + 8 * t;
-    float va[8], vb[8];
-    load_act8(ra, k0, va);
-    load_act8(rb, k0, vb);
+    float (&va)[8] = pa[u];
+    float (&vb)[8] = pb[u];
     if (gain != nullptr) {
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -629,6 +644,7 @@ __device__ __forceinline__ void tc_block(const FrameParams& P, int l, const int*
       mma_bf16_16816(c[j], ah[1][0], ah[1][1], ah[1][2], ah[1][3], w.z, w.w);
       mma_bf16_16816(c[j], al[1][0], al[1][1], al[1][2], al[1][3], w.z, w.w);
     }
+  }
   }
   // C fragment: c[j][0..1] = rows g, cols 8j + 2t, +1; c[j][2..3] = row g + 8
   const int W = NT * 8;
@@ -747,7 +763,7 @@ __device__ __forceinline__ bool gemv_dispatch(const FrameParams& P, const CallAr
 // tiles, each group's inputs are loaded once and every tile streams through
 // them; otherwise tile by tile, group by group.
 template <typename WT, int KIND, bool TC>
-__global__ void __launch_bounds__(kThreads, 2) gemv_kernel(const __grid_constant__ FrameParams P, int l) {
+__global__ void __launch_bounds__(kThreads, TC ? 1 : 2) gemv_kernel(const __grid_constant__ FrameParams P, int l) {
   extern __shared__ __align__(128) unsigned char smem[];
   pdl_launch_dependents();
   __shared__ GemvShared sh;
