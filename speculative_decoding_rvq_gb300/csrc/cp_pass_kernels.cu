@@ -100,7 +100,8 @@ struct Tile {
   int u0, n;  // first output unit and unit count
 };
 constexpr int kMaxTiles = 96;
-constexpr int kRedFloats = 1280;       // GEMV partial sums of two tiles: rows x 4 input rows x warps per row group, per tile
+constexpr int kRedQ = 8;               // input rows per group at most (partial-sum row stride)
+constexpr int kRedFloats = 1536;       // GEMV partial sums of two tiles: rows x kRedQ x warps per row group, per tile
 constexpr int kRopeSmemBytes = 8192;   // RoPE table copied to shared memory up to this size
 constexpr uint64_t kTileTimeoutNs = 2ull * 1000ull * 1000ull * 1000ull;  // a bulk copy that has not landed in 2 s failed
 
@@ -329,8 +330,8 @@ struct GemvShared {
   int ntiles;
   int heads[kMaxHeadsPerPass];
   int issued;                 // tiles whose copies were issued
-  ActRow src[4];
-  float ss[kWarps][4];        // RMSNorm partial sums of squares per warp
+  ActRow src[kRedQ];
+  float ss[kWarps][kRedQ];    // RMSNorm partial sums of squares per warp
 };
 
 // Issue the bulk copies of tile t into slot t & 1 (thread 0).
@@ -366,6 +367,7 @@ __device__ __forceinline__ bool gemv_run(const FrameParams& P, const CallArgs& c
   using Raw = typename WTraits<WT>::Raw;
   constexpr int EPC = WTraits<WT>::EPC, PPC = EPC / 2;
   constexpr int EB = WTraits<WT>::EB;
+  constexpr int KRB = NQ >= 8 ? 2 : kRB;  // weight rows per batch (fewer with 8 input rows, for registers)
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int g = tid / G.TPG;
   const bool active = g < G.RG;  // whole warps: TPG is a multiple of 32
@@ -463,24 +465,24 @@ __device__ __forceinline__ bool gemv_run(const FrameParams& P, const CallArgs& c
       if (!active || !ok) continue;
       const unsigned char* tp = slots + (size_t)slot * kSlotBytes;
       const int nrow = (R - g + G.RG - 1) / G.RG;  // rows g, g + RG, ... of the tile
-      for (int i0 = 0; i0 < nrow; i0 += kRB) {
-        int rw[kRB];
+      for (int i0 = 0; i0 < nrow; i0 += KRB) {
+        int rw[KRB];
 #pragma unroll
-        for (int w = 0; w < kRB; ++w) rw[w] = g + G.RG * min(i0 + w, nrow - 1);
-        float2 acc[kRB][NQ];
+        for (int w = 0; w < KRB; ++w) rw[w] = g + G.RG * min(i0 + w, nrow - 1);
+        float2 acc[KRB][NQ];
 #pragma unroll
-        for (int w = 0; w < kRB; ++w)
+        for (int w = 0; w < KRB; ++w)
 #pragma unroll
           for (int q = 0; q < NQ; ++q) acc[w][q] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < CPT; ++j) {
           const int c = tl + j * G.TPG;
           if (c >= G.nch) continue;
-          Raw raw[kRB];
+          Raw raw[KRB];
 #pragma unroll
-          for (int w = 0; w < kRB; ++w) raw[w] = WTraits<WT>::ld_raw(tp + (size_t)rw[w] * row_bytes + (size_t)c * 16);
+          for (int w = 0; w < KRB; ++w) raw[w] = WTraits<WT>::ld_raw(tp + (size_t)rw[w] * row_bytes + (size_t)c * 16);
 #pragma unroll
-          for (int w = 0; w < kRB; ++w) {
+          for (int w = 0; w < KRB; ++w) {
             float2 wv[PPC];
             WTraits<WT>::cvt(raw[w], wv);
 #pragma unroll
@@ -489,17 +491,17 @@ __device__ __forceinline__ bool gemv_run(const FrameParams& P, const CallArgs& c
               for (int p = 0; p < PPC; ++p) acc[w][q] = ffma2(wv[p], av[j][q][p], acc[w][q]);
           }
         }
-        float v[kRB * NQ];
+        float v[KRB * NQ];
 #pragma unroll
-        for (int w = 0; w < kRB; ++w)
+        for (int w = 0; w < KRB; ++w)
 #pragma unroll
           for (int q = 0; q < NQ; ++q) v[w * NQ + q] = acc[w][q].x + acc[w][q].y;
-        const float sum = reduce_scatter<kRB * NQ>(v);
-        constexpr int NV = kRB * NQ;
+        const float sum = reduce_scatter<KRB * NQ>(v);
+        constexpr int NV = KRB * NQ;
         constexpr int shift = NV >= 32 ? 0 : (NV >= 16 ? 1 : (NV >= 8 ? 2 : (NV >= 4 ? 3 : 4)));
         if ((lane & ((1 << shift) - 1)) == 0) {
           const int vi = lane >> shift, w = vi / NQ, q = vi % NQ;
-          if (i0 + w < nrow) rk[((size_t)rw[w] * 4 + q) * WPG + wg] = sum;
+          if (i0 + w < nrow) rk[((size_t)rw[w] * kRedQ + q) * WPG + wg] = sum;
         }
       }
     }
@@ -512,7 +514,7 @@ __device__ __forceinline__ bool gemv_run(const FrameParams& P, const CallArgs& c
       const float* rk = red + k * (kRedFloats / 2);
       float ys[2] = {0.0f, 0.0f};
       for (int h = 0; h < rpu; ++h) {
-        const float* rr = rk + ((size_t)(i + h * tile.n) * 4 + q) * WPG;
+        const float* rr = rk + ((size_t)(i + h * tile.n) * kRedQ + q) * WPG;
         float s = 0.0f;
         for (int w = 0; w < WPG; ++w) s += rr[w];
         ys[h] = s;
@@ -730,9 +732,9 @@ __device__ __forceinline__ bool gemv_tc_any(const FrameParams& P, const CallArgs
   return false;  // fp32 weights never take the tensor path
 }
 
-// Input rows per group for a geometry (2 when a thread owns 3 chunks, to
-// bound registers).
-__device__ __forceinline__ int group_rows(const RowGeom& G) { return G.CPT >= 3 ? 2 : 4; }
+// Input rows per group for a geometry: 8 when a thread owns one chunk of a
+// row, 4 with two and 2 with three (registers).
+__device__ __forceinline__ int group_rows(const RowGeom& G) { return G.CPT >= 3 ? 2 : (G.CPT == 2 ? 4 : 8); }
 
 template <typename WT, int KIND>
 __device__ __forceinline__ bool gemv_dispatch(const FrameParams& P, const CallArgs& ca, int l, const RowGeom& G,
@@ -742,6 +744,7 @@ __device__ __forceinline__ bool gemv_dispatch(const FrameParams& P, const CallAr
 #define CP_RUN(C_, Q_) \
   gemv_run<WT, KIND, C_, Q_>(P, ca, l, G, sh, pr, rope, slots, red, q0, nqv, ta, tb, issue_next, gain)
   if (G.CPT == 1) {
+    if (nqv >= 5) return CP_RUN(1, 8);
     if (nqv >= 3) return CP_RUN(1, 4);
     if (nqv == 2) return CP_RUN(1, 2);
     return CP_RUN(1, 1);

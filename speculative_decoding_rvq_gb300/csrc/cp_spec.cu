@@ -142,7 +142,8 @@ cp_spec_status check_weights(const cp_spec_model* model, const cp_spec_weights* 
 // Shape limits of the pass kernels (checked before anything is launched).
 constexpr size_t kSmemPerSm = 227 * 1024;
 constexpr int kMaxChunksPerRow = 3 * cpk::kThreads;  // a GEMV thread owns at most 3 chunks of a row
-constexpr int kRedFloatsHost = 1280;                 // the GEMV kernel's partial-sum buffer (floats)
+constexpr int kRedFloatsHost = 1536;                 // the GEMV kernel's partial-sum buffer (floats)
+constexpr int kRedQHost = 8;                         // its input-row stride
 constexpr int kTcMinRows = 32;                       // rows per pass (max_streams x row slots) that select the tensor path
 
 cp_spec_status check_shapes(const cp_spec_model* m, int N, int KC) {
@@ -156,7 +157,7 @@ cp_spec_status check_shapes(const cp_spec_model* m, int N, int KC) {
     return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "GEMV width %zu bytes above %d", maxk * 16, kMaxChunksPerRow * 16);
   if (m->num_code_groups > 64 || (size_t)(64 + m->num_code_groups * m->head_dim) * 4 > kSmemPerSm)
     return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "attention scratch too large");
-  // partial sums of one GEMV tile: rows x 4 input rows x warps per row group
+  // partial sums of one GEMV tile: rows x 8 input rows x warps per row group
   // (the kernel's tile and row-group geometry, restated)
   const int Ks[4] = {H, QD, F, H};
   const int rpus[4] = {2, 1, 1, 1};
@@ -165,7 +166,7 @@ cp_spec_status check_shapes(const cp_spec_model* m, int N, int KC) {
     const int TPG = std::min(cpk::kThreads, (nch + 31) / 32 * 32);
     const int WPG = TPG / 32;
     const int rows = std::max(1, std::min((int)(cpk::kSlotBytes / ((size_t)rpus[i] * nch * 16)), cpk::kMaxTileRows / rpus[i])) * rpus[i];
-    if ((size_t)rows * 4 * WPG > (size_t)kRedFloatsHost / 2)  // two tiles' sums at once
+    if ((size_t)rows * kRedQHost * WPG > (size_t)kRedFloatsHost / 2)  // two tiles' sums at once
       return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "GEMV partial-sum buffer too small for width %d", Ks[i]);
   }
   (void)N;
