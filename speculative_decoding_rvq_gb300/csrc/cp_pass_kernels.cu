@@ -580,78 +580,88 @@ __device__ __forceinline__ void load_act8(const ActRow& a, int k0, float (&v)[8]
 }
 
 constexpr int kTcMaxN = 4;  // n-tiles of 8 weight rows per tile (tiles hold at most 32 rows on this path)
-constexpr int kTcPipe = 2;  // K blocks of 32 whose inputs are loaded ahead
-// per-warp output blocks (16 rows x 32 columns) and 16 row descriptors
-constexpr int kTcYFloats = kWarps * 16 * kTcMaxN * 8 + kWarps * 16 * (int)(sizeof(ActRow) / sizeof(float));
+constexpr int kTcPipe = 1;  // K blocks of 32 whose inputs are loaded ahead
+// per-warp output blocks (16 rows x the columns of two tiles) and 16 row descriptors
+constexpr int kTcYCols = 2 * kTcMaxN * 8;
+constexpr int kTcYFloats = kWarps * 16 * kTcYCols + kWarps * 16 * (int)(sizeof(ActRow) / sizeof(float));
 
-// One tile (R weight rows, K inputs) against pass rows [m0, m0 + 16) by one
-// warp: the MMA chain over K, then the outputs of the tile's units for those
-// rows.  src/inv: the warp's 16 input rows (rows past nrows repeat the last).
-template <int KIND, int NT>
-__device__ __forceinline__ void tc_block(const FrameParams& P, int l, const int* heads, const PassRows& pr,
-                                         const float2* rope, const unsigned char* tile, Tile tl, int R, int K,
-                                         const ActRow* src, const float* inv, const float* gain, int m0, int nrows,
-                                         float* y) {
-  // inv: RMSNorm scales of all pass rows (null when not normed)
+// A pair of resident tiles (R0 and R1 weight rows, K inputs; R1 = 0 when
+// there is one) against pass rows [m0, m0 + 16) by one warp: one MMA chain
+// over K per 8-row n-tile, the inputs loaded and split once for both tiles;
+// then the outputs of the tiles' units for those rows.  src: the warp's 16
+// input rows (rows past nrows repeat the last); inv: RMSNorm scales of all
+// pass rows (null when not normed).
+template <int KIND, int NTT>
+__device__ __noinline__ void tc_block(const FrameParams& P, int l, const int* heads, const PassRows& pr,
+                                         const float2* rope, const unsigned char* tp0, const unsigned char* tp1,
+                                         Tile tl0, Tile tl1, int nt0, int K, const ActRow* src, const float* inv,
+                                         const float* gain, int m0, int nrows, float* y) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int rpu = rows_per_unit(KIND);
+  const int R0 = tl0.n * rpu, R1 = tl1.n * rpu;
   const size_t row_bytes = (size_t)K * 2;
-  float c[NT][4];
+  float c[NTT][4];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
+  for (int j = 0; j < NTT; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
   const ActRow ra = src[g], rb = src[g + 8];
   const float ia = inv ? inv[min(m0 + g, nrows - 1)] : 1.0f, ib = inv ? inv[min(m0 + g + 8, nrows - 1)] : 1.0f;
-  const unsigned char* wr[NT];
+  // weight row of n-tile j for this lane, as a byte offset from tp0 (the
+  // second slot follows the first)
+  uint32_t wr[NTT];
 #pragma unroll
-  for (int j = 0; j < NT; ++j) wr[j] = tile + (size_t)min(8 * j + g, R - 1) * row_bytes + (size_t)t * 16;
+  for (int j = 0; j < NTT; ++j)
+    wr[j] = (uint32_t)(j < nt0 ? (size_t)min(8 * j + g, R0 - 1) * row_bytes
+                               : (size_t)(tp1 - tp0) + (size_t)min(8 * (j - nt0) + g, R1 - 1) * row_bytes) +
+            (uint32_t)t * 16;
   // K in blocks of 32; the inputs of kTcPipe blocks are loaded before any of
   // them is used, so that many L2 reads are in flight per warp
   for (int kb0 = 0; kb0 < K; kb0 += 32 * kTcPipe) {
-  float pa[kTcPipe][8], pb[kTcPipe][8];
+    float pa[kTcPipe][8], pb[kTcPipe][8];
 #pragma unroll
-  for (int u = 0; u < kTcPipe; ++u) {
-    const int kb = kb0 + 32 * u;
-    if (kb < K) {
-      load_act8(ra, kb + 8 * t, pa[u]);
-      load_act8(rb, kb + 8 * t, pb[u]);
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < kTcPipe; ++u) {
-    const int kb = kb0 + 32 * u;
-    if (kb >= K) break;
-    const int k0 = kb + 8 * t;
-    float (&va)[8] = pa[u];
-    float (&vb)[8] = pb[u];
-    if (gain != nullptr) {
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float gk = gain[k0 + e];
-        va[e] = va[e] * ia * gk;
-        vb[e] = vb[e] * ib * gk;
+    for (int u = 0; u < kTcPipe; ++u) {
+      const int kb = kb0 + 32 * u;
+      if (kb < K) {
+        load_act8(ra, kb + 8 * t, pa[u]);
+        load_act8(rb, kb + 8 * t, pb[u]);
       }
     }
-    uint32_t ah[2][4], al[2][4];
 #pragma unroll
-    for (int s = 0; s < 2; ++s) {
-      split_bf16x2(va[4 * s + 0], va[4 * s + 1], ah[s][0], al[s][0]);
-      split_bf16x2(vb[4 * s + 0], vb[4 * s + 1], ah[s][1], al[s][1]);
-      split_bf16x2(va[4 * s + 2], va[4 * s + 3], ah[s][2], al[s][2]);
-      split_bf16x2(vb[4 * s + 2], vb[4 * s + 3], ah[s][3], al[s][3]);
-    }
+    for (int u = 0; u < kTcPipe; ++u) {
+      const int kb = kb0 + 32 * u;
+      if (kb >= K) break;
+      const int k0 = kb + 8 * t;
+      float (&va)[8] = pa[u];
+      float (&vb)[8] = pb[u];
+      if (gain != nullptr) {
 #pragma unroll
-    for (int j = 0; j < NT; ++j) {
-      const uint4 w = *reinterpret_cast<const uint4*>(wr[j] + (size_t)kb * 2);
-      mma_bf16_16816(c[j], ah[0][0], ah[0][1], ah[0][2], ah[0][3], w.x, w.y);
-      mma_bf16_16816(c[j], al[0][0], al[0][1], al[0][2], al[0][3], w.x, w.y);
-      mma_bf16_16816(c[j], ah[1][0], ah[1][1], ah[1][2], ah[1][3], w.z, w.w);
-      mma_bf16_16816(c[j], al[1][0], al[1][1], al[1][2], al[1][3], w.z, w.w);
+        for (int e = 0; e < 8; ++e) {
+          const float gk = gain[k0 + e];
+          va[e] = va[e] * ia * gk;
+          vb[e] = vb[e] * ib * gk;
+        }
+      }
+      uint32_t ah[2][4], al[2][4];
+#pragma unroll
+      for (int s = 0; s < 2; ++s) {
+        split_bf16x2(va[4 * s + 0], va[4 * s + 1], ah[s][0], al[s][0]);
+        split_bf16x2(vb[4 * s + 0], vb[4 * s + 1], ah[s][1], al[s][1]);
+        split_bf16x2(va[4 * s + 2], va[4 * s + 3], ah[s][2], al[s][2]);
+        split_bf16x2(vb[4 * s + 2], vb[4 * s + 3], ah[s][3], al[s][3]);
+      }
+#pragma unroll
+      for (int j = 0; j < NTT; ++j) {
+        const uint4 w = *reinterpret_cast<const uint4*>(tp0 + wr[j] + (size_t)kb * 2);
+        mma_bf16_16816(c[j], ah[0][0], ah[0][1], ah[0][2], ah[0][3], w.x, w.y);
+        mma_bf16_16816(c[j], al[0][0], al[0][1], al[0][2], al[0][3], w.x, w.y);
+        mma_bf16_16816(c[j], ah[1][0], ah[1][1], ah[1][2], ah[1][3], w.z, w.w);
+        mma_bf16_16816(c[j], al[1][0], al[1][1], al[1][2], al[1][3], w.z, w.w);
+      }
     }
   }
-  }
-  // C fragment: c[j][0..1] = rows g, cols 8j + 2t, +1; c[j][2..3] = row g + 8
-  const int W = NT * 8;
+  // C fragment: c[j][0..1] = row g, cols 8j + 2t, +1; c[j][2..3] = row g + 8
+  constexpr int W = NTT * 8;
 #pragma unroll
-  for (int j = 0; j < NT; ++j) {
+  for (int j = 0; j < NTT; ++j) {
     y[g * W + 8 * j + 2 * t] = c[j][0];
     y[g * W + 8 * j + 2 * t + 1] = c[j][1];
     y[(g + 8) * W + 8 * j + 2 * t] = c[j][2];
@@ -659,23 +669,28 @@ __device__ __forceinline__ void tc_block(const FrameParams& P, int l, const int*
   }
   __syncwarp();
   const int rows = min(16, nrows - m0);
-  const int rpu = rows_per_unit(KIND);
-  for (int it = lane; it < tl.n * rows; it += 32) {
-    const int i = it / rows, q = it - i * rows;
-    const float y0 = y[q * W + i], y1 = rpu == 2 ? y[q * W + i + tl.n] : 0.0f;
-    float ho = 0.0f;
-    if (KIND == kO || KIND == kDown) ho = __ldcg(P.h + (size_t)pr.prow[m0 + q] * P.H + tl.u0 + i);
-    gemv_out<KIND>(P, l, heads, pr, rope, tl.u0 + i, m0 + q, y0, y1, ho);
+  for (int k = 0; k < 2; ++k) {
+    const Tile tl = k == 0 ? tl0 : tl1;
+    const int col0 = k == 0 ? 0 : 8 * nt0;
+    for (int it = lane; it < tl.n * rows; it += 32) {
+      const int i = it / rows, q = it - i * rows;
+      const float y0 = y[q * W + col0 + i], y1 = rpu == 2 ? y[q * W + col0 + i + tl.n] : 0.0f;
+      float ho = 0.0f;
+      if (KIND == kO || KIND == kDown) ho = __ldcg(P.h + (size_t)pr.prow[m0 + q] * P.H + tl.u0 + i);
+      gemv_out<KIND>(P, l, heads, pr, rope, tl.u0 + i, m0 + q, y0, y1, ho);
+    }
   }
   __syncwarp();
 }
 
 // The tensor-core GEMV of one kind for all rows of the pass (bf16 weights):
-// per tile, warp w takes row blocks w, w + kWarps, ... of 16 rows.
+// tiles in resident pairs (both slots); per pair, warp w takes row blocks
+// w, w + kWarps, ... of 16 rows, so each row block's inputs are read and
+// split once per pair.
 template <int KIND>
-__device__ __forceinline__ bool gemv_tc(const FrameParams& P, const CallArgs& ca, int l, GemvShared& sh, const PassRows& pr,
-                        const float2* rope, unsigned char* slots, float* ybuf, float* s_inv, int nrows,
-                        const float* gain) {
+__device__ __forceinline__ bool gemv_tc(const FrameParams& P, const CallArgs& ca, int l, GemvShared& sh,
+                                        const PassRows& pr, const float2* rope, unsigned char* slots, float* ybuf,
+                                        float* s_inv, int nrows, const float* gain) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = gemv_K(P, KIND);
   const int rpu = rows_per_unit(KIND);
@@ -694,32 +709,43 @@ __device__ __forceinline__ bool gemv_tc(const FrameParams& P, const CallArgs& ca
       if (lane == 0) s_inv[i] = 1.0f / sqrtf(ss / (float)K + P.eps);
     }
   __syncthreads();
-  float* y = ybuf + (size_t)warp * 16 * (kTcMaxN * 8);
-  ActRow* src = reinterpret_cast<ActRow*>(ybuf + (size_t)kWarps * 16 * (kTcMaxN * 8)) + warp * 16;  // 16 row descriptors per warp
+  float* y = ybuf + (size_t)warp * 16 * kTcYCols;
+  ActRow* src = reinterpret_cast<ActRow*>(ybuf + (size_t)kWarps * 16 * kTcYCols) + warp * 16;  // 16 row descriptors per warp
   const int nblk = (nrows + 15) / 16;
+  const float* inv = gain ? s_inv : nullptr;
   bool ok = true;
-  for (int t = 0; t < sh.ntiles; ++t) {
-    const int slot = t & 1;
-    const Tile tl = sh.tiles[t];
-    const int R = tl.n * rpu;
-    if (!mbar_wait_bounded(&sh.full[slot], (uint32_t)(t >> 1) & 1u, &P.ctl->status, kTileTimeoutNs)) ok = false;
+  for (int t0 = 0; t0 < sh.ntiles; t0 += 2) {
+    const bool two = t0 + 1 < sh.ntiles;
+    const Tile tl0 = sh.tiles[t0], tl1 = two ? sh.tiles[t0 + 1] : Tile{0, 0};
+    if (!mbar_wait_bounded(&sh.full[0], (uint32_t)(t0 >> 1) & 1u, &P.ctl->status, kTileTimeoutNs)) ok = false;
+    if (two && !mbar_wait_bounded(&sh.full[1], (uint32_t)(t0 >> 1) & 1u, &P.ctl->status, kTileTimeoutNs)) ok = false;
     if (ok) {
-      const unsigned char* tp = slots + (size_t)slot * kSlotBytes;
+      const int nt0 = (tl0.n * rpu + 7) / 8, ntt = nt0 + (tl1.n * rpu + 7) / 8;
       for (int mb = warp; mb < nblk; mb += kWarps) {
         const int m0 = mb * 16;
         if (lane < 16) src[lane] = act_row<__nv_bfloat16>(P, ca, pr, KIND, l, min(m0 + lane, nrows - 1));
         __syncwarp();
-        const float* inv = gain ? s_inv : nullptr;
-        const int nt = (R + 7) / 8;
-        if (nt <= 1) tc_block<KIND, 1>(P, l, sh.heads, pr, rope, tp, tl, R, K, src, inv, gain, m0, nrows, y);
-        else if (nt == 2) tc_block<KIND, 2>(P, l, sh.heads, pr, rope, tp, tl, R, K, src, inv, gain, m0, nrows, y);
-        else if (nt == 3) tc_block<KIND, 3>(P, l, sh.heads, pr, rope, tp, tl, R, K, src, inv, gain, m0, nrows, y);
-        else tc_block<KIND, 4>(P, l, sh.heads, pr, rope, tp, tl, R, K, src, inv, gain, m0, nrows, y);
+#define CP_TC(N_) \
+  tc_block<KIND, N_>(P, l, sh.heads, pr, rope, slots, slots + kSlotBytes, tl0, tl1, nt0, K, src, inv, gain, m0, nrows, y)
+        switch (ntt) {
+          case 1: CP_TC(1); break;
+          case 2: CP_TC(2); break;
+          case 3: CP_TC(3); break;
+          case 4: CP_TC(4); break;
+          case 5: CP_TC(5); break;
+          case 6: CP_TC(6); break;
+          case 7: CP_TC(7); break;
+          default: CP_TC(8); break;
+        }
+#undef CP_TC
       }
     }
     ok = __syncthreads_and(ok ? 1 : 0) != 0;
     if (!ok) return false;
-    if (threadIdx.x == 0 && t + 2 < sh.ntiles) gemv_issue<__nv_bfloat16, KIND>(P, l, sh, slots, t + 2);
+    if (threadIdx.x == 0) {
+      if (t0 + 2 < sh.ntiles) gemv_issue<__nv_bfloat16, KIND>(P, l, sh, slots, t0 + 2);
+      if (t0 + 3 < sh.ntiles) gemv_issue<__nv_bfloat16, KIND>(P, l, sh, slots, t0 + 3);
+    }
   }
   return true;
 }
