@@ -896,8 +896,8 @@ __global__ void __launch_bounds__(kThreads, TC ? 1 : 2) gemv_kernel(const __grid
 // 0..pos of the stream's KV cache (this pass's rows were appended by the QKV
 // kernel): warp w scores positions w, w + kWarps, ... (the dot product split
 // over lanes, reduced by a butterfly) and parks their value rows in shared
-// memory; then each output pair forms the softmax over all positions in
-// index order and sums the values in index order.
+// memory; then warp 0 forms the softmax weights (denominator summed in index
+// order) and each output pair sums the weighted values in index order.
 __global__ void __launch_bounds__(kThreads, 2) attention_kernel(const __grid_constant__ FrameParams P, int l) {
   extern __shared__ __align__(16) float asmem[];
   pdl_launch_dependents();
@@ -937,14 +937,26 @@ __global__ void __launch_bounds__(kThreads, 2) attention_kernel(const __grid_con
     if (lane == 0) sc[j] = sdot;
   }
   __syncthreads();
-  if (tid < lines) {
+  // softmax weights by warp 0, one lane per position: e_j = exp(s_j - max),
+  // the denominator summed in index order, w_j = e_j / den (in place of s_j)
+  if (warp == 0) {
     float mx = -INFINITY;
-    for (int j = 0; j <= pos; ++j) mx = fmaxf(mx, sc[j]);
+    for (int j = lane; j <= pos; j += 32) mx = fmaxf(mx, sc[j]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    for (int j = lane; j <= pos; j += 32) sc[j] = expf(sc[j] - mx);
+    __syncwarp();
     float den = 0.0f;
-    for (int j = 0; j <= pos; ++j) den += expf(sc[j] - mx);
+    if (lane == 0)
+      for (int j = 0; j <= pos; ++j) den += sc[j];
+    den = __shfl_sync(0xffffffffu, den, 0);
+    for (int j = lane; j <= pos; j += 32) sc[j] = sc[j] / den;
+  }
+  __syncthreads();
+  if (tid < lines) {
     float2 o = make_float2(0.f, 0.f);
     for (int j = 0; j <= pos; ++j) {
-      const float w = expf(sc[j] - mx) / den;
+      const float w = sc[j];
       const float2 v = *reinterpret_cast<const float2*>(vs + (size_t)j * d + 2 * tid);
       o.x = fmaf(w, v.x, o.x);
       o.y = fmaf(w, v.y, o.y);
