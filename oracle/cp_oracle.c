@@ -396,6 +396,21 @@ void orc_head_logits(const orc_model* M, int j, const double* hn, double* out64,
   }
 }
 
+/* "RVQ Position Aware Speculative Decoding for On Device TTS", section 2.2:
+ * the drafter adds the offset of its lookahead distance to the hidden state
+ * the heads read (the final-normed output), then applies the later head. */
+void orc_draft_logits(const orc_model* M, int j, int t, const double* hn, float* out32) {
+  if (t > M->K || !M->draft_offset) {
+    orc_head_logits(M, j, hn, NULL, out32);
+    return;
+  }
+  double* shifted = (double*)malloc(sizeof(double) * (size_t)M->H);
+  const float* b = M->draft_offset + (size_t)(t - 1) * M->H;
+  for (int i = 0; i < M->H; ++i) shifted[i] = hn[i] + (double)b[i];
+  orc_head_logits(M, j, shifted, NULL, out32);
+  free(shifted);
+}
+
 /* Input row of position pos: x at position 0, E_{pos-1}(code) otherwise. */
 static void input_row(const orc_model* M, const float* x, int pos, int code, double* row) {
   if (pos == 0) {
@@ -423,7 +438,7 @@ void orc_teacher_logits(const orc_model* M, const float* x, const int* codes, in
     if (draft) {
       for (int t = 1; t <= n_draft; ++t) {
         float* dst = draft + ((size_t)(j - 1) * n_draft + (t - 1)) * V;
-        if (j + t <= M->G - 1) orc_head_logits(M, j + t, hn + (size_t)j * H, NULL, dst);
+        if (j + t <= M->G - 1) orc_draft_logits(M, j + t, t, hn + (size_t)j * H, dst);
         else for (int v = 0; v < V; ++v) dst[v] = 0.0f;
       }
     }
@@ -496,9 +511,10 @@ static void decode_one_frame(const orc_model* M, int N, int top_k, float T, uint
       const int R = G - 1 - s;
       const int n_d = (N - 1) < R ? (N - 1) : R;
       mg = INFINITY;
-      /* Draft: head_{s+t} applied to the current hidden h_s. */
+      /* Draft: head_{s+t} applied to the current hidden h_s (plus the
+       * offset b_t where one is given). */
       for (int t = 1; t <= n_d; ++t) {
-        orc_head_logits(M, s + t, hs, NULL, lg);
+        orc_draft_logits(M, s + t, t, hs, lg);
         orc_process(lg, V, top_k, T, q + (size_t)(t - 1) * V, &m1);
         if (m1 < mg) mg = m1;
         dr[t - 1] = orc_sample(q + (size_t)(t - 1) * V, V,
@@ -557,6 +573,7 @@ int orc_decode_frames(const orc_model* M, int N, const int* top_k, const float* 
   if (!M || !codes || !x || !c0 || !st) return -1;
   if (!(N == 0 || (N >= 2 && N <= 8))) return -1;
   if (M->G < 2 || M->nq % M->nkv != 0 || M->d % 2 != 0) return -1;
+  if (M->K < 0 || (M->K > 0 && !M->draft_offset)) return -1;
   if (n_log) *n_log = 0;
   for (int f = 0; f < F; ++f)
     for (int b = 0; b < B; ++b)

@@ -17,6 +17,9 @@
  *    embedding table and one LM head per codebook position).
  *  - "Awesome-ML-SYS-Tutorial" (Fast AR / MTP sections): the two-position
  *    prefix [hidden, code-0 embedding], per-frame KV rebuilt each frame.
+ *  - "RVQ Position Aware Speculative Decoding for On Device TTS", section 2.2
+ *    (position-aware offsets) and Figure 3: the draft at lookahead t reads
+ *    head_{k+t} on h_k + b_t; the target head never sees an offset.
  *
  * Precision: the forward pass runs in float64 on weights given as float32
  * (bf16 and fp32 storage values are exact in float32); logits are rounded
@@ -60,6 +63,10 @@ typedef struct {
   const float *w_gate;     /* [L][F][H]    */
   const float *w_up;       /* [L][F][H]    */
   const float *w_down;     /* [L][H][F]    */
+  /* Position-aware draft offsets b_1..b_K ([K][H], float32), shared by every
+   * starting depth.  K = 0 (or NULL): the heads are reused as they are. */
+  int K;
+  const float *draft_offset;
 } orc_model;
 
 typedef struct {
@@ -121,10 +128,13 @@ void orc_forward(const orc_model* M, double* kv, int n, const double* in_rows, c
                  double* out_normed);
 /* logits of head_j (1 <= j <= G-1) on a normed hidden, float64 and float32. */
 void orc_head_logits(const orc_model* M, int j, const double* hn, double* out64, float* out32);
+/* Draft logits at lookahead t >= 1 from the normed hidden hn of depth s
+ * (j = s + t): head_j on hn + b_t when t <= K, head_j on hn otherwise. */
+void orc_draft_logits(const orc_model* M, int j, int t, const double* hn, float* out32);
 /* Teacher-forced logits over positions 0..P-1 of one frame (rows x,
  * E_0(c_0), ..., E_{P-2}(c_{P-2})): logits [P-1][V] for head_j at position
- * j; draft (optional) [P-1][n_draft][V] for head_{j+t} at position j (zero
- * where j+t > G-1). */
+ * j; draft (optional) [P-1][n_draft][V]: the draft logits of lookahead t
+ * at position j (orc_draft_logits with head_{j+t}; zero where j+t > G-1). */
 void orc_teacher_logits(const orc_model* M, const float* x, const int* codes, int P, int n_draft,
                         float* logits, float* draft);
 /* Decode frames.  N = 0: autoregressive loop; N in 2..8: speculative rounds.

@@ -43,7 +43,8 @@ class OrcModel(C.Structure):
     _fields_ = [(n, C.c_int) for n in ("H", "L", "nq", "nkv", "d", "F", "V", "G")] + [
         ("theta", C.c_double), ("eps", C.c_double)] + [
         (n, C.c_void_p) for n in ("embed", "head", "final_norm", "attn_norm", "wq", "wk", "wv", "wo",
-                                  "ffn_norm", "w_gate", "w_up", "w_down")]
+                                  "ffn_norm", "w_gate", "w_up", "w_down")] + [
+        ("K", C.c_int), ("draft_offset", C.c_void_p)]
 
 
 class OrcStats(C.Structure):
@@ -93,6 +94,7 @@ def lib():
             L.orc_kv_doubles.restype = C.c_size_t
             L.orc_forward.argtypes = [vp, vp, i32, vp, vp, vp]
             L.orc_head_logits.argtypes = [vp, i32, vp, vp, vp]
+            L.orc_draft_logits.argtypes = [vp, i32, i32, vp, vp]
             L.orc_teacher_logits.argtypes = [vp, vp, vp, i32, i32, vp, vp]
             L.orc_decode_frames.argtypes = [vp, i32, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp]
             L.orc_decode_frames.restype = i32
@@ -208,9 +210,16 @@ class Model:
             "w_up": np.ascontiguousarray(np.stack([f32(l["w_up"]) for l in L])),
             "w_down": np.ascontiguousarray(np.stack([f32(l["w_down"]) for l in L])),
         }
+        # optional position-aware draft offsets b_1..b_K [K, H] float32
+        off = weights.get("draft_offset")
+        K = 0
+        if off is not None and np.asarray(off).shape[0] > 0:
+            self._arrs["draft_offset"] = np.ascontiguousarray(off, dtype=np.float32).reshape(-1, spec.hidden)
+            K = self._arrs["draft_offset"].shape[0]
         s = spec
+        self.K = K
         self.c = OrcModel(H=s.hidden, L=s.n_layers, nq=s.n_q_heads, nkv=s.n_kv_heads, d=s.head_dim,
-                          F=s.ffn, V=s.vocab, G=s.num_code_groups, theta=s.rope_theta, eps=s.rms_eps,
+                          F=s.ffn, V=s.vocab, G=s.num_code_groups, theta=s.rope_theta, eps=s.rms_eps, K=K,
                           **{k: v.ctypes.data for k, v in self._arrs.items()})
 
     @property
@@ -236,6 +245,13 @@ class Model:
         o32 = np.empty(self.spec.vocab, np.float32)
         lib().orc_head_logits(self.ptr, int(j), _p(hn), _p(o64), _p(o32))
         return o64, o32
+
+    def draft_logits(self, j: int, t: int, hn: np.ndarray) -> np.ndarray:
+        """float32 draft logits of lookahead t read by head_j from the normed hidden hn."""
+        hn = np.ascontiguousarray(hn, dtype=np.float64)
+        o32 = np.empty(self.spec.vocab, np.float32)
+        lib().orc_draft_logits(self.ptr, int(j), int(t), _p(hn), _p(o32))
+        return o32
 
     def input_row(self, x, pos: int, code: int) -> np.ndarray:
         if pos == 0:

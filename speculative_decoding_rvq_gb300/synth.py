@@ -108,7 +108,7 @@ def _normal(seed: int, tensor_id: int, shape, std: float) -> np.ndarray:
     return out.reshape(shape)
 
 
-# tensor ids: 0 embed, 1 lm_head, 2 final_norm, then 16 + 16*layer + j
+# tensor ids: 0 embed, 1 lm_head, 2 final_norm, 3 draft offsets, then 16 + 16*layer + j
 _T_EMBED, _T_HEAD = 0, 1
 
 
@@ -151,6 +151,17 @@ def gen_weights(spec: ModelSpec, seed: int = 0, std: float = WEIGHT_STD) -> dict
             "w_down": mat(_layer_tid(l, 6), (H, F)),
         })
     return w
+
+
+_T_OFFSET = 3
+
+
+def gen_draft_offsets(spec: ModelSpec, K: int, seed: int = 0, std: float = 0.25) -> np.ndarray:
+    """K position-aware draft offset vectors b_1..b_K ~ N(0, std^2), [K, H] float32.
+
+    The pages train these on speech data; synthetic runs draw them at random,
+    which exercises the arithmetic without the acceptance gain."""
+    return _normal(seed, _T_OFFSET, (K, spec.hidden), std)
 
 
 def weights_as_f64(spec: ModelSpec, w: dict) -> dict:

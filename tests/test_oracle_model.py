@@ -149,11 +149,18 @@ def test_greedy_speculative_equals_greedy_ar(orc, G):
         assert np.all(rounds["n_acc"] <= rounds["n_d"])
 
 
-def test_speculative_law_equals_autoregressive_law(orc):
-    """Exact law of (c_1, c_2, c_3) under AR by enumeration vs speculative frequencies (chi-square)."""
+@pytest.mark.parametrize("K", [0, 2])
+def test_speculative_law_equals_autoregressive_law(orc, K):
+    """Exact law of (c_1, c_2, c_3) under AR by enumeration vs speculative frequencies (chi-square).
+
+    K = 2 adds position-aware draft offsets: they change only the drafts, so
+    the law is the same ("RVQ Position Aware Speculative Decoding for On
+    Device TTS", section 3.2)."""
     spec = S.ModelSpec(hidden=16, n_layers=1, n_q_heads=2, n_kv_heads=1, head_dim=8, ffn=32, vocab=4,
                        num_code_groups=4, dtype=S.DTYPE_F32)
     w = S.gen_weights(spec, seed=21, std=0.5)
+    if K:
+        w = {**w, "draft_offset": S.gen_draft_offsets(spec, K, seed=5, std=1.0)}
     m = orc.Model(spec, w)
     x, c0 = S.gen_frames(spec, 1, 1, seed=22)
     k, T = 3, 0.9
