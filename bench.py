@@ -254,15 +254,38 @@ def run_gpu(args, rank, world):
                                 xd=xd[:200], cd=cd[:200], G=spec.num_code_groups, peak=peak)
         result["accept_microbench"] = accept_microbench(peak)
         result["batched"] = batched(spec, dw, peak)
+        result["draft_offsets"] = offsets_line(spec, dw, xd[:200], cd[:200], peak)
     return result
 
 
-def sweep(cp_factory, xd, cd, G, peak):
+def offsets_line(spec, dw, xd, cd, peak, K=3):
+    """N = 4 with K = 3 position-aware draft offsets (synthetic N(0, 0.25^2): the pages'
+    trained offsets need speech data) on the sweep's 200 frames: the cost per pass and the
+    acceptance by offset, next to the same run without offsets."""
+    import torch
+    from speculative_decoding_rvq_gb300 import binding, synth as S
+    dwo = dict(dw)
+    dwo["draft_offset"] = torch.from_numpy(S.gen_draft_offsets(spec, K, seed=1)).cuda()
+    out = {"K": K, "offsets": "synthetic N(0, 0.25^2), seed 1"}
+    for name, w in (("with_offsets", dwo), ("without", dw)):
+        made = []
+
+        def factory(n, w=w):
+            made.append(binding.CpSpec(spec, w, n, TOP_K, TEMP, SEED, 1))
+            return made[-1]
+
+        r = sweep(factory, xd, cd, spec.num_code_groups, peak, windows=(4,))["N4"]
+        r["accepted_by_offset"] = made[-1].last_stats["accepted_by_offset"][1:4]
+        out[name] = r
+    return out
+
+
+def sweep(cp_factory, xd, cd, G, peak, windows=(0, 2, 3, 4, 5, 6, 7, 8)):
     """codes/s and per-pass time for the AR loop (N=0) and windows 2..8 on 200 frames."""
     import torch
     out = {}
     F = xd.shape[0]
-    for n in (0, 2, 3, 4, 5, 6, 7, 8):
+    for n in windows:
         cp = cp_factory(n)
         codes = torch.empty((F, 1, G), dtype=torch.int32, device="cuda")
         for _ in range(2):
@@ -278,6 +301,7 @@ def sweep(cp_factory, xd, cd, G, peak):
         torch.cuda.synchronize()
         ms = a.elapsed_time(b) / reps
         st = cp.stats()
+        cp.last_stats = st
         passes = st["passes"] / reps
         out[f"N{n}"] = {"codes_per_s": round(F * (G - 1) / (ms / 1e3), 1), "passes_per_frame": round(passes / F, 3),
                         "us_per_pass": round(ms * 1e3 / passes, 2),

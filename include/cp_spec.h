@@ -90,7 +90,17 @@ typedef struct {
  * Per layer l: wq [nq*d][H], wk [nkv*d][H], wv [nkv*d][H], wo [H][nq*d],
  * w_gate [F][H], w_up [F][H], w_down [H][F]; attn_norm, ffn_norm [H] fp32.
  * final_norm [H] fp32.  The blocks are pre-norm: h += Wo attn(RMSNorm(h));
- * h += Wdown (silu(Wgate b) * Wup b) with b = RMSNorm(h). */
+ * h += Wdown (silu(Wgate b) * Wup b) with b = RMSNorm(h).
+ * draft_offset: [K][H] fp32 position-aware draft offsets b_1..b_K, K =
+ * config.draft_offsets (NULL when K = 0).  The draft of lookahead t reads
+ * head_{s+t} on h_s + b_t for t <= K, and h_s alone beyond K, where h_s is
+ * the final-normed hidden the target head_s reads; the target heads never see
+ * an offset, so the committed codes keep the autoregressive law ("RVQ
+ * Position Aware Speculative Decoding for On Device TTS", section 2.2 and
+ * Figure 3).  The library reads b once, in cp_spec_init (and in every
+ * cp_spec_decode_frames_static call), and keeps the products head_j . b_t
+ * in the workspace: later changes to the values behind the pointer are not
+ * seen by an existing context. */
 typedef struct {
   const void* embed;
   const void* lm_head;
@@ -104,6 +114,7 @@ typedef struct {
   const void* w_gate[CP_SPEC_MAX_LAYERS];
   const void* w_up[CP_SPEC_MAX_LAYERS];
   const void* w_down[CP_SPEC_MAX_LAYERS];
+  const float* draft_offset;
 } cp_spec_weights;
 
 /* verify_window: 0 = autoregressive loop; 2..8 = one committed depth plus
@@ -111,19 +122,23 @@ typedef struct {
  * rejected because it leaves no draft slot).  top_k: 1..vocab, the default
  * for every stream and the maximum any stream may use.  temperature: 0 =
  * greedy, else in [1e-3, 100].  max_streams: streams the workspace is sized
- * for (>= 1). */
+ * for (>= 1).  draft_offsets: K, the number of position-aware draft offset
+ * vectors in weights.draft_offset, 0..7 (0 = the heads are reused without
+ * offsets); offsets beyond verify_window - 1 are never read. */
 typedef struct {
   int32_t verify_window;
   int32_t top_k;
   float temperature;
   uint64_t seed;
   int32_t max_streams;
+  int32_t draft_offsets;
 } cp_spec_config;
 
 /* Counters accumulated since init (or the last cp_spec_reset_stats).
  * committed = codes c_1..c_{G-1} emitted; passes = decoder passes (frame
  * prefills + rounds, or AR steps); accepted/drafted_by_offset[t] = drafts at
- * offset t (1..8) accepted / verified ("report acceptance by offset",
+ * offset t (1..8) accepted / reached by the left-to-right test (every draft
+ * up to and including the first rejection; "report acceptance by offset",
  * "Speculative Decoding, Beyond Text", section 06).  weight_bytes and
  * kv_bytes count the algorithmic HBM bytes of all decoder passes (every
  * layer matrix once per pass, each distinct lm_head applied in the pass

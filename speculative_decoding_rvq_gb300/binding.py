@@ -43,12 +43,12 @@ class Model(C.Structure):
 class Weights(C.Structure):
     _fields_ = [("embed", C.c_void_p), ("lm_head", C.c_void_p), ("final_norm", C.c_void_p)] + [
         (n, C.c_void_p * MAX_LAYERS) for n in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up",
-                                               "w_down")]
+                                               "w_down")] + [("draft_offset", C.c_void_p)]
 
 
 class Config(C.Structure):
     _fields_ = [("verify_window", C.c_int32), ("top_k", C.c_int32), ("temperature", C.c_float),
-                ("seed", C.c_uint64), ("max_streams", C.c_int32)]
+                ("seed", C.c_uint64), ("max_streams", C.c_int32), ("draft_offsets", C.c_int32)]
 
 
 class Stats(C.Structure):
@@ -135,7 +135,15 @@ def weights_to_device(spec: synth.ModelSpec, w: dict, device="cuda") -> dict:
 
     out = {k: dev(w[k]) for k in ("embed", "lm_head", "final_norm")}
     out["layers"] = [{k: dev(v) for k, v in lw.items()} for lw in w["layers"]]
+    if w.get("draft_offset") is not None and len(w["draft_offset"]) > 0:
+        out["draft_offset"] = dev(np.asarray(w["draft_offset"], np.float32).reshape(-1, spec.hidden))
     return out
+
+
+def n_draft_offsets(dw: dict) -> int:
+    """K of the position-aware draft offsets held in device weights (0 if none)."""
+    off = dw.get("draft_offset")
+    return 0 if off is None else int(off.shape[0])
 
 
 def weights_struct(dw: dict) -> Weights:
@@ -144,6 +152,7 @@ def weights_struct(dw: dict) -> Weights:
     for l, lw in enumerate(dw["layers"]):
         for n in ("attn_norm", "wq", "wk", "wv", "wo", "ffn_norm", "w_gate", "w_up", "w_down"):
             getattr(ws, n)[l] = _ptr(lw[n])
+    ws.draft_offset = _ptr(dw.get("draft_offset"))
     return ws
 
 
@@ -158,7 +167,7 @@ class CpSpec:
         self.dw = device_weights
         self.model = model_struct(spec)
         self.weights = weights_struct(device_weights)
-        self.config = Config(verify_window, top_k, temperature, seed, max_streams)
+        self.config = Config(verify_window, top_k, temperature, seed, max_streams, n_draft_offsets(device_weights))
         nbytes = self.lib.cp_spec_workspace_bytes(C.byref(self.model), C.byref(self.config))
         if nbytes == 0:
             _check(E_INVALID)
@@ -257,7 +266,8 @@ def decode_frames_static(spec: synth.ModelSpec, device_weights: dict, verify_win
         codes = torch.empty((F, B, spec.num_code_groups), dtype=torch.int32, device=x.device)
     model = model_struct(spec)
     weights = weights_struct(device_weights)
-    config = Config(verify_window, top_k, temperature, seed, B if max_streams is None else max_streams)
+    config = Config(verify_window, top_k, temperature, seed, B if max_streams is None else max_streams,
+                    n_draft_offsets(device_weights))
     rc = lib.cp_spec_decode_frames_static(C.byref(model), C.byref(weights), C.byref(config), B, F, first_frame,
                                           _ptr(x), _ptr(c0), _ptr(codes), _ptr(status), _stream())
     _check(rc, None, allow=(OK, W_AR_FALLBACK))

@@ -96,6 +96,8 @@ struct FrameParams {
   int Bmax; // stream capacity of the workspace (row slots = Bmax * NS)
   int kernels_per_pass;
   int tc;   // bf16 GEMVs on the tensor-core path (contexts with many rows per pass)
+  int KO;   // lookaheads with a position-aware draft offset = min(K, ND)
+  int pad0;
   unsigned long long seed;
   unsigned long long cond;            // graph conditional handle of the pass loop (0 = none)
   long long layer_bytes, head_bytes;  // algorithmic bytes per layer / per lm_head
@@ -111,6 +113,7 @@ struct FrameParams {
   const void* w_gate[CP_SPEC_MAX_LAYERS];
   const void* w_up[CP_SPEC_MAX_LAYERS];
   const void* w_down[CP_SPEC_MAX_LAYERS];
+  const float* draft_offset;  // [K][H] b_1..b_K (read by the offset table kernel only)
   // workspace (row slot r = b * NS + k)
   float* h;        // [Bmax*NS][H]     residual stream
   float* qbuf;     // [Bmax*NS][nq*d]  queries after RoPE
@@ -118,6 +121,7 @@ struct FrameParams {
   float* fbuf;     // [Bmax*NS][F]     SwiGLU activations
   float* kv;       // [Bmax][L][2][G][nkv][d]
   float* logits;   // [Bmax*NS][1+ND][V]
+  float* otab;     // [G-1][KO][V]     head_j . b_t, added to the lookahead-t draft logits
   int* lidx;       // [Bmax*NS][1+ND][KC]
   float* lprob;    // [Bmax*NS][1+ND][KC]
   int* lcount;     // [Bmax*NS][1+ND]
@@ -157,13 +161,14 @@ inline __host__ __device__ size_t accept_scratch_bytes(int NS, int KC) {
 
 // Workspace carve-up, computed identically by the host for sizing.
 struct Layout {
-  size_t h, qbuf, abuf, fbuf, kv, logits, lidx, lprob, lcount, qidx, qprob, qcount, row_pos, row_code, prow, ppos,
+  size_t h, qbuf, abuf, fbuf, kv, logits, otab, lidx, lprob, lcount, qidx, qprob, qcount, row_pos, row_code, prow, ppos,
       pcode, plan, st, sstats, rope, top_k, temp, ctl, call, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline Layout make_layout(int H, int L, int nq, int nkv, int d, int F, int V, int G, int N, int KC, int Bmax) {
+inline Layout make_layout(int H, int L, int nq, int nkv, int d, int F, int V, int G, int N, int KC, int Bmax,
+                          int KO) {
   const int NS = N > 2 ? N : 2, ND = N > 1 ? N - 1 : 0, NDq = ND > 0 ? ND : 1;
   const size_t rows = (size_t)Bmax * NS;
   Layout o{};
@@ -175,6 +180,7 @@ inline Layout make_layout(int H, int L, int nq, int nkv, int d, int F, int V, in
   o.fbuf = take(4 * rows * F);
   o.kv = take(4 * (size_t)Bmax * L * 2 * G * nkv * d);
   o.logits = take(4 * rows * (1 + ND) * V);
+  o.otab = take(4 * (size_t)(G - 1) * KO * V);
   o.lidx = take(sizeof(int) * rows * (1 + ND) * KC);
   o.lprob = take(sizeof(float) * rows * (1 + ND) * KC);
   o.lcount = take(sizeof(int) * rows * (1 + ND));

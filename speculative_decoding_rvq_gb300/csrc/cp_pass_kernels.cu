@@ -319,6 +319,9 @@ __device__ __forceinline__ void gemv_out(const FrameParams& P, int l, const int*
   } else {
     const int hi = u / P.V, v = u - hi * P.V;
     const int slot = heads[hi] - pos;
+    // a lookahead-t draft with a position-aware offset reads head_j on
+    // h + b_t = head_j . h + head_j . b_t (the second term from the table)
+    if (slot >= 1 && slot <= P.KO) y0 += __ldg(&P.otab[((size_t)(heads[hi] - 1) * P.KO + slot - 1) * P.V + v]);
     if (pos >= 1 && slot >= 0 && slot <= P.ND) P.logits[((size_t)r * (1 + P.ND) + slot) * P.V + v] = y0;
   }
 }
@@ -1736,6 +1739,43 @@ __global__ void init_tables_kernel(float2* rope, int G, int d, double theta, int
   }
 }
 
+// Position-aware draft offsets ("RVQ Position Aware Speculative Decoding for
+// On Device TTS", section 2.2): the draft of lookahead t applies head_j to
+// h + b_t.  The product is linear, so head_j . b_t is formed once per
+// context: otab[j-1][t-1][v] = sum_k head_j[v][k] b_t[k], one warp per
+// (head, vocabulary row), fp32 accumulation in a fixed order.
+template <typename WT>
+__global__ void __launch_bounds__(256) offset_table_kernel(const void* head, const float* b, float* otab, int G,
+                                                            int V, int H, int KO) {
+  constexpr int kMaxKO = CP_SPEC_MAX_WINDOW - 1;
+  const int lane = threadIdx.x & 31;
+  const long long nwarps = (long long)gridDim.x * (blockDim.x / 32);
+  for (long long w = (long long)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32; w < (long long)(G - 1) * V;
+       w += nwarps) {
+    const size_t row = (size_t)w * H;  // head j = w / V + 1, vocabulary row v = w % V
+    float acc[kMaxKO];
+#pragma unroll
+    for (int t = 0; t < kMaxKO; ++t) acc[t] = 0.0f;
+    for (int k = lane; k < H; k += 32) {
+      const float x = WTraits<WT>::load1(head, row + k);
+#pragma unroll
+      for (int t = 0; t < kMaxKO; ++t)
+        if (t < KO) acc[t] = fmaf(x, __ldg(&b[(size_t)t * H + k]), acc[t]);
+    }
+#pragma unroll
+    for (int t = 0; t < kMaxKO; ++t) {
+      float a = acc[t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+      acc[t] = a;
+    }
+    if (lane == 0) {
+      const int hj = (int)(w / V), v = (int)(w % V);
+      for (int t = 0; t < KO; ++t) otab[((size_t)hj * KO + t) * V + v] = acc[t];
+    }
+  }
+}
+
 }  // namespace cpk
 
 // ------------------------------------------------------------ host side
@@ -1913,6 +1953,18 @@ cudaError_t build_call_graph(FrameParams P, int sms, int accept_warps, cudaStrea
 cudaError_t launch_init_tables(float2* rope, int G, int d, double theta, int* top_k, float* temp, int Bmax, int k,
                                float T, cudaStream_t stream) {
   cpk::init_tables_kernel<<<8, 256, 0, stream>>>(rope, G, d, theta, top_k, temp, Bmax, k, T);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_offset_table(const FrameParams& P, cudaStream_t stream) {
+  if (P.KO <= 0) return cudaSuccess;
+  if (P.KO > CP_SPEC_MAX_WINDOW - 1 || !P.draft_offset) return cudaErrorInvalidValue;
+  const long long warps = (long long)(P.G - 1) * P.V;
+  const int blocks = (int)((warps + 7) / 8 < 65535 ? (warps + 7) / 8 : 65535);
+  if (P.dtype == 1)
+    cpk::offset_table_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(P.head, P.draft_offset, P.otab, P.G, P.V, P.H, P.KO);
+  else
+    cpk::offset_table_kernel<float><<<blocks, 256, 0, stream>>>(P.head, P.draft_offset, P.otab, P.G, P.V, P.H, P.KO);
   return cudaGetLastError();
 }
 

@@ -25,6 +25,7 @@ cudaError_t build_call_graph(cpk::FrameParams P, int sms, int accept_warps, cuda
 size_t accept_smem(const cpk::FrameParams& P, int warps);
 cudaError_t launch_init_tables(float2* rope, int G, int d, double theta, int* top_k, float* temp, int Bmax, int k,
                                float T, cudaStream_t stream);
+cudaError_t launch_offset_table(const cpk::FrameParams& P, cudaStream_t stream);
 cudaError_t launch_accept_batch(int R, int N, int V, int k, float T, unsigned long long seed, int mode,
                                 const float* tgt, const float* drf, int* tokens, int* nacc, int* drafts,
                                 cudaStream_t stream);
@@ -100,6 +101,8 @@ cp_spec_status validate(const cp_spec_model* m, const cp_spec_config* cfg, cp_sp
   const float T = cfg->temperature;
   if (!(T == 0.0f || (T >= 1e-3f && T <= 100.0f))) return fail(c, CP_SPEC_E_INVALID, "temperature must be 0 or in [1e-3, 100]");
   if (cfg->max_streams < 1) return fail(c, CP_SPEC_E_INVALID, "max_streams must be >= 1");
+  if (cfg->draft_offsets < 0 || cfg->draft_offsets > CP_SPEC_MAX_WINDOW - 1)
+    return fail(c, CP_SPEC_E_INVALID, "draft_offsets must be in [0, %d]", CP_SPEC_MAX_WINDOW - 1);
   return CP_SPEC_OK;
 }
 
@@ -116,17 +119,26 @@ int list_capacity(const cp_spec_model* m, const cp_spec_config* cfg) {
   return (k + 3) / 4 * 4;
 }
 
+// Lookaheads that carry a position-aware draft offset: offsets beyond the
+// drafted depths (N - 1) are never read.
+int offset_lookaheads(const cp_spec_config* cfg, int N) {
+  const int ND = N > 1 ? N - 1 : 0;
+  return cfg->draft_offsets < ND ? cfg->draft_offsets : ND;
+}
+
 cpk::Layout layout_for(const cp_spec_model* m, const cp_spec_config* cfg, int N) {
   const int KC = list_capacity(m, cfg);
   return cpk::make_layout(m->hidden, m->n_layers, m->n_q_heads, m->n_kv_heads, m->head_dim, m->ffn, m->vocab,
-                          m->num_code_groups, N, KC, cfg->max_streams);
+                          m->num_code_groups, N, KC, cfg->max_streams, offset_lookaheads(cfg, N));
 }
 
 template <typename T>
 T* at(unsigned char* base, size_t off) { return reinterpret_cast<T*>(base + off); }
 
-cp_spec_status check_weights(const cp_spec_model* model, const cp_spec_weights* weights) {
+cp_spec_status check_weights(const cp_spec_model* model, const cp_spec_config* config, const cp_spec_weights* weights) {
   if (!weights) return fail(nullptr, CP_SPEC_E_INVALID, "weights is null");
+  if (config->draft_offsets > 0 && (!weights->draft_offset || !aligned16(weights->draft_offset)))
+    return fail(nullptr, CP_SPEC_E_INVALID, "draft_offsets > 0 needs a 16-byte aligned draft_offset pointer");
   const void* ptrs[] = {weights->embed, weights->lm_head, weights->final_norm};
   for (const void* p : ptrs)
     if (!p || !aligned16(p)) return fail(nullptr, CP_SPEC_E_INVALID, "embed/lm_head/final_norm null or not 16-byte aligned");
@@ -215,6 +227,7 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
   P.N = N; P.NS = NS; P.ND = N > 1 ? N - 1 : 0; P.KC = dp.KC;
   P.Bmax = config->max_streams;
   P.kernels_per_pass = 5 * L + 3;
+  P.KO = offset_lookaheads(config, N);
   // bf16 contexts with many rows per pass run the GEMVs on tensor cores
   // (every GEMV width a multiple of 32); the choice depends on the context,
   // not on the pass, so a stream's results do not depend on its batch-mates
@@ -233,8 +246,10 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
     P.wv[l] = weights->wv[l]; P.wo[l] = weights->wo[l]; P.ffn_norm[l] = weights->ffn_norm[l];
     P.w_gate[l] = weights->w_gate[l]; P.w_up[l] = weights->w_up[l]; P.w_down[l] = weights->w_down[l];
   }
+  P.draft_offset = P.KO > 0 ? weights->draft_offset : nullptr;
   P.h = at<float>(ws, lay.h); P.qbuf = at<float>(ws, lay.qbuf); P.abuf = at<float>(ws, lay.abuf);
   P.fbuf = at<float>(ws, lay.fbuf); P.kv = at<float>(ws, lay.kv); P.logits = at<float>(ws, lay.logits);
+  P.otab = at<float>(ws, lay.otab);
   P.lidx = at<int>(ws, lay.lidx); P.lprob = at<float>(ws, lay.lprob); P.lcount = at<int>(ws, lay.lcount);
   P.qidx = at<int>(ws, lay.qidx); P.qprob = at<float>(ws, lay.qprob); P.qcount = at<int>(ws, lay.qcount);
   P.row_pos = at<int>(ws, lay.row_pos); P.row_code = at<int>(ws, lay.row_code);
@@ -351,7 +366,7 @@ cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* w
   *out = nullptr;
   cp_spec_status v = validate(model, config, nullptr);
   if (v != CP_SPEC_OK) return v;
-  v = check_weights(model, weights);
+  v = check_weights(model, config, weights);
   if (v != CP_SPEC_OK) return v;
   if (!d_workspace || !aligned16(d_workspace)) return fail(nullptr, CP_SPEC_E_INVALID, "workspace null or not 16-byte aligned");
   const int N = effective_window(model, config);
@@ -388,13 +403,14 @@ cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* w
   if (e == cudaSuccess)
     e = cpk_host::launch_init_tables(P.rope, P.G, P.d, (double)model->rope_theta, P.top_k, P.temp, config->max_streams,
                                      config->top_k, config->temperature, 0);
+  if (e == cudaSuccess && P.KO > 0) e = cpk_host::launch_offset_table(P, 0);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     cp_spec_status s = check_cuda(nullptr, e, "workspace initialisation");
     delete c;
     return s;
   }
-  c->launches += 1;
+  c->launches += P.KO > 0 ? 2 : 1;
   *out = c;
   if (N != window_of(config)) {
     c->err = "speculation disabled: fewer than 3 code groups leave no draft slot; running the autoregressive loop";
@@ -528,7 +544,7 @@ cp_spec_status cp_spec_decode_frames_static(const cp_spec_model* model, const cp
                                             int32_t* d_codes, int32_t* d_status, void* stream) {
   cp_spec_status v = validate(model, config, nullptr);
   if (v != CP_SPEC_OK) return v;
-  v = check_weights(model, weights);
+  v = check_weights(model, config, weights);
   if (v != CP_SPEC_OK) return v;
   if (n_streams < 1 || n_streams > config->max_streams)
     return fail(nullptr, CP_SPEC_E_INVALID, "n_streams out of [1, max_streams]");
@@ -564,6 +580,7 @@ cp_spec_status cp_spec_decode_frames_static(const cp_spec_model* model, const cp
   if (e == cudaSuccess)
     e = cpk_host::launch_init_tables(P.rope, P.G, P.d, (double)model->rope_theta, P.top_k, P.temp, config->max_streams,
                                      config->top_k, config->temperature, s);
+  if (e == cudaSuccess && P.KO > 0) e = cpk_host::launch_offset_table(P, s);
   if (e != cudaSuccess) return check_cuda(nullptr, e, "static scratch initialisation");
   v = put_call(nullptr, P, ca, s);
   if (v != CP_SPEC_OK) return v;
@@ -576,7 +593,7 @@ cp_spec_status cp_spec_decode_frames_static(const cp_spec_model* model, const cp
     e = cudaMemcpyAsync(d_status, &P.ctl->status, sizeof(int32_t), cudaMemcpyDeviceToDevice, s);
     if (e != cudaSuccess) return check_cuda(nullptr, e, "status copy");
   }
-  g_free_launches.fetch_add(3);
+  g_free_launches.fetch_add(P.KO > 0 ? 4 : 3);
   if (N != window_of(config)) {
     fail(nullptr, CP_SPEC_W_AR_FALLBACK,
          "speculation disabled: fewer than 3 code groups leave no draft slot; running the autoregressive loop");

@@ -56,6 +56,30 @@ def test_workspace_bytes_validates(lib):
     assert many > 32 * one // 2
 
 
+def test_draft_offsets_validate_and_size_the_workspace(lib):
+    """K position-aware offsets: 0..7 accepted; the head . b table is sized by
+    min(K, N - 1) lookaheads, and nothing is reserved without drafts."""
+    from speculative_decoding_rvq_gb300 import binding as b, synth as S
+    spec = S.TTS06B_BF16
+    m = b.model_struct(spec)
+    ws = lambda **kw: lib.cp_spec_workspace_bytes(C.byref(m), C.byref(_cfg(b, **kw)))
+    for bad in (-1, 8):
+        assert ws(draft_offsets=bad) == 0, bad
+    table = (spec.num_code_groups - 1) * spec.vocab * 4
+    base = ws(verify_window=4)
+    for K, used in ((1, 1), (3, 3), (7, 3)):
+        grown = ws(verify_window=4, draft_offsets=K) - base
+        assert used * table <= grown < used * table + 512, (K, grown)
+    assert ws(verify_window=0, draft_offsets=3) == ws(verify_window=0)
+    # K > 0 with a null offset pointer is rejected before any device call
+    w = b.weights_struct(b.weights_to_device(S.TINY_FP32, S.gen_weights(S.TINY_FP32, 0), device="cpu"))
+    mt = b.model_struct(S.TINY_FP32)
+    ctx = C.c_void_p()
+    rc = lib.cp_spec_init(C.byref(mt), C.byref(w), C.byref(_cfg(b, draft_offsets=2)), C.c_void_p(16), 1 << 30,
+                          C.byref(ctx))
+    assert rc == b.E_INVALID and b"draft_offset" in lib.cp_spec_last_error(None)
+
+
 def test_init_rejects_on_host(lib):
     from speculative_decoding_rvq_gb300 import binding as b, synth as S
     m = b.model_struct(S.TINY_FP32)

@@ -48,15 +48,18 @@ def _gpu():
 
 
 @pytest.mark.gpu
-@pytest.mark.parametrize("which", ["tiny_fp32_3streams", "bf16_0p6b_1stream"])
+@pytest.mark.parametrize("which", ["tiny_fp32_3streams", "bf16_0p6b_1stream", "tiny_fp32_offsets"])
 def test_static_matches_context_decode_twice(which):
     _gpu()
     from speculative_decoding_rvq_gb300 import binding, synth as S
-    if which == "tiny_fp32_3streams":
-        spec, B, F, N, k, T = S.TINY_FP32, 3, 6, 3, 20, 0.9
-    else:
+    if which == "bf16_0p6b_1stream":
         spec, B, F, N, k, T = S.TTS06B_BF16, 1, 4, 4, 50, 0.9
-    dw = binding.weights_to_device(spec, S.gen_weights(spec, 0))
+    else:
+        spec, B, F, N, k, T = S.TINY_FP32, 3, 6, 3, 20, 0.9
+    w = S.gen_weights(spec, 0)
+    if which == "tiny_fp32_offsets":  # position-aware draft offsets: the static call forms head . b itself
+        w["draft_offset"] = S.gen_draft_offsets(spec, 3, seed=1, std=1.0)
+    dw = binding.weights_to_device(spec, w)
     status = torch.full((4,), 123, dtype=torch.int32, device="cuda")
     for call, (seed, first) in enumerate(((11, 0), (12, F))):
         x, c0 = S.gen_frames(spec, B, F, seed=seed)
