@@ -160,10 +160,9 @@ __device__ __forceinline__ TileRuns tile_runs(const FrameParams& P, int kind, in
   return r;
 }
 
-// Tiles of this CTA's share [U*c/grid, U*(c+1)/grid) of `kind`: at most
-// `upt` units each, none crossing a head boundary (QKV, lm_heads).
-__device__ int make_tiles(int U, int upt, int period, Tile* out) {
-  const int c = blockIdx.x, g = gridDim.x;
+// Tiles of share c of g, units [U*c/g, U*(c+1)/g) of a kind: at most `upt`
+// units each, none crossing a head boundary (QKV, lm_heads).
+__device__ int make_tiles(int U, int upt, int period, int c, int g, Tile* out) {
   const int u0 = (int)(((long long)U * c) / g), u1 = (int)(((long long)U * (c + 1)) / g);
   int n = 0;
   for (int u = u0; u < u1;) {
@@ -333,6 +332,7 @@ struct GemvShared {
   int ntiles;
   int heads[kMaxHeadsPerPass];
   int issued;                 // tiles whose copies were issued
+  int blk0, blk1;             // tensor path: the CTA's blocks of 16 pass rows
   ActRow src[kRedQ];
   float ss[kWarps][kRedQ];    // RMSNorm partial sums of squares per warp
 };
@@ -592,12 +592,15 @@ constexpr int kTcYFloats = kWarps * 16 * kTcYCols + kWarps * 16 * (int)(sizeof(A
 // there is one) against pass rows [m0, m0 + 16) by one warp: one MMA chain
 // over K per 8-row n-tile, the inputs loaded and split once for both tiles;
 // then the outputs of the tiles' units for those rows.  src: the warp's 16
-// input rows (rows past nrows repeat the last); inv: RMSNorm scales of all
-// pass rows (null when not normed).
+// input rows (rows past nrows repeat the last).  Normed kinds (gain set):
+// RMSNorm(x) . w = inv(x) * sum_k (x_k g_k) w_k, so the MMAs take x * g and
+// the row's sum of squares is accumulated in the same pass over K (per lane
+// in element order, then over the 4 lanes of a row in a fixed order); the
+// scale inv = 1 / sqrt(mean(x^2) + eps) multiplies the accumulators.
 template <int KIND, int NTT>
 __device__ __noinline__ void tc_block(const FrameParams& P, int l, const int* heads, const PassRows& pr,
                                          const float2* rope, const unsigned char* tp0, const unsigned char* tp1,
-                                         Tile tl0, Tile tl1, int nt0, int K, const ActRow* src, const float* inv,
+                                         Tile tl0, Tile tl1, int nt0, int K, const ActRow* src,
                                          const float* gain, int m0, int nrows, float* y) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int rpu = rows_per_unit(KIND);
@@ -607,7 +610,7 @@ __device__ __noinline__ void tc_block(const FrameParams& P, int l, const int* he
 #pragma unroll
   for (int j = 0; j < NTT; ++j) c[j][0] = c[j][1] = c[j][2] = c[j][3] = 0.0f;
   const ActRow ra = src[g], rb = src[g + 8];
-  const float ia = inv ? inv[min(m0 + g, nrows - 1)] : 1.0f, ib = inv ? inv[min(m0 + g + 8, nrows - 1)] : 1.0f;
+  float ssa = 0.0f, ssb = 0.0f;
   // weight row of n-tile j for this lane, as a byte offset from tp0 (the
   // second slot follows the first)
   uint32_t wr[NTT];
@@ -639,8 +642,10 @@ __device__ __noinline__ void tc_block(const FrameParams& P, int l, const int* he
 #pragma unroll
         for (int e = 0; e < 8; ++e) {
           const float gk = gain[k0 + e];
-          va[e] = va[e] * ia * gk;
-          vb[e] = vb[e] * ib * gk;
+          ssa = fmaf(va[e], va[e], ssa);
+          ssb = fmaf(vb[e], vb[e], ssb);
+          va[e] *= gk;
+          vb[e] *= gk;
         }
       }
       uint32_t ah[2][4], al[2][4];
@@ -659,6 +664,20 @@ __device__ __noinline__ void tc_block(const FrameParams& P, int l, const int* he
         mma_bf16_16816(c[j], ah[1][0], ah[1][1], ah[1][2], ah[1][3], w.z, w.w);
         mma_bf16_16816(c[j], al[1][0], al[1][1], al[1][2], al[1][3], w.z, w.w);
       }
+    }
+  }
+  if (gain != nullptr) {
+    ssa += __shfl_xor_sync(0xffffffffu, ssa, 1);
+    ssb += __shfl_xor_sync(0xffffffffu, ssb, 1);
+    ssa += __shfl_xor_sync(0xffffffffu, ssa, 2);
+    ssb += __shfl_xor_sync(0xffffffffu, ssb, 2);
+    const float ia = 1.0f / sqrtf(ssa / (float)K + P.eps), ib = 1.0f / sqrtf(ssb / (float)K + P.eps);
+#pragma unroll
+    for (int j = 0; j < NTT; ++j) {
+      c[j][0] *= ia;
+      c[j][1] *= ia;
+      c[j][2] *= ib;
+      c[j][3] *= ib;
     }
   }
   // C fragment: c[j][0..1] = row g, cols 8j + 2t, +1; c[j][2..3] = row g + 8
@@ -686,36 +705,20 @@ __device__ __noinline__ void tc_block(const FrameParams& P, int l, const int* he
   __syncwarp();
 }
 
-// The tensor-core GEMV of one kind for all rows of the pass (bf16 weights):
-// tiles in resident pairs (both slots); per pair, warp w takes row blocks
-// w, w + kWarps, ... of 16 rows, so each row block's inputs are read and
-// split once per pair.
+// The tensor-core GEMV of one kind for the CTA's blocks of 16 pass rows
+// [blk0, blk1) (bf16 weights): tiles in resident pairs (both slots); per
+// pair, warp w takes blocks blk0 + w, blk0 + w + kWarps, ..., so each block's
+// inputs are read and split once per pair.
 template <int KIND>
 __device__ __forceinline__ bool gemv_tc(const FrameParams& P, const CallArgs& ca, int l, GemvShared& sh,
                                         const PassRows& pr, const float2* rope, unsigned char* slots, float* ybuf,
-                                        float* s_inv, int nrows, const float* gain) {
+                                        int nrows, const float* gain) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = gemv_K(P, KIND);
   const int rpu = rows_per_unit(KIND);
-  // RMSNorm scales of every row, one warp per row
-  if (gain != nullptr)
-    for (int i = warp; i < nrows; i += kWarps) {
-      const ActRow a = act_row<__nv_bfloat16>(P, ca, pr, KIND, l, i);
-      float ss = 0.0f;
-      for (int k = 8 * lane; k < K; k += 256) {
-        float v[8];
-        load_act8(a, k, v);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) ss = fmaf(v[e], v[e], ss);
-      }
-      ss = warp_sum(ss);
-      if (lane == 0) s_inv[i] = 1.0f / sqrtf(ss / (float)K + P.eps);
-    }
-  __syncthreads();
   float* y = ybuf + (size_t)warp * 16 * kTcYCols;
   ActRow* src = reinterpret_cast<ActRow*>(ybuf + (size_t)kWarps * 16 * kTcYCols) + warp * 16;  // 16 row descriptors per warp
-  const int nblk = (nrows + 15) / 16;
-  const float* inv = gain ? s_inv : nullptr;
+  const int nblk = min((nrows + 15) / 16, sh.blk1);
   bool ok = true;
   for (int t0 = 0; t0 < sh.ntiles; t0 += 2) {
     const bool two = t0 + 1 < sh.ntiles;
@@ -724,12 +727,12 @@ __device__ __forceinline__ bool gemv_tc(const FrameParams& P, const CallArgs& ca
     if (two && !mbar_wait_bounded(&sh.full[1], (uint32_t)(t0 >> 1) & 1u, &P.ctl->status, kTileTimeoutNs)) ok = false;
     if (ok) {
       const int nt0 = (tl0.n * rpu + 7) / 8, ntt = nt0 + (tl1.n * rpu + 7) / 8;
-      for (int mb = warp; mb < nblk; mb += kWarps) {
+      for (int mb = sh.blk0 + warp; mb < nblk; mb += kWarps) {
         const int m0 = mb * 16;
         if (lane < 16) src[lane] = act_row<__nv_bfloat16>(P, ca, pr, KIND, l, min(m0 + lane, nrows - 1));
         __syncwarp();
 #define CP_TC(N_) \
-  tc_block<KIND, N_>(P, l, sh.heads, pr, rope, slots, slots + kSlotBytes, tl0, tl1, nt0, K, src, inv, gain, m0, nrows, y)
+  tc_block<KIND, N_>(P, l, sh.heads, pr, rope, slots, slots + kSlotBytes, tl0, tl1, nt0, K, src, gain, m0, nrows, y)
         switch (ntt) {
           case 1: CP_TC(1); break;
           case 2: CP_TC(2); break;
@@ -756,8 +759,8 @@ __device__ __forceinline__ bool gemv_tc(const FrameParams& P, const CallArgs& ca
 template <typename WT, int KIND>
 __device__ __forceinline__ bool gemv_tc_any(const FrameParams& P, const CallArgs& ca, int l, GemvShared& sh,
                                             const PassRows& pr, const float2* rope, unsigned char* slots, float* ybuf,
-                                            float* s_inv, int nrows, const float* gain) {
-  if constexpr (WTraits<WT>::EB == 2) return gemv_tc<KIND>(P, ca, l, sh, pr, rope, slots, ybuf, s_inv, nrows, gain);
+                                            int nrows, const float* gain) {
+  if constexpr (WTraits<WT>::EB == 2) return gemv_tc<KIND>(P, ca, l, sh, pr, rope, slots, ybuf, nrows, gain);
   return false;  // fp32 weights never take the tensor path
 }
 
@@ -821,7 +824,6 @@ __global__ void __launch_bounds__(kThreads, TC ? 1 : 2) gemv_kernel(const __grid
   // rows' RMSNorm scales
   float* s_gain = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(s_rope) + kRopeSmemBytes);
   float* s_tcy = s_gain + (P.H + 3) / 4 * 4;
-  float* s_tcinv = s_tcy + kTcYFloats;
   const float* gain_g = KIND == kQKV ? P.attn_norm[l] : (KIND == kGU ? P.ffn_norm[l] : (KIND == kHeads ? P.final_norm : nullptr));
   // Before the dependency wait: everything that does not come from the
   // previous kernels of the pass (weight tiles, call arguments, the pass
@@ -832,8 +834,32 @@ __global__ void __launch_bounds__(kThreads, TC ? 1 : 2) gemv_kernel(const __grid
       nheads = min(__ldcg(&P.plan->nheads), kMaxHeadsPerPass);
       for (int i = 0; i < nheads; ++i) sh.heads[i] = __ldcg(&P.plan->heads[i]);
     }
+    s_nrows = min(__ldcg(&P.plan->nrows), rows_cap);
     const int period = KIND == kQKV ? P.d / 2 : (KIND == kHeads ? P.V : 0);
-    int n = make_tiles(gemv_units(P, KIND, nheads), upt, period, sh.tiles);
+    const int U = gemv_units(P, KIND, nheads);
+    // Share of the output units.  On the tensor path, when there are fewer
+    // tile pairs than CTAs, the CTAs also split the pass's blocks of 16 rows
+    // S ways (S CTAs per unit share), so that each CTA reads and splits 1/S
+    // of the input rows; an output element is still one warp's MMA chain.
+    int c = blockIdx.x, g = gridDim.x;
+    sh.blk0 = 0;
+    sh.blk1 = 1 << 30;
+    if (TC) {
+      const int nblk = (s_nrows + 15) / 16;
+      const int pairs = max(1, ((U + upt - 1) / upt + 1) / 2);
+      const int S = max(1, min(g / pairs, nblk));
+      const int NG = g / S;
+      if (c < NG * S) {
+        const int rs = c / NG;
+        sh.blk0 = (nblk * rs) / S;
+        sh.blk1 = (nblk * (rs + 1)) / S;
+        c -= rs * NG;
+        g = NG;
+      } else {
+        c = -1;  // spare CTA: no share
+      }
+    }
+    int n = c < 0 ? 0 : make_tiles(U, upt, period, c, g, sh.tiles);
     if (n < 0) { raise_status(&P.ctl->status, kStatusDevice); n = 0; }
     sh.ntiles = n;
     sh.issued = 0;
@@ -842,7 +868,6 @@ __global__ void __launch_bounds__(kThreads, TC ? 1 : 2) gemv_kernel(const __grid
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     for (int t = 0; t < min(n, 2); ++t) gemv_issue<WT, KIND>(P, l, sh, slots, t);
     s_ca = *P.call;
-    s_nrows = min(__ldcg(&P.plan->nrows), rows_cap);
   }
   __syncthreads();
   const int nrows = s_nrows;
@@ -876,7 +901,7 @@ __global__ void __launch_bounds__(kThreads, TC ? 1 : 2) gemv_kernel(const __grid
   const int ngroups = (nrows + NQG - 1) / NQG;
   bool ok = true;
   if constexpr (TC) {
-    if (nrows > 0) ok = gemv_tc_any<WT, KIND>(P, ca, l, sh, pr, rope, slots, s_tcy, s_tcinv, nrows, gain);
+    if (nrows > 0) ok = gemv_tc_any<WT, KIND>(P, ca, l, sh, pr, rope, slots, s_tcy, nrows, gain);
   } else if (ngroups <= 1 || ntiles <= 2) {
     for (int gq = 0; gq < ngroups && ok; ++gq)
       ok = gemv_dispatch<WT, KIND>(P, ca, l, G, sh, pr, rope, slots, red, gq * NQG, min(NQG, nrows - gq * NQG), 0,
@@ -1814,9 +1839,8 @@ size_t gemv_smem(const FrameParams& P, int kind) {
   // per kind so that consecutive kernels' CTAs fit on one SM together.
   size_t b = 2 * (size_t)cpk::kSlotBytes + cpk::kRedFloats * sizeof(float) +
              ((3 * (size_t)P.Bmax * P.NS + 3) / 4 * 4) * sizeof(int);
-  if (P.tc)  // every region, then the tensor path's output blocks and the rows' RMSNorm scales
-    return b + cpk::kRopeSmemBytes + (size_t)(P.H + 3) / 4 * 4 * sizeof(float) + cpk::kTcYFloats * sizeof(float) +
-           (size_t)P.Bmax * P.NS * sizeof(float);
+  if (P.tc)  // every region, then the tensor path's output blocks and row descriptors
+    return b + cpk::kRopeSmemBytes + (size_t)(P.H + 3) / 4 * 4 * sizeof(float) + cpk::kTcYFloats * sizeof(float);
   if (kind == cpk::kQKV || kind == cpk::kGU || kind == cpk::kHeads) b += cpk::kRopeSmemBytes + (size_t)P.H * sizeof(float);
   return b;
 }

@@ -85,3 +85,21 @@ def test_tensor_path_decode_matches_oracle(orc):
     compare_codes_with_margins(g, o, log, 1e-4, max_frac=0.5)
     st = cp.stats()
     assert st["committed"] == B * F * (spec.num_code_groups - 1)
+
+
+def test_tensor_path_row_split_is_batch_invariant(orc):
+    """64 streams x 4 row slots: the O and down GEMVs split each pass's 16-row blocks
+    over 2-3 CTAs per weight tile.  An output element is still one warp's MMA chain over K,
+    so the first 16 streams decode exactly as in a 16-stream context."""
+    from speculative_decoding_rvq_gb300 import synth as S
+    spec = S.TTS06B_BF16
+    B, F = 64, 1
+    x, c0 = S.gen_frames(spec, B, F, seed=19)
+    cp64, _ = _ctx(orc, 4, maxs=64)
+    c64 = cp64.decode_frames(torch.from_numpy(x).cuda(), torch.from_numpy(c0).cuda()).cpu().numpy()
+    cp64.status()
+    cp16, _ = _ctx(orc, 4, maxs=16)
+    c16 = cp16.decode_frames(torch.from_numpy(x[:, :16].copy()).cuda(),
+                             torch.from_numpy(c0[:, :16].copy()).cuda()).cpu().numpy()
+    cp16.status()
+    assert np.array_equal(c64[:, :16], c16)
