@@ -333,6 +333,7 @@ struct GemvShared {
   int heads[kMaxHeadsPerPass];
   int issued;                 // tiles whose copies were issued
   int blk0, blk1;             // tensor path: the CTA's blocks of 16 pass rows
+  int wcnt[kWarps];           // tensor path, lm_heads: rows found per warp (compaction)
   ActRow src[kRedQ];
   float ss[kWarps][kRedQ];    // RMSNorm partial sums of squares per warp
 };
@@ -601,7 +602,7 @@ template <int KIND, int NTT>
 __device__ __noinline__ void tc_block(const FrameParams& P, int l, const int* heads, const PassRows& pr,
                                          const float2* rope, const unsigned char* tp0, const unsigned char* tp1,
                                          Tile tl0, Tile tl1, int nt0, int K, const ActRow* src,
-                                         const float* gain, int m0, int nrows, float* y) {
+                                         const float* gain, int m0, int nrows, const int* rl, float* y) {
   const int lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
   const int rpu = rows_per_unit(KIND);
   const int R0 = tl0.n * rpu, R1 = tl1.n * rpu;
@@ -697,12 +698,41 @@ __device__ __noinline__ void tc_block(const FrameParams& P, int l, const int* he
     for (int it = lane; it < tl.n * rows; it += 32) {
       const int i = it / rows, q = it - i * rows;
       const float y0 = y[q * W + col0 + i], y1 = rpu == 2 ? y[q * W + col0 + i + tl.n] : 0.0f;
+      const int gi = rl != nullptr ? rl[m0 + q] : m0 + q;
       float ho = 0.0f;
-      if (KIND == kO || KIND == kDown) ho = __ldcg(P.h + (size_t)pr.prow[m0 + q] * P.H + tl.u0 + i);
-      gemv_out<KIND>(P, l, heads, pr, rope, tl.u0 + i, m0 + q, y0, y1, ho);
+      if (KIND == kO || KIND == kDown) ho = __ldcg(P.h + (size_t)pr.prow[gi] * P.H + tl.u0 + i);
+      gemv_out<KIND>(P, l, heads, pr, rope, tl.u0 + i, gi, y0, y1, ho);
     }
   }
   __syncwarp();
+}
+
+// The pass rows (compacted indices, ascending) whose logit slots read head
+// h0 or h1: the rows the lm_head epilogue keeps an output of.  Every thread
+// of the CTA takes part.
+__device__ int heads_rows(const FrameParams& P, const PassRows& pr, int nrows, int h0, int h1, int* out, int* wcnt) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int total = 0;
+  for (int base = 0; base < nrows; base += kThreads) {
+    const int i = base + threadIdx.x;
+    bool need = false;
+    if (i < nrows) {
+      const int pos = pr.ppos[i], s0 = h0 - pos, s1 = h1 - pos;
+      need = pos >= 1 && ((s0 >= 0 && s0 <= P.ND) || (s1 >= 0 && s1 <= P.ND));
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, need);
+    if (lane == 0) wcnt[warp] = __popc(bal);
+    __syncthreads();
+    int off = total, sum = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      if (w < warp) off += wcnt[w];
+      sum += wcnt[w];
+    }
+    if (need) out[off + __popc(bal & ((1u << lane) - 1u))] = i;
+    total += sum;
+    __syncthreads();
+  }
+  return total;
 }
 
 // The tensor-core GEMV of one kind for the CTA's blocks of 16 pass rows
@@ -712,27 +742,38 @@ __device__ __noinline__ void tc_block(const FrameParams& P, int l, const int* he
 template <int KIND>
 __device__ __forceinline__ bool gemv_tc(const FrameParams& P, const CallArgs& ca, int l, GemvShared& sh,
                                         const PassRows& pr, const float2* rope, unsigned char* slots, float* ybuf,
-                                        int nrows, const float* gain) {
+                                        int* s_rl, int nrows, const float* gain) {
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int K = gemv_K(P, KIND);
   const int rpu = rows_per_unit(KIND);
   float* y = ybuf + (size_t)warp * 16 * kTcYCols;
   ActRow* src = reinterpret_cast<ActRow*>(ybuf + (size_t)kWarps * 16 * kTcYCols) + warp * 16;  // 16 row descriptors per warp
-  const int nblk = min((nrows + 15) / 16, sh.blk1);
   bool ok = true;
   for (int t0 = 0; t0 < sh.ntiles; t0 += 2) {
     const bool two = t0 + 1 < sh.ntiles;
     const Tile tl0 = sh.tiles[t0], tl1 = two ? sh.tiles[t0 + 1] : Tile{0, 0};
+    // lm_heads: only the rows whose logit slots read the pair's heads (each
+    // row reads 1 + N-1 of the pass's heads); other kinds: every row
+    int nr = nrows;
+    const int* rl = nullptr;
+    if (KIND == kHeads) {
+      nr = heads_rows(P, pr, nrows, sh.heads[tl0.u0 / P.V], sh.heads[(two ? tl1.u0 : tl0.u0) / P.V], s_rl, sh.wcnt);
+      rl = s_rl;
+    }
+    const int nblk = min((nr + 15) / 16, sh.blk1);
     if (!mbar_wait_bounded(&sh.full[0], (uint32_t)(t0 >> 1) & 1u, &P.ctl->status, kTileTimeoutNs)) ok = false;
     if (two && !mbar_wait_bounded(&sh.full[1], (uint32_t)(t0 >> 1) & 1u, &P.ctl->status, kTileTimeoutNs)) ok = false;
     if (ok) {
       const int nt0 = (tl0.n * rpu + 7) / 8, ntt = nt0 + (tl1.n * rpu + 7) / 8;
       for (int mb = sh.blk0 + warp; mb < nblk; mb += kWarps) {
         const int m0 = mb * 16;
-        if (lane < 16) src[lane] = act_row<__nv_bfloat16>(P, ca, pr, KIND, l, min(m0 + lane, nrows - 1));
+        if (lane < 16) {
+          const int q = min(m0 + lane, nr - 1);
+          src[lane] = act_row<__nv_bfloat16>(P, ca, pr, KIND, l, rl != nullptr ? rl[q] : q);
+        }
         __syncwarp();
 #define CP_TC(N_) \
-  tc_block<KIND, N_>(P, l, sh.heads, pr, rope, slots, slots + kSlotBytes, tl0, tl1, nt0, K, src, gain, m0, nrows, y)
+  tc_block<KIND, N_>(P, l, sh.heads, pr, rope, slots, slots + kSlotBytes, tl0, tl1, nt0, K, src, gain, m0, nr, rl, y)
         switch (ntt) {
           case 1: CP_TC(1); break;
           case 2: CP_TC(2); break;
@@ -759,8 +800,8 @@ __device__ __forceinline__ bool gemv_tc(const FrameParams& P, const CallArgs& ca
 template <typename WT, int KIND>
 __device__ __forceinline__ bool gemv_tc_any(const FrameParams& P, const CallArgs& ca, int l, GemvShared& sh,
                                             const PassRows& pr, const float2* rope, unsigned char* slots, float* ybuf,
-                                            int nrows, const float* gain) {
-  if constexpr (WTraits<WT>::EB == 2) return gemv_tc<KIND>(P, ca, l, sh, pr, rope, slots, ybuf, nrows, gain);
+                                            int* s_rl, int nrows, const float* gain) {
+  if constexpr (WTraits<WT>::EB == 2) return gemv_tc<KIND>(P, ca, l, sh, pr, rope, slots, ybuf, s_rl, nrows, gain);
   return false;  // fp32 weights never take the tensor path
 }
 
@@ -824,6 +865,7 @@ __global__ void __launch_bounds__(kThreads, TC ? 1 : 2) gemv_kernel(const __grid
   // rows' RMSNorm scales
   float* s_gain = reinterpret_cast<float*>(reinterpret_cast<unsigned char*>(s_rope) + kRopeSmemBytes);
   float* s_tcy = s_gain + (P.H + 3) / 4 * 4;
+  int* s_rl = reinterpret_cast<int*>(s_tcy + kTcYFloats);  // tensor path, lm_heads: row list
   const float* gain_g = KIND == kQKV ? P.attn_norm[l] : (KIND == kGU ? P.ffn_norm[l] : (KIND == kHeads ? P.final_norm : nullptr));
   // Before the dependency wait: everything that does not come from the
   // previous kernels of the pass (weight tiles, call arguments, the pass
@@ -844,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, TC ? 1 : 2) gemv_kernel(const __grid
     int c = blockIdx.x, g = gridDim.x;
     sh.blk0 = 0;
     sh.blk1 = 1 << 30;
-    if (TC) {
+    if (TC && KIND != kHeads) {
       const int nblk = (s_nrows + 15) / 16;
       const int pairs = max(1, ((U + upt - 1) / upt + 1) / 2);
       const int S = max(1, min(g / pairs, nblk));
@@ -901,7 +943,7 @@ __global__ void __launch_bounds__(kThreads, TC ? 1 : 2) gemv_kernel(const __grid
   const int ngroups = (nrows + NQG - 1) / NQG;
   bool ok = true;
   if constexpr (TC) {
-    if (nrows > 0) ok = gemv_tc_any<WT, KIND>(P, ca, l, sh, pr, rope, slots, s_tcy, nrows, gain);
+    if (nrows > 0) ok = gemv_tc_any<WT, KIND>(P, ca, l, sh, pr, rope, slots, s_tcy, s_rl, nrows, gain);
   } else if (ngroups <= 1 || ntiles <= 2) {
     for (int gq = 0; gq < ngroups && ok; ++gq)
       ok = gemv_dispatch<WT, KIND>(P, ca, l, G, sh, pr, rope, slots, red, gq * NQG, min(NQG, nrows - gq * NQG), 0,
@@ -1839,8 +1881,9 @@ size_t gemv_smem(const FrameParams& P, int kind) {
   // per kind so that consecutive kernels' CTAs fit on one SM together.
   size_t b = 2 * (size_t)cpk::kSlotBytes + cpk::kRedFloats * sizeof(float) +
              ((3 * (size_t)P.Bmax * P.NS + 3) / 4 * 4) * sizeof(int);
-  if (P.tc)  // every region, then the tensor path's output blocks and row descriptors
-    return b + cpk::kRopeSmemBytes + (size_t)(P.H + 3) / 4 * 4 * sizeof(float) + cpk::kTcYFloats * sizeof(float);
+  if (P.tc)  // every region, then the tensor path's output blocks and row descriptors, and a row list
+    return b + cpk::kRopeSmemBytes + (size_t)(P.H + 3) / 4 * 4 * sizeof(float) + cpk::kTcYFloats * sizeof(float) +
+           (size_t)P.Bmax * P.NS * sizeof(int);
   if (kind == cpk::kQKV || kind == cpk::kGU || kind == cpk::kHeads) b += cpk::kRopeSmemBytes + (size_t)P.H * sizeof(float);
   return b;
 }
