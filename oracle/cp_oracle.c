@@ -461,9 +461,9 @@ static void log_round(orc_round_rec* log, int log_cap, int* n_log, int frame, in
 /* One frame of one stream.  Sequence layout: position 0 holds the talker
  * hidden x, position j >= 1 holds E_{j-1}(c_{j-1}); the output at position
  * j is h_j and p_j = proc(head_j . h_j) is the law of c_j. */
-static void decode_one_frame(const orc_model* M, int N, int top_k, float T, uint64_t seed, int stream,
+static void decode_one_frame(const orc_model* M, int N, int w, int top_k, float T, uint64_t seed, int stream,
                              int frame, const float* x, int c0, int* codes, orc_stats* st,
-                             orc_round_rec* log, int log_cap, int* n_log) {
+                             orc_round_rec* log, int log_cap, int* n_log, int64_t* reach, int64_t* acc) {
   const int H = M->H, V = M->V, G = M->G;
   double* kv = (double*)calloc(orc_kv_doubles(M), sizeof(double));
   double* rows = (double*)malloc(sizeof(double) * 9 * H);
@@ -509,7 +509,7 @@ static void decode_one_frame(const orc_model* M, int N, int top_k, float T, uint
   } else {
     while (s < G - 1) {
       const int R = G - 1 - s;
-      const int n_d = (N - 1) < R ? (N - 1) : R;
+      const int n_d = (w - 1) < R ? (w - 1) : R; /* the frame's window w <= N */
       mg = INFINITY;
       /* Draft: head_{s+t} applied to the current hidden h_s (plus the
        * offset b_t where one is given). */
@@ -549,6 +549,10 @@ static void decode_one_frame(const orc_model* M, int N, int top_k, float T, uint
       int na = orc_accept_chain(V, n_d, m, q, dr, p, ua, ut, em, &ne, &m1);
       if (m1 < mg) mg = m1;
       for (int t = 1; t <= na; ++t) st->accepted_by_offset[t]++;
+      /* the window policy's counters: drafts the left-to-right test reached
+       * (up to and including the first rejection) and accepted, by offset */
+      for (int t = 1; t <= n_d && t <= na + 1; ++t) reach[t]++;
+      for (int t = 1; t <= na; ++t) acc[t]++;
       if (ne > na && na < n_d) st->rejections++;
       if (ne > n_d) st->bonus++;
       for (int i = 0; i < ne; ++i) codes[s + 1 + i] = em[i];
@@ -567,18 +571,52 @@ static void decode_one_frame(const orc_model* M, int N, int top_k, float T, uint
   free(kv); free(rows); free(hn); free(hs); free(lg); free(q); free(p);
 }
 
-int orc_decode_frames(const orc_model* M, int N, const int* top_k, const float* temp, uint64_t seed,
-                      int B, int F, int first_frame, const float* x, const int* c0, int* codes,
-                      orc_stats* st, orc_round_rec* log, int log_cap, int* n_log) {
+/* Window of a stream's next frame under the acceptance policy: offsets
+ * t = 1, 2, ... are kept while each either has fewer than min_reached
+ * reached drafts or accepted at least pct percent of them (integer test
+ * 100 * acc >= pct * reach); the window is 1 + the kept leading offsets, at
+ * most N.  Window 1 runs the frame's rounds without drafts (one row per
+ * pass, each code drawn from the target as in the AR loop). */
+int orc_policy_window(int N, int pct, int min_reached, const int64_t* reach, const int64_t* acc) {
+  if (N < 2 || pct <= 0) return N;
+  int w = 1;
+  for (int t = 1; t <= N - 1; ++t) {
+    const int keep = reach[t] < min_reached || 100 * acc[t] >= (int64_t)pct * reach[t];
+    if (!keep) break;
+    w = t + 1;
+  }
+  return w;
+}
+
+int orc_decode_frames_policy(const orc_model* M, int N, const int* top_k, const float* temp, uint64_t seed,
+                             int B, int F, int first_frame, const float* x, const int* c0, int* codes,
+                             orc_stats* st, orc_round_rec* log, int log_cap, int* n_log, int pct,
+                             int min_reached) {
   if (!M || !codes || !x || !c0 || !st) return -1;
   if (!(N == 0 || (N >= 2 && N <= 8))) return -1;
   if (M->G < 2 || M->nq % M->nkv != 0 || M->d % 2 != 0) return -1;
   if (M->K < 0 || (M->K > 0 && !M->draft_offset)) return -1;
+  if (pct < 0 || pct > 100 || (pct > 0 && min_reached < 1)) return -1;
   if (n_log) *n_log = 0;
+  /* per-stream policy counters, from the start of the call */
+  int64_t* reach = (int64_t*)calloc((size_t)(B > 0 ? B : 1) * 9, sizeof(int64_t));
+  int64_t* acc = (int64_t*)calloc((size_t)(B > 0 ? B : 1) * 9, sizeof(int64_t));
   for (int f = 0; f < F; ++f)
-    for (int b = 0; b < B; ++b)
-      decode_one_frame(M, N, top_k[b], temp[b], seed, b, first_frame + f,
+    for (int b = 0; b < B; ++b) {
+      const int w = orc_policy_window(N, pct, min_reached, reach + (size_t)b * 9, acc + (size_t)b * 9);
+      decode_one_frame(M, N, w, top_k[b], temp[b], seed, b, first_frame + f,
                        x + ((size_t)f * B + b) * M->H, c0[(size_t)f * B + b],
-                       codes + ((size_t)f * B + b) * M->G, st, log, log_cap, n_log);
+                       codes + ((size_t)f * B + b) * M->G, st, log, log_cap, n_log,
+                       reach + (size_t)b * 9, acc + (size_t)b * 9);
+    }
+  free(reach);
+  free(acc);
   return 0;
+}
+
+int orc_decode_frames(const orc_model* M, int N, const int* top_k, const float* temp, uint64_t seed,
+                      int B, int F, int first_frame, const float* x, const int* c0, int* codes,
+                      orc_stats* st, orc_round_rec* log, int log_cap, int* n_log) {
+  return orc_decode_frames_policy(M, N, top_k, temp, seed, B, F, first_frame, x, c0, codes, st, log, log_cap,
+                                  n_log, 0, 1);
 }

@@ -143,6 +143,17 @@ void orc_teacher_logits(const orc_model* M, const float* x, const int* codes, in
 int orc_decode_frames(const orc_model* M, int N, const int* top_k, const float* temp, uint64_t seed,
                       int B, int F, int first_frame, const float* x, const int* c0, int* codes,
                       orc_stats* st, orc_round_rec* log, int log_cap, int* n_log);
+/* Adaptive window ("Speculative Decoding, Beyond Text", runtime policies;
+ * "CodePredictor Speculative Decoding", "Options": acceptance flattens past
+ * a few drafts): each stream picks its window for the next frame from its
+ * acceptance by offset so far in the call (orc_policy_window).  pct = 0
+ * turns the policy off (every frame uses N).  The window depends only on
+ * earlier frames, so each frame keeps the autoregressive law. */
+int orc_policy_window(int N, int pct, int min_reached, const int64_t* reach /*[9]*/, const int64_t* acc /*[9]*/);
+int orc_decode_frames_policy(const orc_model* M, int N, const int* top_k, const float* temp, uint64_t seed,
+                             int B, int F, int first_frame, const float* x, const int* c0, int* codes,
+                             orc_stats* st, orc_round_rec* log, int log_cap, int* n_log, int pct,
+                             int min_reached);
 
 #ifdef __cplusplus
 }

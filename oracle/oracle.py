@@ -98,6 +98,11 @@ def lib():
             L.orc_teacher_logits.argtypes = [vp, vp, vp, i32, i32, vp, vp]
             L.orc_decode_frames.argtypes = [vp, i32, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp]
             L.orc_decode_frames.restype = i32
+            L.orc_decode_frames_policy.argtypes = [vp, i32, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp,
+                                                   i32, i32]
+            L.orc_decode_frames_policy.restype = i32
+            L.orc_policy_window.argtypes = [i32, i32, i32, vp, vp]
+            L.orc_policy_window.restype = i32
             _lib = L
     return _lib
 
@@ -246,6 +251,13 @@ class Model:
         lib().orc_head_logits(self.ptr, int(j), _p(hn), _p(o64), _p(o32))
         return o64, o32
 
+    @staticmethod
+    def policy_window(N: int, pct: int, min_reached: int, reach, acc) -> int:
+        r = np.ascontiguousarray(reach, dtype=np.int64)
+        a = np.ascontiguousarray(acc, dtype=np.int64)
+        assert r.shape == (9,) and a.shape == (9,)
+        return int(lib().orc_policy_window(int(N), int(pct), int(min_reached), _p(r), _p(a)))
+
     def draft_logits(self, j: int, t: int, hn: np.ndarray) -> np.ndarray:
         """float32 draft logits of lookahead t read by head_j from the normed hidden hn."""
         hn = np.ascontiguousarray(hn, dtype=np.float64)
@@ -269,8 +281,10 @@ class Model:
         return lg, (dr if n_draft > 0 else None)
 
     def decode_frames(self, N: int, top_k, temperature, seed: int, x: np.ndarray, c0: np.ndarray,
-                      first_frame: int = 0, log_cap: int = 0):
-        """x [F, B, H], c0 [F, B] -> codes [F, B, G], stats dict, round log (structured array)."""
+                      first_frame: int = 0, log_cap: int = 0, adapt_pct: int = 0, adapt_min: int = 16):
+        """x [F, B, H], c0 [F, B] -> codes [F, B, G], stats dict, round log (structured array).
+
+        adapt_pct > 0 turns on the per-stream adaptive window (orc_policy_window)."""
         F, B, H = x.shape
         tk = np.ascontiguousarray(np.broadcast_to(np.asarray(top_k, np.int32), (B,)))
         tp = np.ascontiguousarray(np.broadcast_to(np.asarray(temperature, np.float32), (B,)))
@@ -280,9 +294,9 @@ class Model:
         st = OrcStats()
         log = np.zeros(max(log_cap, 1), ROUND_DTYPE)
         nlog = C.c_int(0)
-        rc = lib().orc_decode_frames(self.ptr, int(N), _p(tk), _p(tp), int(seed), B, F, int(first_frame),
-                                     _p(xx), _p(cc), _p(codes), C.byref(st), _p(log), int(log_cap),
-                                     C.byref(nlog))
+        rc = lib().orc_decode_frames_policy(self.ptr, int(N), _p(tk), _p(tp), int(seed), B, F, int(first_frame),
+                                            _p(xx), _p(cc), _p(codes), C.byref(st), _p(log), int(log_cap),
+                                            C.byref(nlog), int(adapt_pct), int(adapt_min))
         if rc != 0:
             raise ValueError("oracle rejected the decode arguments")
         return codes, st.as_dict(), log[: min(nlog.value, log_cap)]

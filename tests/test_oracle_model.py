@@ -149,13 +149,14 @@ def test_greedy_speculative_equals_greedy_ar(orc, G):
         assert np.all(rounds["n_acc"] <= rounds["n_d"])
 
 
-@pytest.mark.parametrize("K", [0, 2])
-def test_speculative_law_equals_autoregressive_law(orc, K):
+@pytest.mark.parametrize("K,adapt", [(0, 0), (2, 0), (2, 60)])
+def test_speculative_law_equals_autoregressive_law(orc, K, adapt):
     """Exact law of (c_1, c_2, c_3) under AR by enumeration vs speculative frequencies (chi-square).
 
     K = 2 adds position-aware draft offsets: they change only the drafts, so
     the law is the same ("RVQ Position Aware Speculative Decoding for On
-    Device TTS", section 3.2)."""
+    Device TTS", section 3.2).  adapt = 60 lets each frame's window follow the
+    acceptance of the frames before it, which leaves every frame's law exact."""
     spec = S.ModelSpec(hidden=16, n_layers=1, n_q_heads=2, n_kv_heads=1, head_dim=8, ffn=32, vocab=4,
                        num_code_groups=4, dtype=S.DTYPE_F32)
     w = S.gen_weights(spec, seed=21, std=0.5)
@@ -178,7 +179,7 @@ def test_speculative_law_equals_autoregressive_law(orc, K):
     xs = np.broadcast_to(x, (F, 1, spec.hidden)).copy()
     cs = np.broadcast_to(c0, (F, 1)).copy()
     for N in (0, 2, 3, 4):
-        codes, st, _ = m.decode_frames(N, k, T, 77, xs, cs)
+        codes, st, _ = m.decode_frames(N, k, T, 77, xs, cs, adapt_pct=adapt, adapt_min=8)
         cnt = {}
         for row in codes[:, 0, 1:]:
             cnt[tuple(int(v) for v in row)] = cnt.get(tuple(int(v) for v in row), 0) + 1
