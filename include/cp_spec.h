@@ -124,7 +124,19 @@ typedef struct {
  * greedy, else in [1e-3, 100].  max_streams: streams the workspace is sized
  * for (>= 1).  draft_offsets: K, the number of position-aware draft offset
  * vectors in weights.draft_offset, 0..7 (0 = the heads are reused without
- * offsets); offsets beyond verify_window - 1 are never read. */
+ * offsets); offsets beyond verify_window - 1 are never read.
+ * adapt_accept_pct, adapt_min_reached: the adaptive window ("Speculative
+ * Decoding, Beyond Text", runtime policies).  0 = off: every round drafts
+ * min(verify_window - 1, codes left).  With pct in 1..100, each stream picks
+ * the window of its next frame from its acceptance by offset earlier in the
+ * same cp_spec_decode_frames call: offsets t = 1, 2, ... are kept while each
+ * has fewer than adapt_min_reached (>= 1) drafts reached by the left-to-right
+ * test, or accepted at least pct percent of them (100 * accepted >= pct *
+ * reached); the window is 1 + the kept leading offsets.  Window 1 runs the
+ * frame without drafts, one row per pass.  The choice depends only on
+ * earlier frames, so the committed codes keep the autoregressive law.  Each
+ * call (and each cp_spec_begin_frame) starts with no history, i.e. with the
+ * full window. */
 typedef struct {
   int32_t verify_window;
   int32_t top_k;
@@ -132,6 +144,8 @@ typedef struct {
   uint64_t seed;
   int32_t max_streams;
   int32_t draft_offsets;
+  int32_t adapt_accept_pct;
+  int32_t adapt_min_reached;
 } cp_spec_config;
 
 /* Counters accumulated since init (or the last cp_spec_reset_stats).

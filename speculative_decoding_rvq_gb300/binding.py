@@ -48,7 +48,8 @@ class Weights(C.Structure):
 
 class Config(C.Structure):
     _fields_ = [("verify_window", C.c_int32), ("top_k", C.c_int32), ("temperature", C.c_float),
-                ("seed", C.c_uint64), ("max_streams", C.c_int32), ("draft_offsets", C.c_int32)]
+                ("seed", C.c_uint64), ("max_streams", C.c_int32), ("draft_offsets", C.c_int32),
+                ("adapt_accept_pct", C.c_int32), ("adapt_min_reached", C.c_int32)]
 
 
 class Stats(C.Structure):
@@ -160,14 +161,15 @@ class CpSpec:
     """One context of the CUDA library over device-resident weights."""
 
     def __init__(self, spec: synth.ModelSpec, device_weights: dict, verify_window: int, top_k: int,
-                 temperature: float, seed: int, max_streams: int = 1):
+                 temperature: float, seed: int, max_streams: int = 1, adapt_pct: int = 0, adapt_min: int = 16):
         import torch
         self.lib = load()
         self.spec = spec
         self.dw = device_weights
         self.model = model_struct(spec)
         self.weights = weights_struct(device_weights)
-        self.config = Config(verify_window, top_k, temperature, seed, max_streams, n_draft_offsets(device_weights))
+        self.config = Config(verify_window, top_k, temperature, seed, max_streams, n_draft_offsets(device_weights),
+                             adapt_pct, adapt_min)
         nbytes = self.lib.cp_spec_workspace_bytes(C.byref(self.model), C.byref(self.config))
         if nbytes == 0:
             _check(E_INVALID)

@@ -36,9 +36,11 @@ struct StreamState {
   int m;          // rows in the pass in flight
   int pos0;       // position of row 0 of the pass
   int n_d;        // drafts verified by the pass in flight
-  int pad;
+  int w;          // verify window of the current frame (the adaptive policy; N when it is off)
   int drafts[8];
   int codes[CP_SPEC_MAX_CODE_GROUPS];
+  int reach[8];   // drafts at offsets 1..8 the left-to-right test reached in this call
+  int acc[8];     // ... and accepted (the adaptive policy's counters)
 };
 
 struct StreamStats {
@@ -97,6 +99,8 @@ struct FrameParams {
   int kernels_per_pass;
   int tc;   // bf16 GEMVs on the tensor-core path (contexts with many rows per pass)
   int KO;   // lookaheads with a position-aware draft offset = min(K, ND)
+  int adapt_pct;  // adaptive window: keep an offset at >= this acceptance percentage (0 = off)
+  int adapt_min;  // ... or while it has fewer reached drafts than this
   int pad0;
   unsigned long long seed;
   unsigned long long cond;            // graph conditional handle of the pass loop (0 = none)

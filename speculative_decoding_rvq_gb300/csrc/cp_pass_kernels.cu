@@ -1279,6 +1279,26 @@ __device__ __forceinline__ void retire_stream(const FrameParams& P, int b, Strea
 
 // Frame start: rows [x, E_0(c_0)] at positions 0, 1.  Scalar state fields
 // are written by lane 0 only; every all-lane read of them follows a __syncwarp().
+// Verify window of a stream's next frame ("Speculative Decoding, Beyond
+// Text", runtime policies: size the window from measured acceptance by
+// offset, stop drafting when it collapses): offsets t = 1, 2, ... are kept
+// while each has fewer than adapt_min reached drafts in this call or
+// accepted at least adapt_pct percent of them; the window is 1 + the kept
+// leading offsets.  Window 1 runs rounds without drafts (one row per pass,
+// each code drawn from the target).  It depends only on earlier frames, so
+// every frame keeps the autoregressive law.
+__device__ __forceinline__ int frame_window(const FrameParams& P, const StreamState& S) {
+  if (P.N < 2 || P.adapt_pct <= 0) return P.N;
+  int w = 1;
+  for (int t = 1; t <= P.N - 1; ++t) {
+    const int r = S.reach[t - 1], a = S.acc[t - 1];
+    const bool keep = r < P.adapt_min || 100ll * a >= (long long)P.adapt_pct * r;
+    if (!keep) break;
+    w = t + 1;
+  }
+  return w;
+}
+
 template <typename WT>
 __device__ __noinline__ void setup_frame(const FrameParams& P, const CallArgs& ca, int b, StreamState& S, int frame) {
   const int lane = threadIdx.x & 31;
@@ -1293,6 +1313,7 @@ __device__ __noinline__ void setup_frame(const FrameParams& P, const CallArgs& c
     S.pos0 = 0;
     S.m = 2;
     S.n_d = 0;
+    S.w = frame_window(P, S);
     ca.codes_out[((size_t)frame * ca.B + b) * P.G] = c0;
     if (ca.committed_out) ca.committed_out[b] = 1;
   }
@@ -1455,7 +1476,7 @@ __device__ __noinline__ void after_commit(const FrameParams& P, const CallArgs& 
     return;
   }
   const int R = P.G - 1 - s_new;
-  const int n_d = min(P.N - 1, R);
+  const int n_d = min(S.w - 1, R);  // the frame's window (N unless the adaptive policy narrowed it)
   // The draft distributions q_t = proc(head_{s+t} . h_s), t = 1..n_d, are
   // this pass's speculative draft slots on the row at position s_new
   // (already staged with the target lists): draw the drafts (uniforms one
@@ -1602,8 +1623,8 @@ __device__ void accept_stream(const FrameParams& P, const CallArgs& ca, int b, A
     rej = fails ? __ffs(fails) : 0;
     const int reached = rej ? rej : n_d;  // drafts tested
     const int acc = rej ? rej - 1 : n_d;  // drafts accepted
-    if (lane < reached) bump(ss->drafted[lane + 1]);
-    if (lane < acc) { bump(ss->accepted[lane + 1]); S.codes[s + 1 + lane] = S.drafts[lane]; }
+    if (lane < reached) { bump(ss->drafted[lane + 1]); S.reach[lane] += 1; }
+    if (lane < acc) { bump(ss->accepted[lane + 1]); S.acc[lane] += 1; S.codes[s + 1 + lane] = S.drafts[lane]; }
     __syncwarp();
   }
   if (lane == 0) {

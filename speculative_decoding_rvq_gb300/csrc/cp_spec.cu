@@ -103,6 +103,9 @@ cp_spec_status validate(const cp_spec_model* m, const cp_spec_config* cfg, cp_sp
   if (cfg->max_streams < 1) return fail(c, CP_SPEC_E_INVALID, "max_streams must be >= 1");
   if (cfg->draft_offsets < 0 || cfg->draft_offsets > CP_SPEC_MAX_WINDOW - 1)
     return fail(c, CP_SPEC_E_INVALID, "draft_offsets must be in [0, %d]", CP_SPEC_MAX_WINDOW - 1);
+  if (cfg->adapt_accept_pct < 0 || cfg->adapt_accept_pct > 100 ||
+      (cfg->adapt_accept_pct > 0 && cfg->adapt_min_reached < 1))
+    return fail(c, CP_SPEC_E_INVALID, "adapt_accept_pct must be in [0, 100], with adapt_min_reached >= 1 when set");
   return CP_SPEC_OK;
 }
 
@@ -228,6 +231,8 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
   P.Bmax = config->max_streams;
   P.kernels_per_pass = 5 * L + 3;
   P.KO = offset_lookaheads(config, N);
+  P.adapt_pct = config->adapt_accept_pct;
+  P.adapt_min = config->adapt_min_reached;
   // bf16 contexts with many rows per pass run the GEMVs on tensor cores
   // (every GEMV width a multiple of 32); the choice depends on the context,
   // not on the pass, so a stream's results do not depend on its batch-mates

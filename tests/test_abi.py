@@ -58,13 +58,18 @@ def test_workspace_bytes_validates(lib):
 
 def test_draft_offsets_validate_and_size_the_workspace(lib):
     """K position-aware offsets: 0..7 accepted; the head . b table is sized by
-    min(K, N - 1) lookaheads, and nothing is reserved without drafts."""
+    min(K, N - 1) lookaheads, and nothing is reserved without drafts.  The
+    adaptive-window fields are validated on the host and need no workspace."""
     from speculative_decoding_rvq_gb300 import binding as b, synth as S
     spec = S.TTS06B_BF16
     m = b.model_struct(spec)
     ws = lambda **kw: lib.cp_spec_workspace_bytes(C.byref(m), C.byref(_cfg(b, **kw)))
     for bad in (-1, 8):
         assert ws(draft_offsets=bad) == 0, bad
+    # the adaptive window: a percentage in [0, 100], and a sample floor >= 1 when on
+    for bad in (dict(adapt_accept_pct=-1), dict(adapt_accept_pct=101), dict(adapt_accept_pct=50, adapt_min_reached=0)):
+        assert ws(**bad) == 0, bad
+    assert ws(adapt_accept_pct=50, adapt_min_reached=4) == ws()
     table = (spec.num_code_groups - 1) * spec.vocab * 4
     base = ws(verify_window=4)
     for K, used in ((1, 1), (3, 3), (7, 3)):
