@@ -620,3 +620,202 @@ int orc_decode_frames(const orc_model* M, int N, const int* top_k, const float* 
   return orc_decode_frames_policy(M, N, top_k, temp, seed, B, F, first_frame, x, c0, codes, st, log, log_cap,
                                   n_log, 0, 1);
 }
+
+/* ------------------------------------------------------------ sparse tree */
+/* Tree rounds ("RVQ Position Aware Speculative Decoding for On Device TTS",
+ * section 2.2, tree attention and sparse tree attention, Figure 2).  The
+ * drafts of depth t all come from head_{s+t} on h_s (+ b_t), so a node is
+ * named by its depth and the rank of its token among that depth's draft
+ * logits (value descending, index ascending); the tree is a set of such rank
+ * paths, given parents first.  Every node is verified in one pass attending
+ * to the committed prefix and its own ancestors; here each node's output is
+ * computed by a plain causal pass over the prefix cache plus its path, which
+ * is that definition written out.  Acceptance walks down from the committed
+ * code: at a node with target law p, the children are tested in rank order
+ * as drafts with point-mass draft laws (accept child c iff u < p'(c), p' the
+ * residual renormalised over what is left, else remove c), and when none is
+ * accepted, or the node has no child, one code is drawn from what is left
+ * (a correction, or the bonus).  Each draw is then distributed as p, so the
+ * committed codes keep the autoregressive law. */
+
+static int tree_depth(const orc_tree* T, int i) {
+  int d = 0;
+  for (int j = i; j >= 0; j = T->parent[j]) ++d;
+  return d;
+}
+
+/* Final-normed output of the last row of [c_s, path...] at positions
+ * s+1..s+1+len on a copy of the prefix cache. */
+static void path_output(const orc_model* M, const double* kv0, double* kvw, const float* x, int s, int c_s,
+                        const int* path, int len, double* rows, double* outs, double* last) {
+  const size_t nkv = orc_kv_doubles(M);
+  memcpy(kvw, kv0, sizeof(double) * nkv);
+  int pos[64];
+  input_row(M, x, s + 1, c_s, rows);
+  pos[0] = s + 1;
+  for (int i = 0; i < len; ++i) {
+    input_row(M, x, s + 2 + i, path[i], rows + (size_t)(i + 1) * M->H);
+    pos[i + 1] = s + 2 + i;
+  }
+  orc_forward(M, kvw, len + 1, rows, pos, outs);
+  memcpy(last, outs + (size_t)len * M->H, sizeof(double) * M->H);
+}
+
+static void decode_one_frame_tree(const orc_model* M, const orc_tree* T, int top_k, float Tmp, uint64_t seed,
+                                  int stream, int frame, const float* x, int c0, int* codes, orc_stats* st,
+                                  orc_round_rec* log, int log_cap, int* n_log) {
+  const int H = M->H, V = M->V, G = M->G, n = T->n;
+  const size_t nkv = orc_kv_doubles(M);
+  double* kv = (double*)calloc(nkv, sizeof(double));
+  double* kvw = (double*)malloc(sizeof(double) * nkv);
+  double* rows = (double*)malloc(sizeof(double) * 64 * H);
+  double* outs = (double*)malloc(sizeof(double) * 64 * H);
+  double* hs = (double*)malloc(sizeof(double) * H);
+  double* hn = (double*)malloc(sizeof(double) * H);
+  float* lg = (float*)malloc(sizeof(float) * V);
+  float* pn = (float*)malloc(sizeof(float) * (size_t)(n + 1) * V); /* law at the root (0) and node i (i + 1) */
+  float* work = (float*)malloc(sizeof(float) * V);
+  int* order = (int*)malloc(sizeof(int) * V);
+  int* tok = (int*)malloc(sizeof(int) * (n > 0 ? n : 1));
+  int* dep = (int*)malloc(sizeof(int) * (n > 0 ? n : 1));
+  int* keep = (int*)malloc(sizeof(int) * (n > 0 ? n : 1));
+  int pos[2], path[64], dr[8] = {0};
+  double mg, m1;
+
+  /* frame prefill, as in the chain rounds */
+  codes[0] = c0;
+  input_row(M, x, 0, 0, rows);
+  input_row(M, x, 1, c0, rows + H);
+  pos[0] = 0; pos[1] = 1;
+  orc_forward(M, kv, 2, rows, pos, outs);
+  st->passes++;
+  orc_head_logits(M, 1, outs + H, NULL, lg);
+  orc_process(lg, V, top_k, Tmp, work, &mg);
+  codes[1] = orc_sample(work, V, orc_uniform(seed, (uint32_t)stream, (uint32_t)frame, 1, ORC_TARGET), &m1);
+  if (m1 < mg) mg = m1;
+  log_round(log, log_cap, n_log, frame, stream, 0, 0, 1, 0, 1, dr, mg);
+  memcpy(hs, outs + H, sizeof(double) * H);
+  int s = 1;
+  while (s < G - 1) {
+    const int R = G - 1 - s;
+    mg = INFINITY;
+    int nkeep = 0, dmax = 0;
+    for (int i = 0; i < n; ++i) {
+      dep[i] = tree_depth(T, i);
+      keep[i] = dep[i] <= R && T->rank[i] < V && (T->parent[i] < 0 || keep[T->parent[i]]);
+      if (keep[i]) { ++nkeep; if (dep[i] > dmax) dmax = dep[i]; }
+    }
+    /* candidate tokens: rank r of depth t's draft logits (selection by
+     * value descending, index ascending) */
+    for (int t = 1; t <= dmax; ++t) {
+      orc_draft_logits(M, s + t, t, hs, lg);
+      int need = 0;
+      for (int i = 0; i < n; ++i)
+        if (keep[i] && dep[i] == t && T->rank[i] + 1 > need) need = T->rank[i] + 1;
+      for (int r = 0; r < need && r < V; ++r) {
+        int best = -1;
+        for (int v = 0; v < V; ++v) {
+          int used = 0;
+          for (int q = 0; q < r; ++q) used |= order[q] == v;
+          if (used) continue;
+          if (best < 0 || lg[v] > lg[best]) best = v;
+        }
+        order[r] = best;
+      }
+      /* near-ties between consecutive ranks may order differently in float32 */
+      for (int r = 0; r + 1 < need && r + 1 < V; ++r) {
+        const double g = (double)lg[order[r]] - (double)lg[order[r + 1]];
+        if (g < mg) mg = g;
+      }
+      for (int i = 0; i < n; ++i)
+        if (keep[i] && dep[i] == t) tok[i] = order[T->rank[i]];
+    }
+    /* verify: the law at the root (p_{s+1}) and at every kept node short of depth R */
+    path_output(M, kv, kvw, x, s, codes[s], path, 0, rows, outs, hn);
+    orc_head_logits(M, s + 1, hn, NULL, lg);
+    orc_process(lg, V, top_k, Tmp, pn, &m1);
+    if (m1 < mg) mg = m1;
+    for (int i = 0; i < n; ++i) {
+      if (!keep[i] || dep[i] >= R) continue;
+      int len = dep[i];
+      for (int j = i, k = len - 1; j >= 0; j = T->parent[j], --k) path[k] = tok[j];
+      path_output(M, kv, kvw, x, s, codes[s], path, len, rows, outs, hn);
+      orc_head_logits(M, s + len + 1, hn, NULL, lg);
+      orc_process(lg, V, top_k, Tmp, pn + (size_t)(i + 1) * V, &m1);
+      if (m1 < mg) mg = m1;
+    }
+    st->passes++;
+    /* walk down from the committed code */
+    int cur = -1, d = 0, acc_n = 0;
+    while (s + d < G - 1) {
+      const float* p = pn + (size_t)(cur + 1) * V;
+      memcpy(work, p, sizeof(float) * V);
+      int taken = -1, ci = 0;
+      for (int i = 0; i < n && taken < 0; ++i) {
+        if (!keep[i] || T->parent[i] != cur) continue;
+        float S = 0.0f;
+        for (int v = 0; v < V; ++v) S = S + work[v];
+        const float r = S > 0.0f ? work[tok[i]] / S : 0.0f;
+        const float u = orc_uniform(seed, (uint32_t)stream, (uint32_t)frame, (uint32_t)(s + d + 1),
+                                    (uint32_t)(ORC_TREE_ACCEPT + ci));
+        const double g = fabs((double)u - (double)r);
+        if (g < mg) mg = g;
+        if (u < r) taken = i;
+        else work[tok[i]] = 0.0f;
+        ++ci;
+      }
+      if (taken >= 0) {
+        codes[s + d + 1] = tok[taken];
+        cur = taken;
+        ++d;
+        ++acc_n;
+        st->accepted_by_offset[d < 9 ? d : 8]++;
+        continue;
+      }
+      const float u = orc_uniform(seed, (uint32_t)stream, (uint32_t)frame, (uint32_t)(s + d + 1), ORC_TARGET);
+      int y = orc_sample(work, V, u, &m1);
+      if (y < 0) y = orc_sample(p, V, u, &m1);
+      if (m1 < mg) mg = m1;
+      codes[s + d + 1] = y;
+      ++d;
+      if (ci > 0) st->rejections++; else st->bonus++;
+      break;
+    }
+    const int s_new = s + d;
+    /* reconcile: the cache keeps positions 0..s_new (the committed code and
+     * the accepted path); the new hidden is the output at position s_new */
+    if (s_new < G - 1) {
+      for (int k = 0; k < d - 1; ++k) path[k] = codes[s + 1 + k];
+      path_output(M, kv, kvw, x, s, codes[s], path, d - 1, rows, outs, hs);
+      memcpy(kv, kvw, sizeof(double) * nkv);
+    }
+    st->rounds++;
+    for (int k = 0; k < 8; ++k) dr[k] = k < acc_n ? codes[s + 1 + k] : -1;
+    log_round(log, log_cap, n_log, frame, stream, s, nkeep, nkeep + 1, acc_n, s_new, dr, mg);
+    s = s_new;
+  }
+  st->committed += G - 1;
+  st->frames++;
+  free(kv); free(kvw); free(rows); free(outs); free(hs); free(hn); free(lg); free(pn); free(work);
+  free(order); free(tok); free(dep); free(keep);
+}
+
+int orc_decode_frames_tree(const orc_model* M, const orc_tree* T, const int* top_k, const float* temp,
+                           uint64_t seed, int B, int F, int first_frame, const float* x, const int* c0, int* codes,
+                           orc_stats* st, orc_round_rec* log, int log_cap, int* n_log) {
+  if (!M || !T || !codes || !x || !c0 || !st) return -1;
+  if (M->G < 2 || M->nq % M->nkv != 0 || M->d % 2 != 0) return -1;
+  if (M->K < 0 || (M->K > 0 && !M->draft_offset)) return -1;
+  if (T->n < 0 || T->n > 62 || (T->n > 0 && (!T->parent || !T->rank))) return -1;
+  for (int i = 0; i < T->n; ++i) {
+    if (T->parent[i] < -1 || T->parent[i] >= i || T->rank[i] < 0) return -1; /* parents first */
+    for (int j = 0; j < i; ++j) /* siblings in ascending rank, no repeats */
+      if (T->parent[j] == T->parent[i] && T->rank[j] >= T->rank[i]) return -1;
+  }
+  if (n_log) *n_log = 0;
+  for (int f = 0; f < F; ++f)
+    for (int b = 0; b < B; ++b)
+      decode_one_frame_tree(M, T, top_k[b], temp[b], seed, b, first_frame + f, x + ((size_t)f * B + b) * M->H,
+                            c0[(size_t)f * B + b], codes + ((size_t)f * B + b) * M->G, st, log, log_cap, n_log);
+  return 0;
+}

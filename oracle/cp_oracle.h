@@ -45,7 +45,7 @@
 extern "C" {
 #endif
 
-enum { ORC_DRAFT = 0, ORC_ACCEPT = 1, ORC_TARGET = 2, ORC_INPUT = 3 };
+enum { ORC_DRAFT = 0, ORC_ACCEPT = 1, ORC_TARGET = 2, ORC_INPUT = 3, ORC_TREE_ACCEPT = 4 /* + child index */ };
 
 typedef struct {
   int H, L, nq, nkv, d, F, V, G;
@@ -154,6 +154,25 @@ int orc_decode_frames_policy(const orc_model* M, int N, const int* top_k, const 
                              int B, int F, int first_frame, const float* x, const int* c0, int* codes,
                              orc_stats* st, orc_round_rec* log, int log_cap, int* n_log, int pct,
                              int min_reached);
+
+/* Sparse draft tree ("RVQ Position Aware Speculative Decoding for On Device
+ * TTS", section 2.2, Figure 2): n nodes (at most 62), parents first; node i
+ * has parent[i] (-1: a child of the committed code) and rank[i], the rank of
+ * its token among the draft logits of its depth (value descending, index
+ * ascending); siblings appear in ascending rank.  Nodes deeper than the
+ * codes left in a frame are dropped. */
+typedef struct {
+  int n;
+  const int *parent;
+  const int *rank;
+} orc_tree;
+/* Decode frames with tree rounds (acceptance walk described at the
+ * definition).  Log records: n_d = kept nodes, m = rows verified, n_acc =
+ * accepted depth, drafts = the accepted path.  drafted_by_offset stays zero;
+ * accepted_by_offset counts accepted nodes by depth. */
+int orc_decode_frames_tree(const orc_model* M, const orc_tree* T, const int* top_k, const float* temp,
+                           uint64_t seed, int B, int F, int first_frame, const float* x, const int* c0, int* codes,
+                           orc_stats* st, orc_round_rec* log, int log_cap, int* n_log);
 
 #ifdef __cplusplus
 }

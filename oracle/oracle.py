@@ -47,6 +47,10 @@ class OrcModel(C.Structure):
         ("K", C.c_int), ("draft_offset", C.c_void_p)]
 
 
+class OrcTree(C.Structure):
+    _fields_ = [("n", C.c_int), ("parent", C.c_void_p), ("rank", C.c_void_p)]
+
+
 class OrcStats(C.Structure):
     _fields_ = [(n, C.c_int64) for n in ("frames", "passes", "rounds", "committed", "bonus", "rejections")] + [
         ("drafted_by_offset", C.c_int64 * 9), ("accepted_by_offset", C.c_int64 * 9)]
@@ -101,6 +105,8 @@ def lib():
             L.orc_decode_frames_policy.argtypes = [vp, i32, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp,
                                                    i32, i32]
             L.orc_decode_frames_policy.restype = i32
+            L.orc_decode_frames_tree.argtypes = [vp, vp, vp, vp, u64, i32, i32, i32, vp, vp, vp, vp, vp, i32, vp]
+            L.orc_decode_frames_tree.restype = i32
             L.orc_policy_window.argtypes = [i32, i32, i32, vp, vp]
             L.orc_policy_window.restype = i32
             _lib = L
@@ -250,6 +256,28 @@ class Model:
         o32 = np.empty(self.spec.vocab, np.float32)
         lib().orc_head_logits(self.ptr, int(j), _p(hn), _p(o64), _p(o32))
         return o64, o32
+
+    def decode_frames_tree(self, parent, rank, top_k, temperature, seed: int, x: np.ndarray, c0: np.ndarray,
+                           first_frame: int = 0, log_cap: int = 0):
+        """Tree rounds (orc_decode_frames_tree): parent / rank per node, parents first."""
+        F, B, H = x.shape
+        par = np.ascontiguousarray(parent, dtype=np.int32)
+        rk = np.ascontiguousarray(rank, dtype=np.int32)
+        tree = OrcTree(int(par.size), par.ctypes.data, rk.ctypes.data)
+        tk = np.ascontiguousarray(np.broadcast_to(np.asarray(top_k, np.int32), (B,)))
+        tp = np.ascontiguousarray(np.broadcast_to(np.asarray(temperature, np.float32), (B,)))
+        xx = np.ascontiguousarray(x, dtype=np.float32)
+        cc = np.ascontiguousarray(c0, dtype=np.int32)
+        codes = np.zeros((F, B, self.spec.num_code_groups), np.int32)
+        st = OrcStats()
+        log = np.zeros(max(log_cap, 1), ROUND_DTYPE)
+        nlog = C.c_int(0)
+        rc = lib().orc_decode_frames_tree(self.ptr, C.byref(tree), _p(tk), _p(tp), int(seed), B, F,
+                                          int(first_frame), _p(xx), _p(cc), _p(codes), C.byref(st), _p(log),
+                                          int(log_cap), C.byref(nlog))
+        if rc != 0:
+            raise ValueError("oracle rejected the tree decode arguments")
+        return codes, st.as_dict(), log[: min(nlog.value, log_cap)]
 
     @staticmethod
     def policy_window(N: int, pct: int, min_reached: int, reach, acc) -> int:
