@@ -16,6 +16,12 @@
  *      greedy (temperature 0) is exact argmax equality;
  *   4. reconcile: the KV cache keeps positions 0..s' (s' = last committed
  *      depth); rejected entries stay in memory but are never read (section 07).
+ * Two options change only the drafts, so the committed codes keep the
+ * autoregressive law: position-aware draft offsets (the draft of lookahead t
+ * reads head_{s+t} on h_s + b_t; "RVQ Position Aware Speculative Decoding for
+ * On Device TTS", section 2.2) and an adaptive window per stream chosen from
+ * its acceptance by offset ("Speculative Decoding, Beyond Text", runtime
+ * policies).
  *
  * Sequence layout of one frame: position 0 holds x, position j >= 1 holds
  * the embedding E_{j-1}(c_{j-1}); the decoder output at position j, through
