@@ -35,6 +35,7 @@ UNIT = "codes/s"
 FRAMES = 1000
 WINDOW = 4
 TOP_K, TEMP, SEED = 50, 0.9, 1
+HBM_NOMINAL_GBS = 7900.0  # GB300 HBM3e nominal bandwidth, reported beside the measured peak
 
 
 def workload_config(spec, frames, n_streams, window):
@@ -204,6 +205,7 @@ def run_gpu(args, rank, world):
     passes = st["passes"] / args.steps
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                "peak_nominal": HBM_NOMINAL_GBS, "frac_nominal": round(achieved / HBM_NOMINAL_GBS, 4),
                 "traffic": (round(traffic_pp * passes) if traffic_pp else None),
                 "kernel": "verify pass: the call graph's pass kernels (5 per layer + lm_heads, top-k, accept), "
                           "timed per step; GEMV kernels are 21 of the 28 per pass",
