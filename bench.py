@@ -262,24 +262,27 @@ def run_gpu(args, rank, world):
     return result
 
 
-def large_line(peak, frames=16):
+def large_line(peak, frames=16, batched_frames=4):
     """The large model (H 2048, 8 layers, 32 q / 8 kv heads x 64, FFN 6144, V 4096, G 32: 31
-    lm_heads of 16.8 MB) at one stream: the AR loop, N = 4, and N = 4 with the adaptive
-    window; T 0.8, top-k 50, `frames` frames: codes/s, time per pass and the algorithmic
-    HBM fraction."""
+    lm_heads of 16.8 MB), T 0.8, top-k 50: at one stream over `frames` frames the AR loop,
+    N = 4, and N = 4 with the adaptive window; then N = 4 at 8 and 64 streams (tensor-core
+    GEMVs) over `batched_frames` frames.  codes/s, time per pass and the algorithmic HBM
+    fraction."""
     import torch
     from speculative_decoding_rvq_gb300 import binding, synth as S
     spec = S.LARGE_BF16
     dw = binding.weights_to_device(spec, S.gen_weights(spec, 0))
-    x, c0 = S.gen_frames(spec, 1, frames, seed=SEED)
-    xd, cd = torch.from_numpy(x).cuda(), torch.from_numpy(c0).cuda()
     G = spec.num_code_groups
     out = {"model": "H2048, 8L, 32q/8kv x64, FFN6144, V4096, G32, bf16", "frames": frames, "temperature": 0.8}
     # N4_adaptive: the per-stream adaptive window (keep an offset at >= 30 % acceptance,
     # judged after 16 reached drafts)
-    for name, n, pct in (("N0", 0, 0), ("N4", 4, 0), ("N4_adaptive", 4, 30)):
-        cp = binding.CpSpec(spec, dw, n, TOP_K, 0.8, SEED, 1, adapt_pct=pct, adapt_min=16)
-        codes = torch.empty((frames, 1, G), dtype=torch.int32, device="cuda")
+    for name, n, pct, B in (("N0", 0, 0, 1), ("N4", 4, 0, 1), ("N4_adaptive", 4, 30, 1), ("N4_B8", 4, 0, 8),
+                            ("N4_B64", 4, 0, 64)):
+        F = frames if B == 1 else batched_frames
+        x, c0 = S.gen_frames(spec, B, F, seed=SEED)
+        xd, cd = torch.from_numpy(x).cuda(), torch.from_numpy(c0).cuda()
+        cp = binding.CpSpec(spec, dw, n, TOP_K, 0.8, SEED, B, adapt_pct=pct, adapt_min=16)
+        codes = torch.empty((F, B, G), dtype=torch.int32, device="cuda")
         cp.decode_frames(xd, cd, codes)
         torch.cuda.synchronize()
         cp.status()
@@ -292,10 +295,10 @@ def large_line(peak, frames=16):
         cp.status()
         ms = a.elapsed_time(b)
         st = cp.stats()
-        out[name] = {"codes_per_s": round(frames * (G - 1) / (ms / 1e3), 1),
-                        "passes_per_frame": round(st["passes"] / frames, 3),
-                        "us_per_pass": round(ms * 1e3 / st["passes"], 2),
-                        "hbm_frac": round((st["weight_bytes"] + st["kv_bytes"]) / (ms / 1e3) / 1e9 / peak, 4)}
+        out[name] = {"streams": B, "frames": F, "codes_per_s": round(B * F * (G - 1) / (ms / 1e3), 1),
+                     "passes_per_frame": round(st["passes"] / F, 3),
+                     "us_per_pass": round(ms * 1e3 / st["passes"], 2),
+                     "hbm_frac": round((st["weight_bytes"] + st["kv_bytes"]) / (ms / 1e3) / 1e9 / peak, 4)}
         cp.close()
     del dw
     torch.cuda.empty_cache()
