@@ -394,8 +394,28 @@ def batched(spec, dw, peak, streams=64, frames=100):
     return out
 
 
+def expected_accepted(tgt, drf, k: int, T: float) -> float:
+    """Closed-form mean of accepted drafts per round for given logits: with
+    beta_t = sum_v min(p_t(v), q_t(v)) (p, q the processed target and draft laws of
+    position t), a round accepts at least j drafts with probability prod_{t<=j} beta_t,
+    so E[accepted] = sum_j prod_{t<=j} beta_t ("Speculative Decoding, Beyond Text",
+    section 02: sum-min = 1 - TV).  Analysis of the benchmark's inputs, outside the
+    timed region; tgt [R, N, V], drf [R, N-1, V] torch tensors."""
+    import torch
+
+    def proc(x):
+        z = x / T
+        v, i = z.topk(min(k, z.shape[-1]), dim=-1)
+        return torch.zeros_like(z).scatter_(-1, i, torch.softmax(v, dim=-1))
+
+    n = drf.shape[1]
+    beta = torch.minimum(proc(tgt[:, :n]), proc(drf)).sum(-1)  # [R, N-1]
+    return float(torch.cumprod(beta, dim=1).sum(1).mean().item())
+
+
 def accept_microbench(peak):
-    """Acceptance kernels alone: 65536 rounds, V 2048, rho 0.7, top-k 50, T 0.9 (logit mode)."""
+    """Acceptance kernels alone: 65536 rounds, V 2048, rho 0.7, top-k 50, T 0.9 (logit mode);
+    the mean accepted drafts per round beside its closed form for the same inputs."""
     import torch
     from speculative_decoding_rvq_gb300 import binding
     R, V = 65536, 2048
@@ -420,6 +440,10 @@ def accept_microbench(peak):
         res[f"N{N}"] = {"rounds_per_s": round(R / (ms / 1e3), 1), "ms": round(ms, 3), "GB_s": round(gbs, 1),
                         "hbm_frac": round(gbs / peak, 4),
                         "mean_accepted": round(float(na.float().mean().item()), 4)}
+        try:
+            res[f"N{N}"]["closed_form_accepted"] = round(expected_accepted(tgt, drf, TOP_K, TEMP), 4)
+        except Exception as exc:  # analysis only: never lose the measured line over it
+            res[f"N{N}"]["closed_form_accepted"] = f"unavailable: {type(exc).__name__}"
         del tgt, drf
     return res
 
