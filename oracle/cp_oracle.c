@@ -63,47 +63,18 @@ static int cmp_desc(const void* a, const void* b) {
   return (x->idx < y->idx) ? -1 : (x->idx > y->idx);
 }
 
-/* "Let q_i and p_i be the draft and target distributions after temperature,
- * ... top-k ... and every other processor" (Speculative Decoding, Beyond
- * Text, section 02).  Temperature and top-k only; the ordering and rounding
- * are this library's stated reading (T first, exact-k with index tie-break). */
-/* e^d for d <= 0 in float32, written from the mathematics: Cody-Waite range
- * reduction (W. J. Cody and W. Waite, "Software Manual for the Elementary
- * Functions", 1980): n = rint(d * log2 e), r = d - n ln 2 with ln 2 split in
- * a high part (exact products with n) and a low part; then the degree-7
- * Taylor polynomial of e^r on |r| <= ln2/2 (truncation below 6e-9 relative),
- * evaluated by Horner with fused multiply-adds; finally the exact scaling by
- * 2^n.  Below d = -87 (e^d < 2^-125) the value is defined as 0.  Every step
- * is one IEEE float32 operation, so any implementation that follows the same
- * sequence gets the same bits. */
-float orc_expf(float d) {
-  if (!(d >= -87.0f)) return 0.0f;
-  const float log2e = 0x1.715476p+0f, ln2_hi = 0x1.62e4p-1f, ln2_lo = 0x1.7f7d1cp-20f;
-  const float n = rintf(d * log2e);
-  float r = fmaf(-n, ln2_hi, d);
-  r = fmaf(-n, ln2_lo, r);
-  float p = 0x1.a01a02p-13f;        /* 1/7! */
-  p = fmaf(p, r, 0x1.6c16c2p-10f);  /* 1/6! */
-  p = fmaf(p, r, 0x1.111112p-7f);   /* 1/5! */
-  p = fmaf(p, r, 0x1.555556p-5f);   /* 1/4! */
-  p = fmaf(p, r, 0x1.555556p-3f);   /* 1/3! */
-  p = fmaf(p, r, 0.5f);
-  p = fmaf(p, r, 1.0f);
-  p = fmaf(p, r, 1.0f);
-  const int ni = (int)n; /* in [-126, 0] */
-  union { uint32_t u; float f; } sc;
-  sc.u = (uint32_t)(ni + 127) << 23;
-  return p * sc.f;
-}
-
 /* Top-k / temperature processing ("Speculative Decoding, Beyond Text",
- * section 02: the draft and target laws the acceptance rule compares).
+ * section 02: q_i and p_i are the draft and target laws after temperature,
+ * top-k and the other processors; only temperature and top-k are used here).
  * z_i = fl32(logit_i / T); keep exactly min(k, V) entries ordered by
- * (z desc, index asc); e_i = orc_expf(fl32(z_i - z_max)); S = float32 sum of
- * e_i over the kept entries in ascending index order; p_i = fl32(e_i / S).
- * T = 0 is argmax with the lowest index on ties.  `margin` (optional) is the
- * decision gap that a change of rounding would have to cross: the logit gap
- * at the top-k boundary (or to the runner-up for greedy). */
+ * (z desc, index asc); then the softmax over the kept set in float64:
+ * e_i = exp(z_i - z_max), S = sum of e_i (ascending index order),
+ * p_i = e_i / S, each p_i rounded once to float32.  The pages fix no
+ * precision for this step; float64 with one final rounding is the plain
+ * definition.  T = 0 is argmax with the lowest index on ties.  `margin`
+ * (optional) is the decision gap that a change of rounding would have to
+ * cross: the logit gap at the top-k boundary (or to the runner-up for
+ * greedy). */
 void orc_process(const float* logits, int V, int top_k, float T, float* probs, double* margin) {
   if (V <= 0) return;
   for (int i = 0; i < V; ++i) probs[i] = 0.0f;
@@ -132,12 +103,12 @@ void orc_process(const float* logits, int V, int top_k, float T, float* probs, d
   qsort(zs, (size_t)V, sizeof(zi_t), cmp_desc);
   int kk = top_k < V ? top_k : V;
   for (int r = 0; r < kk; ++r) keep[zs[r].idx] = 1;
-  const float zmax = zs[0].z;
-  float S = 0.0f;
+  const double zmax = (double)zs[0].z;
+  double S = 0.0;
   for (int i = 0; i < V; ++i)
-    if (keep[i]) S = S + orc_expf(logits[i] / T - zmax);
+    if (keep[i]) S += exp((double)(logits[i] / T) - zmax);
   for (int i = 0; i < V; ++i)
-    if (keep[i]) probs[i] = orc_expf(logits[i] / T - zmax) / S;
+    if (keep[i]) probs[i] = (float)(exp((double)(logits[i] / T) - zmax) / S);
   if (margin) *margin = (kk < V) ? ((double)zs[kk - 1].z - (double)zs[kk].z) * (double)T : INFINITY;
   free(zs);
   free(keep);

@@ -23,9 +23,10 @@
  *
  * Precision: the forward pass runs in float64 on weights given as float32
  * (bf16 and fp32 storage values are exact in float32); logits are rounded
- * to float32 and all sampling arithmetic is float32 with the exact orders
- * documented at each function, including the softmax (its exponential is
- * orc_expf, a fixed float32 operation sequence).
+ * to float32.  The softmax of the logit processing is float64 (exp and
+ * sum) with one rounding of each probability to float32; the categorical
+ * draw and the acceptance test are float32 with the exact orders documented
+ * at each function.
  *
  * Parity pins: every function here is checked in tests/ against something
  * other than itself (published Philox known-answer vectors, brute-force
@@ -90,12 +91,9 @@ void orc_uniform_fill(uint64_t seed, int n, const uint32_t* ctr4 /*[n][4]*/, flo
 
 /* Logit processing: T == 0 -> one-hot argmax (lowest index on ties); else
  * z = fl32(logit / T), keep exactly min(k, V) entries by (z desc, index asc),
- * e_i = orc_expf(fl32(z_i - zmax)), S = sequential float32 sum of the kept
- * e_i in ascending index order, p_i = fl32(e_i / S).  margin (optional) =
- * decision gap in logit units. */
+ * e_i = exp(z_i - zmax) and S = sum of the kept e_i in float64,
+ * p_i = fl32(e_i / S).  margin (optional) = decision gap in logit units. */
 void orc_process(const float* logits, int V, int top_k, float T, float* probs, double* margin);
-/* e^d for d <= 0 in float32 (Cody-Waite reduction + degree-7 Taylor, fused multiply-adds; 0 below -87). */
-float orc_expf(float d);
 /* Categorical draw: candidates = {i : w_i > 0} ascending; S_j sequential
  * float32 prefix sums; t = fl32(u * S_last); first j with S_j > t, else the
  * last candidate.  Returns -1 if no candidate.  margin = relative distance

@@ -87,8 +87,6 @@ def lib():
             L.orc_uniform.restype = f32
             L.orc_uniform_fill.argtypes = [u64, i32, vp, vp]
             L.orc_process.argtypes = [vp, i32, i32, f32, vp, vp]
-            L.orc_expf.argtypes = [f32]
-            L.orc_expf.restype = f32
             L.orc_sample.argtypes = [vp, i32, f32, vp]
             L.orc_sample.restype = i32
             L.orc_accept_chain.argtypes = [i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
@@ -134,11 +132,6 @@ def uniforms(seed: int, ctr4: np.ndarray) -> np.ndarray:
 
 
 # ------------------------------------------------------------ sampling
-def expf(d: float) -> float:
-    """orc_expf: e^d for d <= 0, float32 (the softmax exponential)."""
-    return float(lib().orc_expf(float(d)))
-
-
 def process(logits, top_k: int, temperature: float):
     z = np.ascontiguousarray(logits, dtype=np.float32)
     out = np.empty_like(z)
