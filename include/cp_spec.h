@@ -267,7 +267,8 @@ cp_spec_status cp_spec_accept_batch(int32_t R, int32_t N, int32_t V, int32_t top
  * workspace it needs is cp_spec_workspace_bytes(model, config); above
  * CP_SPEC_STATIC_SCRATCH_BYTES the call returns CP_SPEC_E_WORKSPACE and
  * enqueues nothing (lower max_streams).  d_status (optional, device, one
- * int32) receives the device status word after the decode: CP_SPEC_OK,
+ * int32, 4-byte aligned; the other device pointers need 16 bytes) receives
+ * the device status word after the decode: CP_SPEC_OK,
  * CP_SPEC_E_DEVICE_TIMEOUT or CP_SPEC_E_DEVICE.
  *
  * Every call clears the scratch, resets it to the state cp_spec_init leaves
@@ -298,6 +299,19 @@ cp_spec_status cp_spec_status_word(cp_spec_ctx* ctx, void* stream);
 /* Synchronise `stream` and copy the counters to *h_stats. */
 cp_spec_status cp_spec_read_stats(cp_spec_ctx* ctx, cp_spec_stats* h_stats, void* stream);
 cp_spec_status cp_spec_reset_stats(cp_spec_ctx* ctx, void* stream);
+
+/* Diagnostic hook for tests of the failure path (the pages have no
+ * counterpart).  wait_limit_ns (1e4 .. 6e10; default 2e9) bounds every
+ * device-side wait of the context's kernels (a weight or input copy that has
+ * not landed): after it the kernel records CP_SPEC_E_DEVICE_TIMEOUT in the
+ * status word, waits (with the same bound) for its own copies still in
+ * flight and returns; the pass loop then stops.  stall_first_wait = 1 makes
+ * one wait of the first decoder kernel of every pass (CTA 0) expect 16 bytes
+ * that no copy delivers, so that wait always runs out; 0 restores normal
+ * operation.  Nothing traps or spins without a bound.  Synchronises the
+ * device if the context's call graph exists (it is rebuilt on the next
+ * call). */
+cp_spec_status cp_spec_test_hooks(cp_spec_ctx* ctx, uint64_t wait_limit_ns, int32_t stall_first_wait);
 
 /* Number of launches the library has enqueued on this context: kernels
  * launched directly, plus one per launch of the context's call graph (whose

@@ -25,7 +25,7 @@ E_INVALID, E_UNSUPPORTED, E_CUDA, E_WORKSPACE, E_DEVICE_TIMEOUT, E_STATE, E_DEVI
 EXPORTS = ("cp_spec_workspace_bytes", "cp_spec_init", "cp_spec_set_stream_sampling", "cp_spec_decode_frames",
            "cp_spec_begin_frame", "cp_spec_round", "cp_spec_teacher_logits", "cp_spec_accept_batch",
            "cp_spec_status_word", "cp_spec_read_stats", "cp_spec_reset_stats", "cp_spec_launch_count",
-           "cp_spec_last_error", "cp_spec_destroy", "cp_spec_decode_frames_static")
+           "cp_spec_last_error", "cp_spec_destroy", "cp_spec_decode_frames_static", "cp_spec_test_hooks")
 
 
 class CpSpecError(RuntimeError):
@@ -87,6 +87,7 @@ def load():
     L.cp_spec_accept_batch.argtypes = [i32, i32, i32, i32, f32, u64, i32, vp, vp, vp, vp, vp, vp]
     L.cp_spec_decode_frames_static.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp, vp, vp]
     L.cp_spec_status_word.argtypes = [vp, vp]
+    L.cp_spec_test_hooks.argtypes = [vp, u64, i32]
     L.cp_spec_read_stats.argtypes = [vp, vp, vp]
     L.cp_spec_reset_stats.argtypes = [vp, vp]
     L.cp_spec_launch_count.argtypes = [vp]
@@ -97,7 +98,7 @@ def load():
     L.cp_spec_destroy.restype = None
     for name in ("cp_spec_init", "cp_spec_set_stream_sampling", "cp_spec_decode_frames", "cp_spec_begin_frame",
                  "cp_spec_round", "cp_spec_teacher_logits", "cp_spec_accept_batch", "cp_spec_status_word",
-                 "cp_spec_read_stats", "cp_spec_reset_stats", "cp_spec_decode_frames_static"):
+                 "cp_spec_read_stats", "cp_spec_reset_stats", "cp_spec_decode_frames_static", "cp_spec_test_hooks"):
         getattr(L, name).restype = C.c_int
     _lib = L
     return L
@@ -227,6 +228,13 @@ class CpSpec:
 
     def status(self):
         _check(self.lib.cp_spec_status_word(self.ctx, _stream()), self.ctx)
+
+    def status_code(self) -> int:
+        """cp_spec_status_word as a code (clears the word)."""
+        return int(self.lib.cp_spec_status_word(self.ctx, _stream()))
+
+    def test_hooks(self, wait_limit_ns: int = 2_000_000_000, stall_first_wait: bool = False):
+        _check(self.lib.cp_spec_test_hooks(self.ctx, int(wait_limit_ns), 1 if stall_first_wait else 0), self.ctx)
 
     def stats(self) -> dict:
         st = Stats()

@@ -23,6 +23,13 @@ constexpr int kSlotBytes = 48 * 1024;       // GEMV weight tile (two slots per C
 constexpr int kRB = 4;                      // weight rows per GEMV batch
 constexpr int kMaxTileRows = 192;           // rows of one weight tile (bounds the partial-sum buffer)
 constexpr int kMaxHeadsPerPass = 64;
+constexpr unsigned long long kDefaultWaitNs = 2000000000ull;  // bounded device waits give up after 2 s
+// Small-batch tensor-core GEMV path (contexts with at most kMvMaxRows row slots).
+constexpr int kMvMaxRows = 8;        // pass rows: two column groups of four
+constexpr int kMvRowPad = 0;         // bytes after each weight row in shared memory (none: rows copied in runs)
+constexpr int kMvPhaseBlocks = 4;    // M-blocks of one phase (partial sums held at once)
+constexpr int kMvMaxBlocks = 96;     // M-blocks of one CTA
+constexpr int kMvMaxPhases = 48;
 
 // GEMV kinds, in pass order within a layer; kHeads closes a pass.
 enum GemvKind : int { kQKV = 0, kO = 1, kGU = 2, kDown = 3, kHeads = 4 };
@@ -101,7 +108,10 @@ struct FrameParams {
   int KO;   // lookaheads with a position-aware draft offset = min(K, ND)
   int adapt_pct;  // adaptive window: keep an offset at >= this acceptance percentage (0 = off)
   int adapt_min;  // ... or while it has fewer reached drafts than this
-  int pad0;
+  int mv;         // bf16 GEMVs on the small-batch tensor-core path (at most kMvMaxRows row slots)
+  int mv_slots[5];  // small-batch path: weight-row slots of shared memory per GEMV kind
+  int test_stall;   // test hook: one bounded wait of the first GEMV of a pass never completes
+  unsigned long long wait_ns;         // limit of every bounded device-side wait
   unsigned long long seed;
   unsigned long long cond;            // graph conditional handle of the pass loop (0 = none)
   long long layer_bytes, head_bytes;  // algorithmic bytes per layer / per lm_head

@@ -37,6 +37,11 @@
 #include "cp_frame.cuh"
 #include "cp_sampling.cuh"
 
+#include <algorithm>
+#include <map>
+#include <mutex>
+#include <utility>
+
 namespace cpk {
 
 // ------------------------------------------------------------ weight types
@@ -103,7 +108,6 @@ constexpr int kMaxTiles = 96;
 constexpr int kRedQ = 8;               // input rows per group at most (partial-sum row stride)
 constexpr int kRedFloats = 1536;       // GEMV partial sums of two tiles: rows x kRedQ x warps per row group, per tile
 constexpr int kRopeSmemBytes = 8192;   // RoPE table copied to shared memory up to this size
-constexpr uint64_t kTileTimeoutNs = 2ull * 1000ull * 1000ull * 1000ull;  // a bulk copy that has not landed in 2 s failed
 
 // The two (or one) contiguous byte runs of a tile in global memory: QKV
 // rows e and e + d/2 of one head; gate and up rows; else one run.
@@ -345,7 +349,10 @@ __device__ __forceinline__ void gemv_issue(const FrameParams& P, int l, GemvShar
   const TileRuns r = tile_runs<WT>(P, KIND, l, sh.heads, sh.tiles[t]);
   unsigned char* dst = slots + (size_t)slot * kSlotBytes;
   const uint64_t pol = l2_evict_first_policy();
-  mbar_arrive_expect_tx(&sh.full[slot], r.src1 ? 2 * r.bytes : r.bytes);
+  // test hook: the first tile of the pass's first GEMV in CTA 0 expects 16
+  // bytes that no copy delivers, so its bounded wait runs out
+  const uint32_t stall = (P.test_stall && KIND == kQKV && l == 0 && t == 0 && blockIdx.x == 0) ? 16u : 0u;
+  mbar_arrive_expect_tx(&sh.full[slot], (r.src1 ? 2 * r.bytes : r.bytes) + stall);
   bulk_copy_g2s(dst, r.src0, r.bytes, &sh.full[slot], pol);
   if (r.src1) bulk_copy_g2s(dst + r.bytes, r.src1, r.bytes, &sh.full[slot], pol);
   sh.issued = t + 1;
@@ -465,7 +472,7 @@ __device__ __forceinline__ bool gemv_run(const FrameParams& P, const CallArgs& c
       const int t = t0 + k, slot = t & 1;
       const int R = tiles[k].n * rpu;
       float* rk = red + k * (kRedFloats / 2);
-      if (!mbar_wait_bounded(&sh.full[slot], (uint32_t)(t >> 1) & 1u, &P.ctl->status, kTileTimeoutNs)) ok = false;
+      if (!mbar_wait_bounded(&sh.full[slot], (uint32_t)(t >> 1) & 1u, &P.ctl->status, P.wait_ns)) ok = false;
       if (!active || !ok) continue;
       const unsigned char* tp = slots + (size_t)slot * kSlotBytes;
       const int nrow = (R - g + G.RG - 1) / G.RG;  // rows g, g + RG, ... of the tile
@@ -761,8 +768,8 @@ __device__ __forceinline__ bool gemv_tc(const FrameParams& P, const CallArgs& ca
       rl = s_rl;
     }
     const int nblk = min((nr + 15) / 16, sh.blk1);
-    if (!mbar_wait_bounded(&sh.full[0], (uint32_t)(t0 >> 1) & 1u, &P.ctl->status, kTileTimeoutNs)) ok = false;
-    if (two && !mbar_wait_bounded(&sh.full[1], (uint32_t)(t0 >> 1) & 1u, &P.ctl->status, kTileTimeoutNs)) ok = false;
+    if (!mbar_wait_bounded(&sh.full[0], (uint32_t)(t0 >> 1) & 1u, &P.ctl->status, P.wait_ns)) ok = false;
+    if (two && !mbar_wait_bounded(&sh.full[1], (uint32_t)(t0 >> 1) & 1u, &P.ctl->status, P.wait_ns)) ok = false;
     if (ok) {
       const int nt0 = (tl0.n * rpu + 7) / 8, ntt = nt0 + (tl1.n * rpu + 7) / 8;
       for (int mb = sh.blk0 + warp; mb < nblk; mb += kWarps) {
@@ -957,81 +964,678 @@ __global__ void __launch_bounds__(kThreads, TC ? 1 : 2) gemv_kernel(const __grid
   if ((!ok || ngroups == 0) && threadIdx.x == 0) {
     // no copy may land after the CTA exits: wait (bounded) for the ones in flight
     for (int t = max(0, sh.issued - 2); t < sh.issued; ++t)
-      mbar_wait_bounded(&sh.full[t & 1], (uint32_t)(t >> 1) & 1u, &P.ctl->status, kTileTimeoutNs);
+      mbar_wait_bounded(&sh.full[t & 1], (uint32_t)(t >> 1) & 1u, &P.ctl->status, P.wait_ns);
+  }
+}
+
+// ------------------------------------------- small-batch tensor-core GEMV
+// Contexts with bf16 weights and at most kMvMaxRows row slots (one stream at
+// any verify window: the batch-1 path).  A GEMV there is a product of
+// (output units) x (pass rows <= 8) x K whose cost is reading the weights
+// once; after its dependency wait a kernel is limited by the latency of its
+// arithmetic, so the weights are the M operand of mma.sync m16n8k16
+// (bf16 x bf16 -> fp32) and the pass rows the N operand.  Each fp32 input x
+// is split into bf16 hi = rn(x) and lo = rn(x - hi) (16 mantissa bits
+// together); pass row r of a group of four takes column 2r (hi) and 2r + 1
+// (lo), so one MMA covers four rows and the lane that holds C[u][2r] also
+// holds C[u][2r + 1].
+//
+// A CTA owns a contiguous range of output units, cut into M-blocks of 16
+// weight rows: 16 units, or 8 units x (first, second) row of a RoPE pair or
+// a gate/up pair, so that both rows of a pair end in the same lane.  The
+// TMA unit copies the weight rows into shared memory with one 1-D bulk copy
+// per contiguous run of rows (a head of QKV or of the lm_heads, else the
+// whole tile; first rows and second rows of pairs apart), because a copy
+// costs about as much to issue as a few kilobytes take to land.  Inside
+// each 32-element block of K a fixed permutation gives lane t the physical
+// elements 8t..8t+7 on both operands, so a lane reads one 16-byte chunk of
+// each of its two weight rows and two float4 of its input row per two MMAs.
+// The input rows are bulk-copied into shared memory once per CTA.  The warps
+// split K; within its slice a warp converts each input block once and runs
+// it against every M-block of the phase.  The warps' partial sums meet in
+// shared memory and the epilogue adds them in warp order.  Reduction orders
+// depend on the model shape and the grid only, never on which rows share a
+// pass.
+//
+// Tiles larger than the CTA's weight region stream in phases through two
+// banks (phase p in bank p & 1); the first two phases are issued before the
+// dependency wait, phase p + 2 once phase p is consumed.  Each kernel also
+// prefetches into L2 the weight rows that the same CTA index of the GEMV two
+// kernels ahead will copy, so HBM keeps streaming through the dependency
+// waits of the chain.
+
+struct MvBlock {
+  int s0, s1;  // slot of A row 0 and of A row 8 (pair kinds: the second rows)
+  int n, n2;   // valid A rows among 0..7 (n) and 8..15 (n2), counted from 0 and from 8
+  int u;       // first unit
+  int pad[3];
+};
+
+struct MvShared {
+  uint64_t wbar[2];  // weight rows of the phase in bank 0 / 1
+  uint64_t ibar;     // input rows
+  int nblk, nphase, nrows, nheads, nbank, issued;
+  int plan_w[2];     // plan words nrows, nheads as loaded
+  int ph[kMvMaxPhases + 1];  // first block of each phase
+  int heads[kMaxHeadsPerPass];
+  int rbf[kMvMaxRows];       // input row held as bf16 (a code embedding of layer 0)
+  float inv[kMvMaxRows];     // RMSNorm scale per pass row
+  CallArgs ca;
+  MvBlock blk[kMvMaxBlocks];
+};
+
+// Global address of weight row h (0, or 1 = the second row of a pair) of
+// output unit u of a GEMV kind (bf16 weights).
+__device__ __forceinline__ const unsigned char* mv_row_src(const FrameParams& P, int kind, int l, const int* heads,
+                                                            int u, int h) {
+  switch (kind) {
+    case kQKV: {
+      const int half = P.d / 2, hh = u / half, e = u - hh * half;
+      const size_t rb = (size_t)P.H * 2;
+      const unsigned char* base;
+      if (hh < P.nq) base = static_cast<const unsigned char*>(P.wq[l]) + (size_t)hh * P.d * rb;
+      else if (hh < P.nq + P.nkv) base = static_cast<const unsigned char*>(P.wk[l]) + (size_t)(hh - P.nq) * P.d * rb;
+      else base = static_cast<const unsigned char*>(P.wv[l]) + (size_t)(hh - P.nq - P.nkv) * P.d * rb;
+      return base + (size_t)(e + h * half) * rb;
+    }
+    case kO: return static_cast<const unsigned char*>(P.wo[l]) + (size_t)u * P.nq * P.d * 2;
+    case kGU: return static_cast<const unsigned char*>(h ? P.w_up[l] : P.w_gate[l]) + (size_t)u * P.H * 2;
+    case kDown: return static_cast<const unsigned char*>(P.w_down[l]) + (size_t)u * P.F * 2;
+    default: {
+      const int hi = u / P.V, v = u - hi * P.V;
+      return static_cast<const unsigned char*>(P.head) + ((size_t)(heads[hi] - 1) * P.V + v) * P.H * 2;
+    }
+  }
+}
+
+__device__ __forceinline__ int mv_period(const FrameParams& P, int kind) {
+  return kind == kQKV ? P.d / 2 : (kind == kHeads ? P.V : 0);
+}
+
+// Units [ua, ub) of CTA c of g for U units (U * g < 2^31: at most 64 heads of
+// 8192 rows on a few hundred CTAs).
+__device__ __forceinline__ void mv_range(int U, int c, int g, int* ua, int* ub) {
+  *ua = (int)(((unsigned)U * (unsigned)c) / (unsigned)g);
+  *ub = (int)(((unsigned)U * (unsigned)(c + 1)) / (unsigned)g);
+}
+
+// L2 prefetch of the weight rows CTA blockIdx.x of GEMV (kind, l) copies:
+// one bulk prefetch per contiguous run.  Warp-wide.
+__device__ void mv_prefetch_l2(const FrameParams& P, int kind, int l, const int* heads, int nheads) {
+  const int lane = threadIdx.x & 31;
+  const int U = gemv_units(P, kind, nheads);
+  const int period = mv_period(P, kind);
+  int ua, ub;
+  mv_range(U, blockIdx.x, gridDim.x, &ua, &ub);
+  const int rpu = rows_per_unit(kind);
+  const uint32_t rowb = (uint32_t)gemv_K(P, kind) * 2u;
+  int j = 0;
+  for (int u = ua; u < ub;) {
+    const int e = period > 0 ? min(ub, (u / period + 1) * period) : ub;
+    for (int h = 0; h < rpu; ++h, ++j)
+      if ((j & 31) == lane) prefetch_l2(mv_row_src(P, kind, l, heads, u, h), (uint32_t)(e - u) * rowb);
+    u = e;
+  }
+}
+
+// This CTA's units cut into M-blocks and phases (one thread): one phase
+// when the whole tile fits the S row slots in at most kMvPhaseBlocks blocks,
+// else phases alternating between two banks of S/2 slots.
+__device__ void mv_build(const FrameParams& P, MvShared& sh, int S, int nheads, int kind) {
+  const bool kPair = kind == kQKV || kind == kGU;
+  const int rpu = kPair ? 2 : 1;
+  const int U = gemv_units(P, kind, nheads);
+  const int period = mv_period(P, kind);
+  int ua, ub;
+  mv_range(U, blockIdx.x, gridDim.x, &ua, &ub);
+  int nb = 0, np = 0, nbank = 1;
+  bool bad = false;
+  for (int attempt = 0; attempt < 2; ++attempt) {
+    nbank = attempt + 1;
+    const int cap = nbank == 1 ? S : S / 2;  // row slots of a bank
+    const int upb = max(1, min(kPair ? 8 : 16, cap / rpu));
+    int used = 0, inph = 0;
+    nb = 0;
+    np = 0;
+    bad = false;
+    sh.ph[0] = 0;
+    for (int u = ua; u < ub;) {
+      int e = min(ub, u + upb);
+      if (period > 0) e = min(e, (u / period + 1) * period);
+      const int n = e - u, rows = n * rpu;
+      if (used + rows > cap || inph == kMvPhaseBlocks) {
+        if (nbank == 1 || np + 2 > kMvMaxPhases) { bad = true; break; }
+        sh.ph[++np] = nb;
+        used = 0;
+        inph = 0;
+      }
+      if (nb >= kMvMaxBlocks) { bad = true; break; }
+      MvBlock B;
+      B.s0 = (nbank == 2 ? (np & 1) * cap : 0) + used / rpu;  // pair kinds: second rows placed below
+      B.s1 = kPair ? 0 : B.s0 + 8;
+      B.n = kPair ? n : min(n, 8);
+      B.n2 = kPair ? n : max(0, n - 8);
+      B.u = u;
+      sh.blk[nb++] = B;
+      used += rows;
+      ++inph;
+      u = e;
+    }
+    if (!bad) break;
+  }
+  // pair kinds: the first rows of a phase's units fill its slots in unit
+  // order, the second rows follow them (so each contiguous run of units is
+  // two bulk copies)
+  if (kPair && !bad) {
+    for (int p = 0; p <= np; ++p) {
+      const int b0 = p == 0 ? 0 : sh.ph[p], b1 = p < np ? sh.ph[p + 1] : nb;
+      int units = 0;
+      for (int b = b0; b < b1; ++b) units += sh.blk[b].n;
+      for (int b = b0; b < b1; ++b) sh.blk[b].s1 = sh.blk[b].s0 + units;
+    }
+  }
+  if (bad) { raise_status(&P.ctl->status, kStatusDevice); nb = 0; }
+  sh.ph[nb > 0 ? np + 1 : 0] = nb;
+  sh.nphase = nb > 0 ? np + 1 : 0;
+  sh.nblk = nb;
+  sh.nbank = nbank;
+}
+
+// Issue the bulk copies of the weight rows of phase p into its bank.  Warp-wide.
+__device__ void mv_issue_phase(const FrameParams& P, int l, MvShared& sh, unsigned char* wreg, int RS, int p, int kind) {
+  const int rpu = (kind == kQKV || kind == kGU) ? 2 : 1;
+  const int lane = threadIdx.x & 31;
+  const int b0 = sh.ph[p], b1 = sh.ph[p + 1];
+  const uint32_t rowb = (uint32_t)gemv_K(P, kind) * 2u;
+  uint64_t* bar = &sh.wbar[p & 1];
+  if (lane == 0) {
+    uint32_t rows = 0;  // pair kinds: n units of two rows; otherwise n + n2 units of one row
+    for (int b = b0; b < b1; ++b) rows += rpu == 2 ? 2u * (uint32_t)sh.blk[b].n : (uint32_t)(sh.blk[b].n + sh.blk[b].n2);
+    mbar_arrive_expect_tx(bar, rows * rowb);
+  }
+  __syncwarp();
+  const uint64_t pol = l2_evict_first_policy();
+  // runs of blocks whose units are consecutive rows in global memory (one
+  // head of QKV or of the lm_heads; the whole tile otherwise) and
+  // consecutive slots: one bulk copy per run and row half, one lane each
+  const int period = mv_period(P, kind);
+  int j = 0;
+  for (int b = b0; b < b1;) {
+    int e = b + 1, nu = rpu == 2 ? sh.blk[b].n : sh.blk[b].n + sh.blk[b].n2;
+    while (e < b1 && (period == 0 || sh.blk[e].u / period == sh.blk[b].u / period)) {
+      nu += rpu == 2 ? sh.blk[e].n : sh.blk[e].n + sh.blk[e].n2;
+      ++e;
+    }
+    for (int h = 0; h < rpu; ++h, ++j)
+      if ((j & 31) == lane)
+        bulk_copy_g2s(wreg + (size_t)(h ? sh.blk[b].s1 : sh.blk[b].s0) * RS,
+                      mv_row_src(P, kind, l, sh.heads, sh.blk[b].u, h), rowb * (uint32_t)nu, bar, pol);
+    b = e;
+  }
+  __syncwarp();
+}
+
+// bf16x2 of (x0, x1): the hi parts rn(x), or the lo parts rn(x - rn(x)).
+__device__ __forceinline__ uint32_t mv_part(float x0, float x1, bool lo) {
+  const __nv_bfloat162 h = __floats2bfloat162_rn(x0, x1);
+  const float2 hf = __bfloat1622float2(h);
+  const __nv_bfloat162 o = __floats2bfloat162_rn(x0 - hf.x, x1 - hf.y);
+  const uint32_t hu = *reinterpret_cast<const uint32_t*>(&h), ou = *reinterpret_cast<const uint32_t*>(&o);
+  return lo ? ou : hu;
+}
+
+// The MMAs of the blocks [b0, b1) of one phase (at most kMvPhaseBlocks):
+// warp w takes K elements [w K/8, (w+1) K/8); per 32-element step it forms
+// its B fragments once (input x gain, split hi or lo; NG groups of four pass
+// rows) and runs them against every block.  The warp leaves its partial
+// sums (hi + lo added) in
+// red[(block - b0)][w][A row][pass row] and, with `do_ss`, the sums of
+// squares of its K slice per pass row in s_ss.  Every order here depends on
+// the tile (model shape and grid), not on the pass rows.
+template <int NG>
+__device__ __forceinline__ void mv_compute(const MvShared& sh, const unsigned char* wreg, int RS, const float* in,
+                                           const float* gain, float* red, float* s_ss, int K, int RW, int b0, int b1,
+                                           bool do_ss) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t = lane & 3;
+  const int KW = K / kWarps, k0 = warp * KW;
+  const int nrows = sh.nrows;
+  const bool lo = (g & 1) != 0;
+  const int nbp = b1 - b0;
+  uint32_t pa[kMvPhaseBlocks], pb[kMvPhaseBlocks];  // shared-memory addresses of this lane's A chunks
+  bool va[kMvPhaseBlocks], vb[kMvPhaseBlocks];
+  const uint32_t wbase = smem_u32(wreg);
+#pragma unroll
+  for (int j = 0; j < kMvPhaseBlocks; ++j) {
+    const MvBlock B = sh.blk[b0 + min(j, nbp - 1)];
+    va[j] = j < nbp && g < B.n;
+    vb[j] = j < nbp && g < B.n2;
+    pa[j] = wbase + (uint32_t)((B.s0 + g) * RS + t * 16 + k0 * 2);
+    pb[j] = wbase + (uint32_t)((B.s1 + g) * RS + t * 16 + k0 * 2);
+  }
+  const float* rowp[NG];
+  bool rv[NG], r16[NG];
+#pragma unroll
+  for (int q = 0; q < NG; ++q) {
+    const int r = 4 * q + (g >> 1);
+    rv[q] = r < nrows;
+    r16[q] = rv[q] && sh.rbf[r] != 0;
+    rowp[q] = in + (size_t)(rv[q] ? r : 0) * K;
+  }
+  float acc[kMvPhaseBlocks][NG][4];
+  float ssq[NG];
+#pragma unroll
+  for (int j = 0; j < kMvPhaseBlocks; ++j)
+#pragma unroll
+    for (int q = 0; q < NG; ++q) acc[j][q][0] = acc[j][q][1] = acc[j][q][2] = acc[j][q][3] = 0.0f;
+#pragma unroll
+  for (int q = 0; q < NG; ++q) ssq[q] = 0.0f;
+#pragma unroll 2
+  for (int kk = 0; kk < KW; kk += 32) {
+    const int k = k0 + kk + 8 * t;
+    float gv[8];
+    if (gain != nullptr) {
+      const float4 g0 = *reinterpret_cast<const float4*>(gain + k);
+      const float4 g1 = *reinterpret_cast<const float4*>(gain + k + 4);
+      gv[0] = g0.x; gv[1] = g0.y; gv[2] = g0.z; gv[3] = g0.w; gv[4] = g1.x; gv[5] = g1.y; gv[6] = g1.z; gv[7] = g1.w;
+    }
+    uint32_t bp[NG][4];
+#pragma unroll
+    for (int q = 0; q < NG; ++q) {
+      float x[8];
+      if (!rv[q]) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] = 0.0f;
+      } else if (r16[q]) {
+        const uint4 w = *reinterpret_cast<const uint4*>(reinterpret_cast<const __nv_bfloat16*>(rowp[q]) + k);
+        const float2 a = bf16x2_to_f2(w.x), b = bf16x2_to_f2(w.y), c = bf16x2_to_f2(w.z), d = bf16x2_to_f2(w.w);
+        x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y; x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
+      } else {
+        const float4 a = *reinterpret_cast<const float4*>(rowp[q] + k), b = *reinterpret_cast<const float4*>(rowp[q] + k + 4);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w; x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+      }
+      if (do_ss && !lo) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) ssq[q] = fmaf(x[e], x[e], ssq[q]);
+      }
+      if (gain != nullptr) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) x[e] *= gv[e];
+      }
+      bp[q][0] = mv_part(x[0], x[1], lo);
+      bp[q][1] = mv_part(x[2], x[3], lo);
+      bp[q][2] = mv_part(x[4], x[5], lo);
+      bp[q][3] = mv_part(x[6], x[7], lo);
+    }
+#pragma unroll
+    for (int j = 0; j < kMvPhaseBlocks; ++j) {
+      if (j >= nbp) break;
+      uint4 A0 = make_uint4(0u, 0u, 0u, 0u), A1 = make_uint4(0u, 0u, 0u, 0u);
+      if (va[j]) asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(A0.x), "=r"(A0.y), "=r"(A0.z), "=r"(A0.w) : "r"(pa[j] + kk * 2));
+      if (vb[j]) asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(A1.x), "=r"(A1.y), "=r"(A1.z), "=r"(A1.w) : "r"(pb[j] + kk * 2));
+#pragma unroll
+      for (int q = 0; q < NG; ++q) {
+        mma_bf16_16816(acc[j][q], A0.x, A1.x, A0.y, A1.y, bp[q][0], bp[q][1]);
+        mma_bf16_16816(acc[j][q], A0.z, A1.z, A0.w, A1.w, bp[q][2], bp[q][3]);
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMvPhaseBlocks; ++j) {
+    if (j >= nbp) break;
+    float* rb = red + (size_t)(j * kWarps + warp) * 16 * RW;
+#pragma unroll
+    for (int q = 0; q < NG; ++q) {
+      rb[g * RW + 4 * q + t] = acc[j][q][0] + acc[j][q][1];
+      rb[(g + 8) * RW + 4 * q + t] = acc[j][q][2] + acc[j][q][3];
+    }
+  }
+  if (do_ss) {
+#pragma unroll
+    for (int q = 0; q < NG; ++q) {
+      float v = ssq[q];
+      v += __shfl_xor_sync(0xffffffffu, v, 1);
+      v += __shfl_xor_sync(0xffffffffu, v, 2);
+      if (t == 0 && !lo) s_ss[warp * kMvMaxRows + 4 * q + (g >> 1)] = v;
+    }
+  }
+}
+
+// Shared-memory carve-up of the small-batch GEMV kernel (the host sizes the
+// launch with the same arithmetic).
+struct MvSmem {
+  size_t w, in, gain, red, ss, rows, rope, total;
+};
+__host__ __device__ inline MvSmem mv_smem_layout(int kind, int S, int K, int rows_cap, int G, int d) {
+  MvSmem o;
+  size_t off = 0;
+  const size_t RS = (size_t)K * 2 + kMvRowPad;
+  o.w = off; off += (size_t)S * RS;
+  o.in = off; off += (size_t)rows_cap * K * 4;
+  o.gain = off; off += (kind == kQKV || kind == kGU || kind == kHeads) ? (size_t)K * 4 : 0;
+  const int RW = 4 * ((rows_cap + 3) / 4);
+  o.red = off; off += (size_t)kMvPhaseBlocks * kWarps * 16 * RW * 4;
+  o.ss = off; off += (size_t)kWarps * kMvMaxRows * 4;
+  o.rows = off; off += (size_t)((3 * rows_cap + 3) / 4 * 4) * 4;
+  o.rope = off; off += kind == kQKV && (size_t)G * (d / 2) * 8 <= (size_t)kRopeSmemBytes ? (size_t)kRopeSmemBytes : 0;
+  o.total = off;
+  return o;
+}
+
+// Kind two GEMVs ahead in the pass (QKV, O, GU, down per layer, then the
+// lm_heads), wrapping to the next pass.
+__device__ __forceinline__ void mv_ahead(const FrameParams& P, int kind, int l, int* kind2, int* l2) {
+  switch (kind) {
+    case kQKV: *kind2 = kGU; *l2 = l; break;
+    case kO: *kind2 = kDown; *l2 = l; break;
+    case kGU: if (l + 1 < P.L) { *kind2 = kQKV; *l2 = l + 1; } else { *kind2 = kHeads; *l2 = 0; } break;
+    case kDown: if (l + 1 < P.L) { *kind2 = kO; *l2 = l + 1; } else { *kind2 = kQKV; *l2 = 0; } break;
+    default: *kind2 = kO; *l2 = 0;
+  }
+}
+
+// One GEMV of the pass (lk = 8 * layer + kind; the kind is also the template
+// argument, so each kind compiles to straight-line code of its own).
+template <int KIND>
+__global__ void __launch_bounds__(kThreads, 2) mv_kernel(const __grid_constant__ FrameParams P, int lk) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  pdl_launch_dependents();
+  __shared__ MvShared sh;
+  const int l = lk >> 3;
+  constexpr bool kPair = KIND == kQKV || KIND == kGU;
+  constexpr bool kNormed = KIND == kQKV || KIND == kGU || KIND == kHeads;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int K = gemv_K(P, KIND);
+  const int RS = K * 2 + kMvRowPad;
+  const int S = P.mv_slots[KIND];
+  const int rows_cap = P.Bmax * P.NS;
+  const MvSmem L = mv_smem_layout(KIND, S, K, rows_cap, P.G, P.d);
+  unsigned char* wreg = smem + L.w;
+  float* in = reinterpret_cast<float*>(smem + L.in);
+  float* s_gain = reinterpret_cast<float*>(smem + L.gain);
+  float* red = reinterpret_cast<float*>(smem + L.red);
+  float* s_ss = reinterpret_cast<float*>(smem + L.ss);
+  int* s_rows = reinterpret_cast<int*>(smem + L.rows);
+  float2* s_rope = reinterpret_cast<float2*>(smem + L.rope);
+  const int RW = 4 * ((rows_cap + 3) / 4);
+  PassRows pr{s_rows, s_rows + rows_cap, s_rows + 2 * rows_cap};
+  const size_t rope_n = (size_t)P.G * (P.d / 2);
+  const bool rope_in_smem = KIND == kQKV && rope_n * sizeof(float2) <= (size_t)kRopeSmemBytes;
+  const float* gain_g = KIND == kQKV ? P.attn_norm[l] : (KIND == kGU ? P.ffn_norm[l] : (KIND == kHeads ? P.final_norm : nullptr));
+  const bool inputs_early = KIND == kQKV && l == 0;  // call inputs and embeddings: not written inside the pass
+  const bool need_heads = KIND == kHeads || (KIND == kGU && l == P.L - 1);
+
+  // ---------------- before the dependency wait: what no kernel of the pass writes
+  // (1) the weight tile: its shape depends on the model and the grid only
+  //     (the lm_heads also on the pass's heads, loaded first)
+  if (KIND != kHeads && warp == 0) {
+    if (lane == 0) {
+      mbar_init(&sh.wbar[0], 1);
+      mbar_init(&sh.wbar[1], 1);
+      mbar_init(&sh.ibar, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+      mv_build(P, sh, S, 0, KIND);
+    }
+    __syncwarp();
+    for (int p = 0; p < min(sh.nphase, sh.nbank); ++p) mv_issue_phase(P, l, sh, wreg, RS, p, KIND);
+    if (lane == 0) sh.issued = min(sh.nphase, sh.nbank);
+  }
+  // (2) every thread: the plan words, pass rows, call arguments, RoPE table
+  //     and norm gain, all loads in flight at once
+  if (tid < 2) sh.plan_w[tid] = __ldcg(tid == 0 ? &P.plan->nrows : &P.plan->nheads);
+  if (need_heads && tid >= 32 && tid < 32 + kMaxHeadsPerPass) sh.heads[tid - 32] = __ldcg(&P.plan->heads[tid - 32]);
+  if (tid >= 96 && tid < 96 + 3 * rows_cap) {
+    const int a = (tid - 96) / rows_cap, i = (tid - 96) - a * rows_cap;
+    s_rows[a * rows_cap + i] = __ldcg((a == 0 ? P.prow : (a == 1 ? P.ppos : P.pcode)) + i);
+  }
+  if (tid >= 128 && tid < 128 + (int)(sizeof(CallArgs) / 4))
+    reinterpret_cast<int*>(&sh.ca)[tid - 128] = __ldcg(reinterpret_cast<const int*>(P.call) + (tid - 128));
+  // RoPE table and norm gain: asynchronous 16-byte copies, all in flight at once
+  if (rope_in_smem)
+    for (int i = tid; i < (int)(rope_n / 2); i += kThreads) cp_async16(s_rope + 2 * i, P.rope + 2 * i);
+  if (gain_g != nullptr)
+    for (int i = tid; i < K / 4; i += kThreads) cp_async16(s_gain + 4 * i, gain_g + 4 * i);
+  cp_async_wait_all();
+  __syncthreads();
+  const int nrows = min(sh.plan_w[0], rows_cap);
+  if (warp == 0) {
+    if (lane == 0) {
+      sh.nrows = nrows;
+      sh.nheads = need_heads ? min(sh.plan_w[1], kMaxHeadsPerPass) : 0;
+      for (int r = 0; r < kMvMaxRows; ++r) sh.rbf[r] = (inputs_early && r < nrows && pr.ppos[r] > 0) ? 1 : 0;
+      if (KIND == kHeads) {
+        mbar_init(&sh.wbar[0], 1);
+        mbar_init(&sh.wbar[1], 1);
+        mbar_init(&sh.ibar, 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mv_build(P, sh, S, sh.nheads, KIND);
+      }
+    }
+    __syncwarp();
+    if (KIND == kHeads) {
+      for (int p = 0; p < min(sh.nphase, sh.nbank); ++p) mv_issue_phase(P, l, sh, wreg, RS, p, KIND);
+      if (lane == 0) sh.issued = min(sh.nphase, sh.nbank);
+    }
+    // input rows of layer 0 (x and code embeddings), one bulk copy each
+    if (inputs_early) {
+      if (lane == 0) {
+        uint32_t bytes = 0;
+        for (int r = 0; r < nrows; ++r) bytes += (uint32_t)K * (sh.rbf[r] ? 2u : 4u);
+        if (P.test_stall && blockIdx.x == 0) bytes += 16u;  // test hook: never completes
+        mbar_arrive_expect_tx(&sh.ibar, bytes);
+      }
+      __syncwarp();
+      if (lane < nrows) {
+        const ActRow a = act_row<__nv_bfloat16>(P, sh.ca, pr, KIND, l, lane);
+        const void* src = a.f != nullptr ? static_cast<const void*>(a.f) : a.w;
+        bulk_copy_g2s_plain(in + (size_t)lane * K, src, (uint32_t)K * (sh.rbf[lane] ? 2u : 4u), &sh.ibar);
+      }
+    }
+    // L2 prefetch for the GEMV two kernels ahead
+    int k2, l2;
+    mv_ahead(P, KIND, l, &k2, &l2);
+    mv_prefetch_l2(P, k2, l2, sh.heads, k2 == kHeads ? sh.nheads : 0);
+  }
+  pdl_wait();
+  // input rows written by the previous kernels of the pass: 16-byte
+  // asynchronous copies by every thread, all in flight at once
+  if (!inputs_early) {
+    const int k4 = K / 4;
+    for (int idx = tid; idx < nrows * k4; idx += kThreads) {
+      const int r = idx / k4, c = idx - r * k4;
+      cp_async16(in + (size_t)r * K + 4 * c, act_row<__nv_bfloat16>(P, sh.ca, pr, KIND, l, r).f + 4 * c);
+    }
+    cp_async_wait_all();
+  }
+  __syncthreads();  // sh.nrows, sh.rbf, the tile of the lm_heads, the input rows
+  const float2* rope = rope_in_smem ? s_rope : P.rope;
+  const float* gain = kNormed ? s_gain : nullptr;
+  // residual values the first phase's epilogue adds to (O, down), fetched now
+  float hold[2] = {0.0f, 0.0f};
+  if ((KIND == kO || KIND == kDown) && sh.nphase > 0 && nrows > 0) {
+    int it = tid;
+#pragma unroll
+    for (int m = 0; m < 2; ++m, it += kThreads) {
+      int rem = it;
+      for (int b = sh.ph[0]; b < sh.ph[1]; ++b) {
+        const int nu = sh.blk[b].n + sh.blk[b].n2, cnt = nu * nrows;
+        if (rem < cnt) {
+          const int i = rem / nrows, r = rem - i * nrows;
+          hold[m] = __ldcg(P.h + (size_t)pr.prow[r] * P.H + sh.blk[b].u + i);
+          break;
+        }
+        rem -= cnt;
+      }
+    }
+  }
+  bool ok = !inputs_early || mbar_wait_bounded(&sh.ibar, 0, &P.ctl->status, P.wait_ns);
+  ok = __syncthreads_and(ok ? 1 : 0) != 0;
+  int waited = 0;  // phases whose barrier has completed
+  if (ok && KIND == kQKV && l == 0) {
+    // the residual stream starts as the input rows: this CTA's slice of H
+    const int c0 = (int)(((long long)P.H * blockIdx.x) / gridDim.x), c1 = (int)(((long long)P.H * (blockIdx.x + 1)) / gridDim.x);
+    const int w = c1 - c0;
+    for (int it = tid; it < nrows * w; it += kThreads) {
+      const int i = it / w, k = c0 + (it - i * w);
+      const float v = sh.rbf[i] ? __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(in + (size_t)i * K)[k])
+                                : in[(size_t)i * K + k];
+      P.h[(size_t)pr.prow[i] * P.H + k] = v;
+    }
+  }
+  for (int p = 0; p < sh.nphase && ok; ++p) {
+    if (!mbar_wait_bounded(&sh.wbar[p & 1], (uint32_t)(p >> 1) & 1u, &P.ctl->status, P.wait_ns)) ok = false;
+    ok = __syncthreads_and(ok ? 1 : 0) != 0;
+    if (!ok) break;
+    waited = p + 1;
+    const int b0 = sh.ph[p], b1 = sh.ph[p + 1];
+    if (nrows > 4) mv_compute<2>(sh, wreg, RS, in, gain, red, s_ss, K, RW, b0, b1, kNormed && p == 0);
+    else mv_compute<1>(sh, wreg, RS, in, gain, red, s_ss, K, RW, b0, b1, kNormed && p == 0);
+    __syncthreads();
+    if (kNormed && p == 0) {
+      if (tid < nrows) {
+        float ts = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) ts += s_ss[w * kMvMaxRows + tid];
+        sh.inv[tid] = rsqrtf(ts / (float)K + P.eps);
+      }
+      __syncthreads();
+    }
+    // epilogue: per (unit, pass row), the warps' partial sums in warp order
+    int it = tid;
+    for (int m = 0;; ++m, it += kThreads) {
+      int rem = it, b = b0;
+      for (; b < b1; ++b) {
+        const int nu = kPair ? sh.blk[b].n : sh.blk[b].n + sh.blk[b].n2, cnt = nu * nrows;
+        if (rem < cnt) break;
+        rem -= cnt;
+      }
+      if (b >= b1) break;
+      const MvBlock B = sh.blk[b];
+      const int i = rem / nrows, r = rem - i * nrows;
+      const float* rbase = red + (size_t)(b - b0) * kWarps * 16 * RW;
+      float y0 = 0.0f, y1 = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kWarps; ++w) {
+        y0 += rbase[((size_t)w * 16 + i) * RW + r];
+        if (kPair) y1 += rbase[((size_t)w * 16 + i + 8) * RW + r];
+      }
+      if (kNormed) {
+        y0 *= sh.inv[r];
+        y1 *= sh.inv[r];
+      }
+      float ho = 0.0f;
+      if (KIND == kO || KIND == kDown) {
+        if (p == 0 && m < 2) ho = m == 0 ? hold[0] : hold[1];
+        else ho = __ldcg(P.h + (size_t)pr.prow[r] * P.H + B.u + i);
+      }
+      gemv_out<KIND>(P, l, sh.heads, pr, rope, B.u + i, r, y0, y1, ho);
+    }
+    __syncthreads();  // the partial sums and this phase's bank are free
+    if (warp == 0 && sh.nbank == 2 && p + 2 < sh.nphase) {
+      mv_issue_phase(P, l, sh, wreg, RS, p + 2, KIND);
+      if (lane == 0) sh.issued = p + 3;
+    }
+  }
+  if (!ok && tid == 0) {
+    // no copy may land after the CTA exits: wait (bounded) for every one in flight
+    for (int q = waited; q < sh.issued; ++q)
+      mbar_wait_bounded(&sh.wbar[q & 1], (uint32_t)(q >> 1) & 1u, &P.ctl->status, P.wait_ns);
+    if (inputs_early) mbar_wait_bounded(&sh.ibar, 0, &P.ctl->status, P.wait_ns);
   }
 }
 
 // ------------------------------------------------------------- attention
-// Causal GQA attention of one (pass row, query head) per CTA over positions
-// 0..pos of the stream's KV cache (this pass's rows were appended by the QKV
-// kernel): warp w scores positions w, w + kWarps, ... (the dot product split
-// over lanes, reduced by a butterfly) and parks their value rows in shared
-// memory; then warp 0 forms the softmax weights (denominator summed in index
-// order) and each output pair sums the weighted values in index order.
-__global__ void __launch_bounds__(kThreads, 2) attention_kernel(const __grid_constant__ FrameParams P, int l) {
+// Causal GQA attention over positions 0..pos of the stream's KV cache (this
+// pass's rows were appended by the QKV kernel), one CTA per (pass row, KV
+// group).  The row's plan entry is read before the dependency wait; after it
+// the group's K and V rows of positions 0..pos and the group's queries are
+// staged in shared memory by one round of asynchronous 16-byte copies.  Then
+// one warp per query head: lane j scores position j (and j + 32), the dot
+// product over the head dimensions taken in 4-element chunks starting at the
+// lane's own chunk (so the lanes of a quarter warp read distinct banks), a
+// fixed order per position; the weights exp(s_j - max) / den with den the
+// warp's butterfly sum; then each output pair sums the weighted value rows in
+// position order.  Every order depends on the position and the head shape
+// only, never on the other rows of the pass.
+constexpr int kAttnThreads = 128;
+__global__ void __launch_bounds__(kAttnThreads) attention_kernel(const __grid_constant__ FrameParams P, int l) {
   extern __shared__ __align__(16) float asmem[];
   pdl_launch_dependents();
-  pdl_wait();
-  const int nrows = __ldcg(&P.plan->nrows);
-  const int i = blockIdx.x / P.nq, hq = blockIdx.x - i * P.nq;
+  const int i = blockIdx.x / P.nkv, g = blockIdx.x - i * P.nkv;
+  const int nrows = __ldcg(&P.plan->nrows);  // written before the pass starts
   if (i >= nrows) return;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int d = P.d, grp = P.nq / P.nkv, lines = d / 2;
-  float* sc = asmem;       // [64] scores
-  float* vs = asmem + 64;  // [G][d] value rows
-  const float scale = 1.0f / sqrtf((float)d);
-  const int r = __ldcg(P.prow + i), pos = __ldcg(P.ppos + i), b = r / P.NS, g = hq / grp;
+  const int r = __ldcg(P.prow + i), pos = __ldcg(P.ppos + i), b = r / P.NS;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = kAttnThreads / 32;
+  const int d = P.d, grp = P.nq / P.nkv, d4 = d / 4, lines = d / 2;
+  const int np = pos + 1;
+  float* ks = asmem;                       // [np][d]
+  float* vs = ks + (size_t)P.G * d;        // [np][d]
+  float* qs = vs + (size_t)P.G * d;        // [grp][d]
+  float* ws = qs + (size_t)grp * d;        // [nw][64] softmax weights
   const size_t pstride = (size_t)P.nkv * d;
-  const float* qsrc = P.qbuf + (size_t)r * P.nq * d + (size_t)hq * d;
   const float* kb = P.kv + ((((size_t)b * P.L + l) * 2 + 0) * P.G) * pstride + (size_t)g * d;
-  const float* vb = P.kv + ((((size_t)b * P.L + l) * 2 + 1) * P.G) * pstride + (size_t)g * d;
-  float2 qv[4];
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    const int ln = lane + 32 * u;
-    qv[u] = ln < lines ? __ldcg(reinterpret_cast<const float2*>(qsrc) + ln) : make_float2(0.f, 0.f);
+  const float* vb = kb + (size_t)P.G * pstride;
+  const float* qb = P.qbuf + (size_t)r * P.nq * d + (size_t)g * grp * d;
+  pdl_wait();
+  for (int idx = tid; idx < np * d4; idx += kAttnThreads) {
+    const int j = idx / d4, c = idx - j * d4;
+    cp_async16(ks + (size_t)j * d + 4 * c, kb + (size_t)j * pstride + 4 * c);
+    cp_async16(vs + (size_t)j * d + 4 * c, vb + (size_t)j * pstride + 4 * c);
   }
-  for (int j = warp; j <= pos; j += kWarps) {
-    float part = 0.0f;
+  for (int idx = tid; idx < grp * d4; idx += kAttnThreads) cp_async16(qs + 4 * idx, qb + 4 * idx);
+  cp_async_wait_all();
+  __syncthreads();
+  const float scale = 1.0f / sqrtf((float)d);
+  float* w = ws + warp * CP_SPEC_MAX_CODE_GROUPS;
+  for (int hh = warp; hh < grp; hh += nw) {
+    const float* q = qs + (size_t)hh * d;
+    float sj[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+    for (int h2 = 0; h2 < 2; ++h2) {
+      const int j = lane + 32 * h2;
+      if (j > pos) continue;
+      const float* kj = ks + (size_t)j * d;
+      const int c0 = lane % d4;
+      float acc = 0.0f;
+      for (int cc = 0; cc < d4; ++cc) {
+        const int c = c0 + cc < d4 ? c0 + cc : c0 + cc - d4;
+        const float4 kv4 = *reinterpret_cast<const float4*>(kj + 4 * c);
+        const float4 q4 = *reinterpret_cast<const float4*>(q + 4 * c);
+        acc = fmaf(q4.x, kv4.x, acc);
+        acc = fmaf(q4.y, kv4.y, acc);
+        acc = fmaf(q4.z, kv4.z, acc);
+        acc = fmaf(q4.w, kv4.w, acc);
+      }
+      sj[h2] = acc * scale;
+    }
+    const float mx = warp_max(fmaxf(sj[0], sj[1]));
+    const float e0 = lane <= pos ? expf(sj[0] - mx) : 0.0f;
+    const float e1 = lane + 32 <= pos ? expf(sj[1] - mx) : 0.0f;
+    const float den = warp_sum(e0 + e1);
+    if (lane <= pos) w[lane] = e0 / den;
+    if (lane + 32 <= pos) w[lane + 32] = e1 / den;
+    __syncwarp();
+    float2 o[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) o[u] = make_float2(0.f, 0.f);
+    for (int j = 0; j <= pos; ++j) {
+      const float wj = w[j];
+      const float2* vj = reinterpret_cast<const float2*>(vs + (size_t)j * d);
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int ln = lane + 32 * u;
+        if (ln >= lines) continue;
+        const float2 v = vj[ln];
+        o[u].x = fmaf(wj, v.x, o[u].x);
+        o[u].y = fmaf(wj, v.y, o[u].y);
+      }
+    }
+    float2* dst = reinterpret_cast<float2*>(P.abuf + (size_t)r * P.nq * d + (size_t)(g * grp + hh) * d);
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const int ln = lane + 32 * u;
-      if (ln >= lines) continue;
-      const float2 kk = __ldcg(reinterpret_cast<const float2*>(kb + (size_t)j * pstride) + ln);
-      const float2 vv = __ldcg(reinterpret_cast<const float2*>(vb + (size_t)j * pstride) + ln);
-      part = fmaf(qv[u].x, kk.x, part);
-      part = fmaf(qv[u].y, kk.y, part);
-      *reinterpret_cast<float2*>(vs + (size_t)j * d + 2 * ln) = vv;
+      if (ln < lines) dst[ln] = o[u];
     }
-    const float sdot = warp_sum(part) * scale;
-    if (lane == 0) sc[j] = sdot;
-  }
-  __syncthreads();
-  // softmax weights by warp 0, one lane per position: e_j = exp(s_j - max),
-  // the denominator summed in index order, w_j = e_j / den (in place of s_j)
-  if (warp == 0) {
-    float mx = -INFINITY;
-    for (int j = lane; j <= pos; j += 32) mx = fmaxf(mx, sc[j]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    for (int j = lane; j <= pos; j += 32) sc[j] = expf(sc[j] - mx);
     __syncwarp();
-    float den = 0.0f;
-    if (lane == 0)
-      for (int j = 0; j <= pos; ++j) den += sc[j];
-    den = __shfl_sync(0xffffffffu, den, 0);
-    for (int j = lane; j <= pos; j += 32) sc[j] = sc[j] / den;
-  }
-  __syncthreads();
-  if (tid < lines) {
-    float2 o = make_float2(0.f, 0.f);
-    for (int j = 0; j <= pos; ++j) {
-      const float w = sc[j];
-      const float2 v = *reinterpret_cast<const float2*>(vs + (size_t)j * d + 2 * tid);
-      o.x = fmaf(w, v.x, o.x);
-      o.y = fmaf(w, v.y, o.y);
-    }
-    *reinterpret_cast<float2*>(P.abuf + (size_t)r * P.nq * d + (size_t)hq * d + 2 * tid) = o;
   }
 }
 
@@ -1888,15 +2492,33 @@ struct KernelSet {
   static const void* accept() { return (const void*)cpk::accept_kernel<WT>; }
 };
 
-// The tensor path exists for bf16 weights only (the host never sets tc for fp32).
-const void* gemv_fn(int dtype, int kind, bool tc = false) {
-  return dtype == 1 ? KernelSet<__nv_bfloat16>::gemv(kind, tc) : KernelSet<float>::gemv(kind, false);
+const void* mv_fn(int kind) {
+  switch (kind) {
+    case cpk::kQKV: return (const void*)cpk::mv_kernel<cpk::kQKV>;
+    case cpk::kO: return (const void*)cpk::mv_kernel<cpk::kO>;
+    case cpk::kGU: return (const void*)cpk::mv_kernel<cpk::kGU>;
+    case cpk::kDown: return (const void*)cpk::mv_kernel<cpk::kDown>;
+    default: return (const void*)cpk::mv_kernel<cpk::kHeads>;
+  }
+}
+
+// The GEMV kernel of a kind for a parameter block: the small-batch tensor
+// path (bf16, few rows), the many-row tensor path (bf16), or CUDA cores.
+const void* gemv_fn(const FrameParams& P, int kind) {
+  if (P.dtype == 1 && P.mv) return mv_fn(kind);
+  return P.dtype == 1 ? KernelSet<__nv_bfloat16>::gemv(kind, P.tc != 0) : KernelSet<float>::gemv(kind, false);
 }
 const void* setup_fn(int dtype) { return dtype == 1 ? KernelSet<__nv_bfloat16>::setup() : KernelSet<float>::setup(); }
 const void* accept_fn(int dtype) { return dtype == 1 ? KernelSet<__nv_bfloat16>::accept() : KernelSet<float>::accept(); }
 
+static int gemv_K_host(const FrameParams& P, int kind) {
+  return kind == cpk::kO ? P.nq * P.d : (kind == cpk::kDown ? P.F : P.H);
+}
+
 // Dynamic shared memory of each kernel for a parameter block.
 size_t gemv_smem(const FrameParams& P, int kind) {
+  if (P.dtype == 1 && P.mv)
+    return cpk::mv_smem_layout(kind, P.mv_slots[kind], gemv_K_host(P, kind), P.Bmax * P.NS, P.G, P.d).total;
   // two weight slots, the partial sums of one tile, the pass rows (3
   // arrays), then (QKV) the RoPE table and (normed kinds) the gain.  Sized
   // per kind so that consecutive kernels' CTAs fit on one SM together.
@@ -1908,11 +2530,67 @@ size_t gemv_smem(const FrameParams& P, int kind) {
   if (kind == cpk::kQKV || kind == cpk::kGU || kind == cpk::kHeads) b += cpk::kRopeSmemBytes + (size_t)P.H * sizeof(float);
   return b;
 }
-size_t attention_smem(const FrameParams& P) { return ((size_t)64 + (size_t)P.G * P.d) * sizeof(float); }
+size_t attention_smem(const FrameParams& P) {
+  return ((size_t)2 * P.G * P.d + (size_t)(P.nq / P.nkv) * P.d + (size_t)(cpk::kAttnThreads / 32) * CP_SPEC_MAX_CODE_GROUPS) *
+         sizeof(float);
+}
 size_t topk_smem(const FrameParams& P) {
   return ((size_t)P.V * 4 + 15) / 16 * 16 + (size_t)cpk::kWarps * 1024 + ((size_t)P.KC * 4 + 15) / 16 * 16 + 256;
 }
 size_t accept_smem(const FrameParams& P, int warps) { return (size_t)warps * cpk::accept_scratch_bytes(P.NS, P.KC); }
+
+// Small-batch tensor path: the weight-row slots of each GEMV kind, or false
+// when the shape does not fit it (then the context keeps the other paths).
+// A kind whose per-CTA tile fits the weight budget holds it whole (one
+// phase, every row copied before the dependency wait); a larger tile (the
+// lm_heads) streams through two banks.
+constexpr size_t kMvWeightBudget = 100 * 1024;   // weight region of one CTA
+constexpr size_t kMvSmemLimit = 220 * 1024;      // dynamic shared memory of one CTA
+bool plan_mv(FrameParams& P, int sms) {
+  const int rows_cap = P.Bmax * P.NS;
+  if (P.dtype != 1 || rows_cap > cpk::kMvMaxRows || sms < 1) return false;
+  const int Ks[3] = {P.H, P.nq * P.d, P.F};
+  for (int K : Ks)
+    if (K % (32 * cpk::kWarps) != 0) return false;  // each warp's K slice: whole 32-element blocks
+  for (int kind = cpk::kQKV; kind <= cpk::kHeads; ++kind) {
+    const int K = gemv_K_host(P, kind);
+    const size_t RS = (size_t)K * 2 + cpk::kMvRowPad;
+    const int rpu = (kind == cpk::kQKV || kind == cpk::kGU) ? 2 : 1;
+    long long U;
+    switch (kind) {
+      case cpk::kQKV: U = (long long)(P.nq + 2 * P.nkv) * (P.d / 2); break;
+      case cpk::kO: case cpk::kDown: U = P.H; break;
+      case cpk::kGU: U = P.F; break;
+      default: U = (long long)std::min(P.G - 1, cpk::kMaxHeadsPerPass) * P.V;
+    }
+    const long long need = (U + sms - 1) / sms * rpu;  // rows of the largest tile
+    long long S = std::min<long long>(need, (long long)(kMvWeightBudget / RS));
+    if (S < need) S = std::max<long long>(S / 2 * 2, 4);
+    while (S >= 4 && cpk::mv_smem_layout(kind, (int)S, K, rows_cap, P.G, P.d).total > kMvSmemLimit) S -= 2;
+    if (S < 4 || (S < need && S / 2 < rpu)) return false;
+    P.mv_slots[kind] = (int)S;
+  }
+  P.mv = 1;
+  return true;
+}
+
+// Raise (never lower) a kernel's dynamic shared-memory limit on the current
+// device.  Contexts and the allocation-free path share the kernels; a limit
+// set for a smaller configuration must not shrink it under a graph that an
+// earlier, larger configuration instantiated.
+static std::mutex g_attr_mu;
+static std::map<std::pair<int, const void*>, size_t> g_smem_high;
+static cudaError_t raise_smem_limit(const void* fn, size_t bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_attr_mu);
+  size_t& high = g_smem_high[std::make_pair(dev, fn)];
+  if (bytes <= high) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e == cudaSuccess) high = bytes;
+  return e;
+}
 
 // Raise the dynamic shared-memory limit of every pass kernel of a dtype.
 cudaError_t configure_kernels(const FrameParams& P, int accept_warps) {
@@ -1921,25 +2599,18 @@ cudaError_t configure_kernels(const FrameParams& P, int accept_warps) {
   // SM configuration never changes between consecutive kernels and a
   // dependent's CTA can start beside its predecessor's
   for (int k = cpk::kQKV; k <= cpk::kHeads && e == cudaSuccess; ++k) {
-    e = cudaFuncSetAttribute(gemv_fn(P.dtype, k, P.tc != 0), cudaFuncAttributeMaxDynamicSharedMemorySize, (int)gemv_smem(P, k));
+    e = raise_smem_limit(gemv_fn(P, k), gemv_smem(P, k));
     if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(gemv_fn(P.dtype, k, P.tc != 0), cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
+      e = cudaFuncSetAttribute(gemv_fn(P, k), cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
   }
   const void* others[] = {(const void*)cpk::attention_kernel, (const void*)cpk::topk_kernel, setup_fn(P.dtype),
                           accept_fn(P.dtype)};
   for (const void* f : others)
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute((const void*)cpk::attention_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)attention_smem(P));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute((const void*)cpk::topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)topk_smem(P));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(setup_fn(P.dtype), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)accept_smem(P, accept_warps));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(accept_fn(P.dtype), cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)accept_smem(P, accept_warps));
+  if (e == cudaSuccess) e = raise_smem_limit((const void*)cpk::attention_kernel, attention_smem(P));
+  if (e == cudaSuccess) e = raise_smem_limit((const void*)cpk::topk_kernel, topk_smem(P));
+  if (e == cudaSuccess) e = raise_smem_limit(setup_fn(P.dtype), accept_smem(P, accept_warps));
+  if (e == cudaSuccess) e = raise_smem_limit(accept_fn(P.dtype), accept_smem(P, accept_warps));
   return e;
 }
 
@@ -1970,22 +2641,29 @@ cudaError_t enqueue_setup(const FrameParams& P, int accept_warps, cudaStream_t s
 cudaError_t enqueue_pass(const FrameParams& P, int sms, int accept_warps, cudaStream_t s) {
   cudaError_t e = cudaSuccess;
   bool first = true;
-  int l = 0;
-  void* gargs[] = {const_cast<FrameParams*>(&P), &l};
+  int l = 0, arg = 0;
+  void* gargs[] = {const_cast<FrameParams*>(&P), &arg};
   void* pargs[] = {const_cast<FrameParams*>(&P)};
   const int rows = P.Bmax * P.NS;
+  // a GEMV of one kind: the small-batch kernel takes 8 * layer + kind
+  auto gemv = [&](int kind, bool pdl) {
+    arg = P.mv ? 8 * l + kind : l;
+    return launch(gemv_fn(P, kind), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, kind), s, pdl, gargs);
+  };
   for (l = 0; l < P.L && e == cudaSuccess; ++l) {
-    e = launch(gemv_fn(P.dtype, cpk::kQKV, P.tc != 0), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kQKV), s, !first, gargs);
+    e = gemv(cpk::kQKV, !first);
     first = false;
-    if (e == cudaSuccess)
-      e = launch((const void*)cpk::attention_kernel, dim3(rows * P.nq), dim3(cpk::kThreads), attention_smem(P), s, true,
+    if (e == cudaSuccess) {
+      arg = l;
+      e = launch((const void*)cpk::attention_kernel, dim3(rows * P.nkv), dim3(cpk::kAttnThreads), attention_smem(P), s, true,
                  gargs);
-    if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kO, P.tc != 0), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kO), s, true, gargs);
-    if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kGU, P.tc != 0), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kGU), s, true, gargs);
-    if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kDown, P.tc != 0), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kDown), s, true, gargs);
+    }
+    if (e == cudaSuccess) e = gemv(cpk::kO, true);
+    if (e == cudaSuccess) e = gemv(cpk::kGU, true);
+    if (e == cudaSuccess) e = gemv(cpk::kDown, true);
   }
   l = 0;
-  if (e == cudaSuccess) e = launch(gemv_fn(P.dtype, cpk::kHeads, P.tc != 0), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, cpk::kHeads), s, true, gargs);
+  if (e == cudaSuccess) e = gemv(cpk::kHeads, true);
   if (e == cudaSuccess)
     e = launch((const void*)cpk::topk_kernel, dim3(rows * (1 + P.ND)), dim3(cpk::kThreads), topk_smem(P), s, true, pargs);
   if (e == cudaSuccess) {

@@ -26,6 +26,7 @@ size_t accept_smem(const cpk::FrameParams& P, int warps);
 cudaError_t launch_init_tables(float2* rope, int G, int d, double theta, int* top_k, float* temp, int Bmax, int k,
                                float T, cudaStream_t stream);
 cudaError_t launch_offset_table(const cpk::FrameParams& P, cudaStream_t stream);
+bool plan_mv(cpk::FrameParams& P, int sms);
 cudaError_t launch_accept_batch(int R, int N, int V, int k, float T, unsigned long long seed, int mode,
                                 const float* tgt, const float* drf, int* tokens, int* nacc, int* drafts,
                                 cudaStream_t stream);
@@ -170,7 +171,9 @@ cp_spec_status check_shapes(const cp_spec_model* m, int N, int KC) {
   const size_t maxk = (size_t)std::max(std::max(H, QD), F) * eb / 16;
   if (maxk > (size_t)kMaxChunksPerRow)
     return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "GEMV width %zu bytes above %d", maxk * 16, kMaxChunksPerRow * 16);
-  if (m->num_code_groups > 64 || (size_t)(64 + m->num_code_groups * m->head_dim) * 4 > kSmemPerSm)
+  if (m->num_code_groups > 64 ||
+      ((size_t)2 * m->num_code_groups * m->head_dim + (size_t)(m->n_q_heads / m->n_kv_heads) * m->head_dim + 4 * 64) * 4 >
+          kSmemPerSm)
     return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "attention scratch too large");
   // partial sums of one GEMV tile: rows x 8 input rows x warps per row group
   // (the kernel's tile and row-group geometry, restated)
@@ -238,6 +241,10 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
   // not on the pass, so a stream's results do not depend on its batch-mates
   P.tc = (model->dtype == 1 && config->max_streams * NS >= kTcMinRows && model->hidden % 32 == 0 &&
           model->ffn % 32 == 0 && (model->n_q_heads * model->head_dim) % 32 == 0) ? 1 : 0;
+  P.mv = 0;
+  if (!P.tc) cpk_host::plan_mv(P, dp.sms);  // bf16 contexts with at most 8 row slots
+  P.wait_ns = cpk::kDefaultWaitNs;
+  P.test_stall = 0;
   P.seed = config->seed;
   P.cond = 0;
   const long long eb = model->dtype == 1 ? 2 : 4;
@@ -561,8 +568,8 @@ cp_spec_status cp_spec_decode_frames_static(const cp_spec_model* model, const cp
                 lay.total, (size_t)CP_SPEC_STATIC_SCRATCH_BYTES);
   if (n_frames == 0) return CP_SPEC_OK;
   if (!d_x || !d_c0 || !d_codes || !aligned16(d_x) || !aligned16(d_c0) || !aligned16(d_codes) ||
-      (d_status && !aligned16(d_status)))
-    return fail(nullptr, CP_SPEC_E_INVALID, "x/c0/codes null, or a pointer not 16-byte aligned");
+      (d_status && ((uintptr_t)d_status & 3u) != 0))
+    return fail(nullptr, CP_SPEC_E_INVALID, "x/c0/codes null or not 16-byte aligned, or d_status not 4-byte aligned");
   DevicePlan dp;
   v = plan_device(model, config, N, &dp);
   if (v != CP_SPEC_OK) return v;
@@ -654,6 +661,23 @@ cp_spec_status cp_spec_reset_stats(cp_spec_ctx* c, void* stream) {
   if (e == cudaSuccess)
     e = cudaMemsetAsync(&c->base.ctl->weight_bytes, 0, cpk::kControlCounters * sizeof(long long), s);
   return check_cuda(c, e, "reset stats");
+}
+
+cp_spec_status cp_spec_test_hooks(cp_spec_ctx* c, uint64_t wait_limit_ns, int32_t stall_first_wait) {
+  if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "null context");
+  if (wait_limit_ns < 10000ull || wait_limit_ns > 60ull * 1000000000ull)
+    return fail(c, CP_SPEC_E_INVALID, "wait_limit_ns must be in [1e4, 6e10]");
+  if (stall_first_wait != 0 && stall_first_wait != 1) return fail(c, CP_SPEC_E_INVALID, "stall_first_wait must be 0 or 1");
+  // the parameter block is part of the call graph: drop the graph (rebuilt on the next call)
+  if (c->graph) {
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = cudaGraphExecDestroy(c->graph);
+    c->graph = nullptr;
+    if (e != cudaSuccess) return check_cuda(c, e, "graph release");
+  }
+  c->base.wait_ns = wait_limit_ns;
+  c->base.test_stall = stall_first_wait;
+  return CP_SPEC_OK;
 }
 
 int64_t cp_spec_launch_count(const cp_spec_ctx* c) {
