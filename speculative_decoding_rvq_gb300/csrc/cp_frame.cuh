@@ -110,6 +110,9 @@ struct FrameParams {
   int adapt_min;  // ... or while it has fewer reached drafts than this
   int mv;         // bf16 GEMVs on the small-batch tensor-core path (at most kMvMaxRows row slots)
   int mv_slots[5];  // small-batch path: weight-row slots of shared memory per GEMV kind
+  int t5;           // bf16 GEMVs as tcgen05 tiles (contexts with many rows per pass)
+  int t5_rb[5];     // ... pass rows per CTA tile, per GEMV kind (16, 32 or 64)
+  int t5_stages[5]; // ... stages of the weight / input ring, per GEMV kind
   int test_stall;   // test hook: one bounded wait of the first GEMV of a pass never completes
   unsigned long long wait_ns;         // limit of every bounded device-side wait
   unsigned long long seed;

@@ -1543,6 +1543,8 @@ __global__ void __launch_bounds__(kThreads, 2) mv_kernel(const __grid_constant__
   }
 }
 
+#include "cp_t5.cuh"
+
 // ------------------------------------------------------------- attention
 // Causal GQA attention over positions 0..pos of the stream's KV cache (this
 // pass's rows were appended by the QKV kernel), one CTA per (pass row, KV
@@ -2502,9 +2504,21 @@ const void* mv_fn(int kind) {
   }
 }
 
+const void* t5_fn(int kind) {
+  switch (kind) {
+    case cpk::kQKV: return (const void*)cpk::t5_kernel<cpk::kQKV>;
+    case cpk::kO: return (const void*)cpk::t5_kernel<cpk::kO>;
+    case cpk::kGU: return (const void*)cpk::t5_kernel<cpk::kGU>;
+    case cpk::kDown: return (const void*)cpk::t5_kernel<cpk::kDown>;
+    default: return (const void*)cpk::t5_kernel<cpk::kHeads>;
+  }
+}
+
 // The GEMV kernel of a kind for a parameter block: the small-batch tensor
-// path (bf16, few rows), the many-row tensor path (bf16), or CUDA cores.
+// path (bf16, few rows), the tcgen05 tiles (bf16, many rows), the mma.sync
+// tensor path (bf16, many rows, shapes the tiles do not take), or CUDA cores.
 const void* gemv_fn(const FrameParams& P, int kind) {
+  if (P.dtype == 1 && P.t5) return t5_fn(kind);
   if (P.dtype == 1 && P.mv) return mv_fn(kind);
   return P.dtype == 1 ? KernelSet<__nv_bfloat16>::gemv(kind, P.tc != 0) : KernelSet<float>::gemv(kind, false);
 }
@@ -2517,6 +2531,8 @@ static int gemv_K_host(const FrameParams& P, int kind) {
 
 // Dynamic shared memory of each kernel for a parameter block.
 size_t gemv_smem(const FrameParams& P, int kind) {
+  if (P.dtype == 1 && P.t5)
+    return cpk::t5_smem_layout(kind, P.t5_rb[kind], P.t5_stages[kind], gemv_K_host(P, kind), P.Bmax * P.NS, P.G, P.d).total;
   if (P.dtype == 1 && P.mv)
     return cpk::mv_smem_layout(kind, P.mv_slots[kind], gemv_K_host(P, kind), P.Bmax * P.NS, P.G, P.d).total;
   // two weight slots, the partial sums of one tile, the pass rows (3
@@ -2572,6 +2588,53 @@ bool plan_mv(FrameParams& P, int sms) {
   }
   P.mv = 1;
   return true;
+}
+
+// Units of a GEMV kind with the most lm_heads a pass can apply.
+static long long gemv_units_max(const FrameParams& P, int kind) {
+  switch (kind) {
+    case cpk::kQKV: return (long long)(P.nq + 2 * P.nkv) * (P.d / 2);
+    case cpk::kO: case cpk::kDown: return P.H;
+    case cpk::kGU: return P.F;
+    default: return (long long)std::min(P.G - 1, cpk::kMaxHeadsPerPass) * P.V;
+  }
+}
+
+// tcgen05 tiles: pass rows per tile and ring stages of each GEMV kind, or
+// false when the shape does not fit them (every GEMV width a multiple of the
+// 64-element slab; a tile of the lm_heads inside one head).  The rows per
+// tile (64, 32 or 16) minimise waves of one CTA per SM x the work of a tile
+// (a fixed part per slab plus the conversion of its rows) for a full pass;
+// the ring takes as many stages as fit the shared-memory budget.
+constexpr size_t kT5SmemBudget = 200 * 1024;
+bool plan_t5(FrameParams& P, int sms) {
+  const int rows_cap = P.Bmax * P.NS;
+  if (P.dtype != 1 || sms < 1 || P.H % 64 != 0 || (P.nq * P.d) % 64 != 0 || P.F % 64 != 0 || P.V % cpk::kT5M != 0 ||
+      P.d % 2 != 0)
+    return false;
+  for (int kind = cpk::kQKV; kind <= cpk::kHeads; ++kind) {
+    const int K = gemv_K_host(P, kind);
+    const long long mtiles = cpk::t5_mtiles(kind, (int)gemv_units_max(P, kind));
+    int RB = 16;
+    long long best = -1;
+    for (int rb : {64, 32, 16}) {
+      const long long waves = (mtiles * ((rows_cap + rb - 1) / rb) + sms - 1) / sms;
+      const long long cost = waves * (32 + rb);
+      if (best < 0 || cost < best) { best = cost; RB = rb; }
+    }
+    int st = cpk::kT5MaxStages;
+    while (st > 3 && cpk::t5_smem_layout(kind, RB, st, K, rows_cap, P.G, P.d).total > kT5SmemBudget) --st;
+    if (cpk::t5_smem_layout(kind, RB, st, K, rows_cap, P.G, P.d).total > kT5SmemBudget || mtiles > 65535) return false;
+    P.t5_rb[kind] = RB;
+    P.t5_stages[kind] = st;
+  }
+  P.t5 = 1;
+  return true;
+}
+
+static dim3 t5_grid(const FrameParams& P, int kind) {
+  const int rows_cap = P.Bmax * P.NS, RB = P.t5_rb[kind];
+  return dim3((rows_cap + RB - 1) / RB, cpk::t5_mtiles(kind, (int)gemv_units_max(P, kind)));
 }
 
 // Raise (never lower) a kernel's dynamic shared-memory limit on the current
@@ -2647,6 +2710,10 @@ cudaError_t enqueue_pass(const FrameParams& P, int sms, int accept_warps, cudaSt
   const int rows = P.Bmax * P.NS;
   // a GEMV of one kind: the small-batch kernel takes 8 * layer + kind
   auto gemv = [&](int kind, bool pdl) {
+    if (P.t5) {
+      arg = l;
+      return launch(gemv_fn(P, kind), t5_grid(P, kind), dim3(cpk::kT5Threads), gemv_smem(P, kind), s, pdl, gargs);
+    }
     arg = P.mv ? 8 * l + kind : l;
     return launch(gemv_fn(P, kind), dim3(sms), dim3(cpk::kThreads), gemv_smem(P, kind), s, pdl, gargs);
   };

@@ -27,6 +27,7 @@ cudaError_t launch_init_tables(float2* rope, int G, int d, double theta, int* to
                                float T, cudaStream_t stream);
 cudaError_t launch_offset_table(const cpk::FrameParams& P, cudaStream_t stream);
 bool plan_mv(cpk::FrameParams& P, int sms);
+bool plan_t5(cpk::FrameParams& P, int sms);
 cudaError_t launch_accept_batch(int R, int N, int V, int k, float T, unsigned long long seed, int mode,
                                 const float* tgt, const float* drf, int* tokens, int* nacc, int* drafts,
                                 cudaStream_t stream);
@@ -242,7 +243,9 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
   P.tc = (model->dtype == 1 && config->max_streams * NS >= kTcMinRows && model->hidden % 32 == 0 &&
           model->ffn % 32 == 0 && (model->n_q_heads * model->head_dim) % 32 == 0) ? 1 : 0;
   P.mv = 0;
+  P.t5 = 0;
   if (!P.tc) cpk_host::plan_mv(P, dp.sms);  // bf16 contexts with at most 8 row slots
+  else cpk_host::plan_t5(P, dp.sms);        // tcgen05 tiles where the shape fits them
   P.wait_ns = cpk::kDefaultWaitNs;
   P.test_stall = 0;
   P.seed = config->seed;
