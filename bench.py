@@ -253,7 +253,7 @@ def run_gpu(args, rank, world):
 
     if rank == 0 and not args.no_sweep:
         result["sweep"] = sweep(cp_factory=lambda n: binding.CpSpec(spec, dw, n, TOP_K, TEMP, SEED, 1),
-                                xd=xd[:200], cd=cd[:200], G=spec.num_code_groups, peak=peak)
+                                xd=xd, cd=cd, G=spec.num_code_groups, peak=peak)
         result["accept_microbench"] = accept_microbench(peak)
         result["batched"] = batched(spec, dw, peak)
         result["draft_offsets"] = offsets_line(spec, dw, xd[:200], cd[:200], peak)
@@ -262,12 +262,12 @@ def run_gpu(args, rank, world):
     return result
 
 
-def large_line(peak, frames=16, batched_frames=4):
+def large_line(peak, frames=256):
     """The large model (H 2048, 8 layers, 32 q / 8 kv heads x 64, FFN 6144, V 4096, G 32: 31
-    lm_heads of 16.8 MB), T 0.8, top-k 50: at one stream over `frames` frames the AR loop,
-    N = 4, and N = 4 with the adaptive window; then N = 4 at 8 and 64 streams (tensor-core
-    GEMVs) over `batched_frames` frames.  codes/s, time per pass and the algorithmic HBM
-    fraction."""
+    lm_heads of 16.8 MB), T 0.8, top-k 50, `frames` frames per stream: at one stream the AR
+    loop, N = 4, and N = 4 with the adaptive window; then N = 4 at 8, 64 and 256 streams
+    (tcgen05 GEMV tiles).  One warm-up decode of 4 frames, then the timed decode.  codes/s,
+    time per pass and the algorithmic HBM fraction."""
     import torch
     from speculative_decoding_rvq_gb300 import binding, synth as S
     spec = S.LARGE_BF16
@@ -277,13 +277,13 @@ def large_line(peak, frames=16, batched_frames=4):
     # N4_adaptive: the per-stream adaptive window (keep an offset at >= 30 % acceptance,
     # judged after 16 reached drafts)
     for name, n, pct, B in (("N0", 0, 0, 1), ("N4", 4, 0, 1), ("N4_adaptive", 4, 30, 1), ("N4_B8", 4, 0, 8),
-                            ("N4_B64", 4, 0, 64)):
-        F = frames if B == 1 else batched_frames
+                            ("N4_B64", 4, 0, 64), ("N4_B256", 4, 0, 256)):
+        F = frames
         x, c0 = S.gen_frames(spec, B, F, seed=SEED)
         xd, cd = torch.from_numpy(x).cuda(), torch.from_numpy(c0).cuda()
         cp = binding.CpSpec(spec, dw, n, TOP_K, 0.8, SEED, B, adapt_pct=pct, adapt_min=16)
         codes = torch.empty((F, B, G), dtype=torch.int32, device="cuda")
-        cp.decode_frames(xd, cd, codes)
+        cp.decode_frames(xd[:4], cd[:4], codes[:4])
         torch.cuda.synchronize()
         cp.status()
         cp.reset_stats()
@@ -328,19 +328,19 @@ def offsets_line(spec, dw, xd, cd, peak, K=3):
 
 
 def sweep(cp_factory, xd, cd, G, peak, windows=(0, 2, 3, 4, 5, 6, 7, 8)):
-    """codes/s and per-pass time for the AR loop (N=0) and windows 2..8 on 200 frames."""
+    """codes/s and per-pass time for the AR loop (N=0) and windows 2..8 on the frames of
+    xd (one warm-up decode, then two timed)."""
     import torch
     out = {}
     F = xd.shape[0]
     for n in windows:
         cp = cp_factory(n)
         codes = torch.empty((F, 1, G), dtype=torch.int32, device="cuda")
-        for _ in range(2):
-            cp.decode_frames(xd, cd, codes)
+        cp.decode_frames(xd, cd, codes)
         torch.cuda.synchronize()
         cp.reset_stats()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        reps = 3
+        reps = 2
         a.record()
         for _ in range(reps):
             cp.decode_frames(xd, cd, codes)
@@ -357,7 +357,7 @@ def sweep(cp_factory, xd, cd, G, peak, windows=(0, 2, 3, 4, 5, 6, 7, 8)):
     return out
 
 
-def batched(spec, dw, peak, streams=64, frames=100):
+def batched(spec, dw, peak, streams=64, frames=500):
     """The batched configuration: `streams` concurrent streams (ragged accept counts and KV
     lengths arise on their own), N=4, half the streams greedy and half top-k 50 / T 0.9,
     `frames` frames each.  max_streams = streams, so the GEMV kernels take the tensor-core
@@ -374,7 +374,7 @@ def batched(spec, dw, peak, streams=64, frames=100):
     tt[: streams // 2] = 0.0
     cp.set_stream_sampling(tk, tt)
     codes = torch.empty((frames, streams, G), dtype=torch.int32, device="cuda")
-    cp.decode_frames(xd, cd, codes)
+    cp.decode_frames(xd[:4], cd[:4], codes[:4])
     torch.cuda.synchronize()
     cp.reset_stats()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -413,8 +413,23 @@ def expected_accepted(tgt, drf, k: int, T: float) -> float:
     return float(torch.cumprod(beta, dim=1).sum(1).mean().item())
 
 
+def expected_accepted_greedy(tgt, drf) -> float:
+    """Greedy mode: a draft is accepted while the argmax of its draft row equals the argmax
+    of the target row at the same position, so the mean accepted count is the mean length
+    of the agreeing prefix (ties between equal maxima have probability zero for these
+    continuous inputs)."""
+    import torch
+    n = drf.shape[1]
+    eq = (drf.argmax(-1) == tgt[:, :n].argmax(-1)).to(torch.float64)
+    return float(torch.cumprod(eq, dim=1).sum(1).mean().item())
+
+
 def accept_microbench(peak):
-    """Acceptance kernels alone: 65536 rounds, V 2048, rho 0.7, top-k 50, T 0.9 (logit mode);
+    """Acceptance kernels alone (the acceptance-kernel microbench configuration): 65536
+    independent rounds, V 2048, target logits N(0, 3^2), draft logits
+    rho * target + sqrt(1 - rho^2) * N(0, 3^2) for rho in {0.3, 0.7, 0.95}, N in {2, 4, 8},
+    top-k 50; sampling mode (T 0.9, Philox draws) and greedy mode (T 0, argmax equality).
+    Each line: rounds/s, the logit bytes read per second against the measured HBM peak, and
     the mean accepted drafts per round beside its closed form for the same inputs."""
     import torch
     from speculative_decoding_rvq_gb300 import binding
@@ -423,28 +438,35 @@ def accept_microbench(peak):
     g = torch.Generator(device="cuda").manual_seed(1)
     for N in (2, 4, 8):
         tgt = torch.randn((R, N, V), device="cuda", generator=g) * 3.0
-        drf = 0.7 * tgt[:, : N - 1] + (1 - 0.49) ** 0.5 * torch.randn((R, N - 1, V), device="cuda", generator=g) * 3.0
-        drf = drf.contiguous()
-        for _ in range(3):
-            binding.accept_batch(tgt, drf, TOP_K, TEMP, SEED, 0)
-        torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        reps = 5
-        for _ in range(reps):
-            tok, na, _ = binding.accept_batch(tgt, drf, TOP_K, TEMP, SEED, 0)
-        b.record()
-        torch.cuda.synchronize()
-        ms = a.elapsed_time(b) / reps
-        gbs = (2 * N - 1) * V * 4 * R / (ms / 1e3) / 1e9
-        res[f"N{N}"] = {"rounds_per_s": round(R / (ms / 1e3), 1), "ms": round(ms, 3), "GB_s": round(gbs, 1),
+        for rho in (0.3, 0.7, 0.95):
+            drf = rho * tgt[:, : N - 1] + (1 - rho * rho) ** 0.5 * torch.randn((R, N - 1, V), device="cuda",
+                                                                               generator=g) * 3.0
+            drf = drf.contiguous()
+            for mode, T in (("sampling", TEMP), ("greedy", 0.0)):
+                for _ in range(3):
+                    binding.accept_batch(tgt, drf, TOP_K, T, SEED, 0)
+                torch.cuda.synchronize()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                reps = 5
+                for _ in range(reps):
+                    tok, na, _ = binding.accept_batch(tgt, drf, TOP_K, T, SEED, 0)
+                b.record()
+                torch.cuda.synchronize()
+                ms = a.elapsed_time(b) / reps
+                gbs = (2 * N - 1) * V * 4 * R / (ms / 1e3) / 1e9
+                line = {"rounds_per_s": round(R / (ms / 1e3), 1), "ms": round(ms, 3), "GB_s": round(gbs, 1),
                         "hbm_frac": round(gbs / peak, 4),
                         "mean_accepted": round(float(na.float().mean().item()), 4)}
-        try:
-            res[f"N{N}"]["closed_form_accepted"] = round(expected_accepted(tgt, drf, TOP_K, TEMP), 4)
-        except Exception as exc:  # analysis only: never lose the measured line over it
-            res[f"N{N}"]["closed_form_accepted"] = f"unavailable: {type(exc).__name__}"
-        del tgt, drf
+                try:
+                    line["closed_form_accepted"] = round(
+                        expected_accepted(tgt, drf, TOP_K, TEMP) if T > 0 else expected_accepted_greedy(tgt, drf), 4)
+                except Exception as exc:  # analysis only: never lose the measured line over it
+                    line["closed_form_accepted"] = f"unavailable: {type(exc).__name__}"
+                res[f"N{N}_rho{rho}_{mode}"] = line
+            del drf
+        del tgt
+        torch.cuda.empty_cache()
     return res
 
 
@@ -472,7 +494,7 @@ def oracle_codes_per_s(frames: int, window: int, model=None, first_frame: int = 
 
 def cpu_baseline_entry(frames=3):
     v, dt = oracle_codes_per_s(frames, WINDOW)
-    return {"value": round(v, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+    return {"value": round(v, 3), "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{frames} frames of the 1-stream workload (N={WINDOW}), {dt:.1f} s single-threaded"}
 
 
@@ -494,7 +516,7 @@ def run_reference(args, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * statistics.mean(times), 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": dict(workload_config(S.TTS06B_BF16, FRAMES, 1, WINDOW), parallelism="cpu oracle, 1 thread"),
-        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "kind": "oracle",
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": 1, "host_cores": os.cpu_count(), "kind": "oracle",
                          "sample": f"{spec_frames} frames per step of the 1-stream workload"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }

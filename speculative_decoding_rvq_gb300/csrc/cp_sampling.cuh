@@ -56,17 +56,15 @@ __device__ __forceinline__ void warp_stage_row(float* dst, const float* __restri
   __syncwarp();
 }
 
-// Processes one row of V float32 logits with one warp.  keys: warp-private
-// scratch of V uint32 (the row is staged there, then replaced by its keys);
-// hist: warp-private 256 uint32; ebuf: warp-private min(k, V) floats;
-// out_idx / out_prob: capacity min(k, V) (1 when T == 0).
+// Processes one row of V float32 logits, already staged in `keys`, with one
+// warp.  keys: warp-private scratch of V uint32 holding the row (replaced by
+// its keys); hist: warp-private 256 uint32; ebuf: warp-private min(k, V)
+// floats; out_idx / out_prob: capacity min(k, V) (1 when T == 0).
 // Returns the list length (all lanes).
-static __device__ __noinline__ int warp_process_row(const float* __restrict__ logits, int V, int k, float T,
-                                                    uint32_t* keys, uint32_t* hist, float* ebuf, int* out_idx,
-                                                    float* out_prob) {
+static __device__ __noinline__ int warp_process_staged(uint32_t* keys, int V, int k, float T, uint32_t* hist,
+                                                       float* ebuf, int* out_idx, float* out_prob) {
   const int lane = threadIdx.x & 31;
   float* row = reinterpret_cast<float*>(keys);
-  warp_stage_row(row, logits, V);
   if (T == 0.0f) {
     float best = -INFINITY;
     int bi = 0x7fffffff;
@@ -176,6 +174,15 @@ static __device__ __noinline__ int warp_process_row(const float* __restrict__ lo
   for (int p = lane; p < kk; p += 32) out_prob[p] = __fdiv_rn(ebuf[p], S);
   __syncwarp();
   return kk;
+}
+
+// Stages one row of V float32 logits into `keys` and processes it (see
+// warp_process_staged).
+static __device__ __noinline__ int warp_process_row(const float* __restrict__ logits, int V, int k, float T,
+                                                    uint32_t* keys, uint32_t* hist, float* ebuf, int* out_idx,
+                                                    float* out_prob) {
+  warp_stage_row(reinterpret_cast<float*>(keys), logits, V);
+  return warp_process_staged(keys, V, k, T, hist, ebuf, out_idx, out_prob);
 }
 
 // Builds the support list of a dense probability row (entries > 0) in index
