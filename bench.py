@@ -257,6 +257,7 @@ def run_gpu(args, rank, world):
         result["accept_microbench"] = accept_microbench(peak)
         result["batched"] = batched(spec, dw, peak)
         result["draft_offsets"] = offsets_line(spec, dw, xd[:200], cd[:200], peak)
+        result["sparse_tree"] = tree_line(spec, dw, xd[:200], cd[:200], peak)
         if not args.no_large:
             result["large"] = large_line(peak)
     return result
@@ -324,6 +325,46 @@ def offsets_line(spec, dw, xd, cd, peak, K=3):
         r = sweep(factory, xd, cd, spec.num_code_groups, peak, windows=(4,))["N4"]
         r["accepted_by_offset"] = made[-1].last_stats["accepted_by_offset"][1:4]
         out[name] = r
+    return out
+
+
+TREE_SHAPES = {
+    # parent, rank per node (parents first): rank r of depth t = the r-th largest draft logit of head_{s+t}
+    "chain3": ([-1, 0, 1], [0, 0, 0]),
+    "sparse7": ([-1, -1, 0, 0, 1, 2, 3], [0, 1, 0, 1, 0, 0, 0]),
+    "wide15": ([-1, -1, -1, 0, 0, 1, 2, 3, 3, 4, 5, 6, 7, 8, 9], [0, 1, 2, 0, 1, 0, 0, 0, 1, 0, 0, 0, 0, 0, 0]),
+}
+
+
+def tree_line(spec, dw, xd, cd, peak):
+    """Sparse-tree rounds on the frames of xd (1 stream), top-k 50, T 0.9: per tree shape
+    codes/s, passes per frame, time per pass, mean committed codes per round and the
+    acceptance by depth."""
+    import torch
+    from speculative_decoding_rvq_gb300 import binding
+    out = {"frames": int(xd.shape[0]), "shapes": {k: {"parent": v[0], "rank": v[1]} for k, v in TREE_SHAPES.items()}}
+    G = spec.num_code_groups
+    F = xd.shape[0]
+    for name, (par, rk) in TREE_SHAPES.items():
+        cp = binding.CpSpec(spec, dw, 4, TOP_K, TEMP, SEED, 1, tree=(par, rk))
+        codes = torch.empty((F, 1, G), dtype=torch.int32, device="cuda")
+        cp.decode_frames(xd[:4], cd[:4], codes[:4])
+        torch.cuda.synchronize()
+        cp.reset_stats()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        cp.decode_frames(xd, cd, codes)
+        b.record()
+        torch.cuda.synchronize()
+        cp.status()
+        ms = a.elapsed_time(b)
+        st = cp.stats()
+        out[name] = {"nodes": len(par), "codes_per_s": round(F * (G - 1) / (ms / 1e3), 1),
+                     "passes_per_frame": round(st["passes"] / F, 3), "us_per_pass": round(ms * 1e3 / st["passes"], 2),
+                     "codes_per_round": round((F * (G - 2)) / max(st["rounds"], 1), 3),
+                     "accepted_by_depth": st["accepted_by_offset"][1:4],
+                     "hbm_frac": round((st["weight_bytes"] + st["kv_bytes"]) / (ms / 1e3) / 1e9 / peak, 4)}
+        cp.close()
     return out
 
 

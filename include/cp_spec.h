@@ -192,6 +192,47 @@ cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* w
                             const cp_spec_config* config, void* d_workspace, size_t workspace_bytes,
                             cp_spec_ctx** out);
 
+/* Sparse draft tree ("RVQ Position Aware Speculative Decoding for On Device
+ * TTS", section 2.2 "tree attention / sparse tree attention", Figure 2).
+ * HOST arrays of n entries (1 <= n <= 62), nodes listed parents first:
+ * parent[i] is -1 for a child of the committed code, else an earlier node;
+ * rank[i] is the rank of the node's token among the draft logits of its
+ * depth (value descending, index ascending; 0 = the largest), below
+ * min(top_k rounded up to a multiple of 4, vocab).  Siblings come in
+ * ascending rank without repeats; depth at most CP_SPEC_MAX_WINDOW - 1.
+ * The arrays are read during the call only. */
+typedef struct {
+  int32_t n;
+  const int32_t* parent;
+  const int32_t* rank;
+} cp_spec_tree;
+
+/* Workspace bytes of a tree context (0 if the arguments are invalid). */
+size_t cp_spec_workspace_bytes_tree(const cp_spec_model* model, const cp_spec_config* config,
+                                    const cp_spec_tree* tree);
+
+/* cp_spec_init for tree rounds instead of chain rounds: every round drafts
+ * the tree's nodes (node i carries the rank[i]-th draft logit of head_{s+d}
+ * on h_s, d its depth; nodes deeper than the codes left are dropped),
+ * verifies the committed code and every node short of the frame end in one
+ * pass (each node attends to the prefix and to its own ancestors), and walks
+ * the tree from the committed code: the children of a node are tested in
+ * rank order as point-mass drafts against the node's target law (accept
+ * child c iff u < p'(c), p' the remaining mass renormalised; Philox purpose
+ * 4 + the child's index among those tested), and one code is drawn from what
+ * remains when none is accepted (purpose TARGET).  Every committed code keeps
+ * the autoregressive law; under temperature 0 the codes equal greedy
+ * autoregressive decoding.  config->verify_window, adapt_accept_pct and
+ * adapt_min_reached are ignored (the tree fixes the drafts); draft_offsets
+ * applies to depths 1..K.  The accepted path's K/V rows are copied from the
+ * nodes' slots to their positions: the one place a round moves cache data.
+ * Decode with cp_spec_decode_frames / cp_spec_begin_frame + cp_spec_round as
+ * for chain contexts.  Errors as cp_spec_init, plus CP_SPEC_E_INVALID for a
+ * malformed tree or fewer than 3 code groups. */
+cp_spec_status cp_spec_init_tree(const cp_spec_model* model, const cp_spec_weights* weights,
+                                 const cp_spec_config* config, const cp_spec_tree* tree, void* d_workspace,
+                                 size_t workspace_bytes, cp_spec_ctx** out);
+
 /* Per-stream sampling overrides, HOST arrays of n entries (n <= max_streams):
  * top_k in 1..config.top_k, temperature 0 (greedy) or in [1e-3, 100].
  * Synchronous (small host-to-device copy). */

@@ -25,7 +25,8 @@ E_INVALID, E_UNSUPPORTED, E_CUDA, E_WORKSPACE, E_DEVICE_TIMEOUT, E_STATE, E_DEVI
 EXPORTS = ("cp_spec_workspace_bytes", "cp_spec_init", "cp_spec_set_stream_sampling", "cp_spec_decode_frames",
            "cp_spec_begin_frame", "cp_spec_round", "cp_spec_teacher_logits", "cp_spec_accept_batch",
            "cp_spec_status_word", "cp_spec_read_stats", "cp_spec_reset_stats", "cp_spec_launch_count",
-           "cp_spec_last_error", "cp_spec_destroy", "cp_spec_decode_frames_static", "cp_spec_test_hooks")
+           "cp_spec_last_error", "cp_spec_destroy", "cp_spec_decode_frames_static", "cp_spec_test_hooks",
+           "cp_spec_workspace_bytes_tree", "cp_spec_init_tree")
 
 
 class CpSpecError(RuntimeError):
@@ -50,6 +51,10 @@ class Config(C.Structure):
     _fields_ = [("verify_window", C.c_int32), ("top_k", C.c_int32), ("temperature", C.c_float),
                 ("seed", C.c_uint64), ("max_streams", C.c_int32), ("draft_offsets", C.c_int32),
                 ("adapt_accept_pct", C.c_int32), ("adapt_min_reached", C.c_int32)]
+
+
+class Tree(C.Structure):
+    _fields_ = [("n", C.c_int32), ("parent", C.c_void_p), ("rank", C.c_void_p)]
 
 
 class Stats(C.Structure):
@@ -79,6 +84,9 @@ def load():
     L.cp_spec_workspace_bytes.argtypes = [vp, vp]
     L.cp_spec_workspace_bytes.restype = sz
     L.cp_spec_init.argtypes = [vp, vp, vp, vp, sz, C.POINTER(vp)]
+    L.cp_spec_workspace_bytes_tree.argtypes = [vp, vp, vp]
+    L.cp_spec_workspace_bytes_tree.restype = sz
+    L.cp_spec_init_tree.argtypes = [vp, vp, vp, vp, vp, sz, C.POINTER(vp)]
     L.cp_spec_set_stream_sampling.argtypes = [vp, i32, vp, vp]
     L.cp_spec_decode_frames.argtypes = [vp, i32, i32, i32, vp, vp, vp, vp]
     L.cp_spec_begin_frame.argtypes = [vp, i32, vp, vp, i32, vp]
@@ -96,7 +104,7 @@ def load():
     L.cp_spec_last_error.restype = C.c_char_p
     L.cp_spec_destroy.argtypes = [vp]
     L.cp_spec_destroy.restype = None
-    for name in ("cp_spec_init", "cp_spec_set_stream_sampling", "cp_spec_decode_frames", "cp_spec_begin_frame",
+    for name in ("cp_spec_init", "cp_spec_init_tree", "cp_spec_set_stream_sampling", "cp_spec_decode_frames", "cp_spec_begin_frame",
                  "cp_spec_round", "cp_spec_teacher_logits", "cp_spec_accept_batch", "cp_spec_status_word",
                  "cp_spec_read_stats", "cp_spec_reset_stats", "cp_spec_decode_frames_static", "cp_spec_test_hooks"):
         getattr(L, name).restype = C.c_int
@@ -162,7 +170,11 @@ class CpSpec:
     """One context of the CUDA library over device-resident weights."""
 
     def __init__(self, spec: synth.ModelSpec, device_weights: dict, verify_window: int, top_k: int,
-                 temperature: float, seed: int, max_streams: int = 1, adapt_pct: int = 0, adapt_min: int = 16):
+                 temperature: float, seed: int, max_streams: int = 1, adapt_pct: int = 0, adapt_min: int = 16,
+                 tree=None):
+        """tree: None (chain rounds of verify_window), or (parent, rank) sequences of a sparse
+        draft tree (cp_spec_init_tree; verify_window and the adaptive window are then ignored)."""
+        import numpy as np
         import torch
         self.lib = load()
         self.spec = spec
@@ -171,13 +183,27 @@ class CpSpec:
         self.weights = weights_struct(device_weights)
         self.config = Config(verify_window, top_k, temperature, seed, max_streams, n_draft_offsets(device_weights),
                              adapt_pct, adapt_min)
-        nbytes = self.lib.cp_spec_workspace_bytes(C.byref(self.model), C.byref(self.config))
+        self.tree = None
+        if tree is not None:
+            par = np.ascontiguousarray(tree[0], dtype=np.int32)
+            rk = np.ascontiguousarray(tree[1], dtype=np.int32)
+            self._tree_arrays = (par, rk)  # kept alive for the call
+            self.tree = Tree(len(par), par.ctypes.data, rk.ctypes.data)
+            nbytes = self.lib.cp_spec_workspace_bytes_tree(C.byref(self.model), C.byref(self.config),
+                                                           C.byref(self.tree))
+        else:
+            nbytes = self.lib.cp_spec_workspace_bytes(C.byref(self.model), C.byref(self.config))
         if nbytes == 0:
             _check(E_INVALID)
         self.workspace = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
         ctx = C.c_void_p()
-        rc = self.lib.cp_spec_init(C.byref(self.model), C.byref(self.weights), C.byref(self.config),
-                                   C.c_void_p(_ptr(self.workspace)), nbytes, C.byref(ctx))
+        if self.tree is not None:
+            rc = self.lib.cp_spec_init_tree(C.byref(self.model), C.byref(self.weights), C.byref(self.config),
+                                            C.byref(self.tree), C.c_void_p(_ptr(self.workspace)), nbytes,
+                                            C.byref(ctx))
+        else:
+            rc = self.lib.cp_spec_init(C.byref(self.model), C.byref(self.weights), C.byref(self.config),
+                                       C.c_void_p(_ptr(self.workspace)), nbytes, C.byref(ctx))
         _check(rc, None, allow=(OK, W_AR_FALLBACK))
         self.ar_fallback = rc == W_AR_FALLBACK
         self.ctx = ctx

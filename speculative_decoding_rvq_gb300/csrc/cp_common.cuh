@@ -26,7 +26,7 @@ struct Philox {
   }
 };
 
-enum : uint32_t { kDraft = 0, kAccept = 1, kTarget = 2 };
+enum : uint32_t { kDraft = 0, kAccept = 1, kTarget = 2, kTreeAccept = 4 /* + child index */ };
 
 // u in [0, 1): top 24 bits of word 0, exact in float32.
 __device__ __forceinline__ float philox_uniform(uint64_t seed, uint32_t stream, uint32_t frame,

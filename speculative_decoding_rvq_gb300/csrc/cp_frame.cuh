@@ -94,6 +94,24 @@ struct CallArgs {
   float* t_draft;        // [B][P-1][ND][V] or null
 };
 
+// Sparse draft tree of a context ("RVQ Position Aware Speculative Decoding
+// for On Device TTS", section 2.2, Figure 2): node i has parent[i] (-1: a
+// child of the committed code, else an earlier node) and rank[i], the rank
+// of its token among its depth's draft logits (value descending, index
+// ascending); siblings come in ascending rank.  Derived on the host: dep[i]
+// (1 for a child of the committed code), anc[i] (bit j set for every
+// ancestor j of i and for i itself), need[t] (1 + the largest rank at depth
+// t) and dmax (the deepest node).
+constexpr int kTreeMaxNodes = 62;
+struct TreeTab {
+  int n, dmax;
+  int parent[64];
+  int rank[64];
+  int dep[64];
+  unsigned long long anc[64];
+  int need[CP_SPEC_MAX_WINDOW + 1];
+};
+
 struct FrameParams {
   // model
   int H, L, nq, nkv, d, F, V, G, dtype;
@@ -114,6 +132,8 @@ struct FrameParams {
   int t5_rb[5];     // ... pass rows per CTA tile, per GEMV kind (16, 32 or 64)
   int t5_stages[5]; // ... stages of the weight / input ring, per GEMV kind
   int test_stall;   // test hook: one bounded wait of the first GEMV of a pass never completes
+  int tree_n;       // sparse-tree rounds: nodes of the tree (0 = chain rounds)
+  int GS;           // KV slots per stream and layer: G canonical positions, then tree_n node slots
   unsigned long long wait_ns;         // limit of every bounded device-side wait
   unsigned long long seed;
   unsigned long long cond;            // graph conditional handle of the pass loop (0 = none)
@@ -150,6 +170,10 @@ struct FrameParams {
   int* prow;       // [Bmax*NS] the pass's active row slots, ascending
   int* ppos;       // [Bmax*NS] their positions
   int* pcode;      // [Bmax*NS] their input codes
+  int* row_slot;   // [Bmax*NS] KV slot of the row (its position, or G + node index for a tree node)
+  int* pslot;      // [Bmax*NS] the pass's rows' KV slots
+  int* ttok;       // [Bmax][64] tree rounds: the token of each node of the stream's current tree
+  const TreeTab* tree;  // tree rounds: the tree (device copy)
   Plan* plan;
   StreamState* st; // [Bmax]
   StreamStats* sstats;  // [Bmax]
@@ -161,32 +185,37 @@ struct FrameParams {
 };
 
 // Staged probability lists of one stream in the accept kernel: the target
-// lists of its NS row slots, the ND saved draft lists q_t, and the ND draft
-// slots of each row (the next pass's candidates).
-inline __host__ __device__ int accept_lists(int NS) {
-  const int ND = NS > 2 ? NS - 1 : 1;  // NS = max(N, 2); ND slots per row (at least one list of room)
-  return NS + ND + NS * ND;
+// lists of NSr row slots, NDr saved draft lists q_t, and the NDr draft
+// slots of each row (the next pass's candidates).  Chain rounds: NSr = NS =
+// max(N, 2), NDr = max(NS - 1, 1).  Tree rounds: NSr = 2 (the walk's
+// current list, and the frame prefill's rows), NDr = max(depth, 1).
+inline __host__ __device__ int accept_rows(int NS, int tree_n) { return tree_n > 0 ? 2 : NS; }
+inline __host__ __device__ int accept_drafts(int NS, int ND, int tree_n) {
+  return tree_n > 0 ? (ND > 1 ? ND : 1) : (NS > 2 ? NS - 1 : 1);
 }
+inline __host__ __device__ int accept_lists(int NSr, int NDr) { return NSr + NDr + NSr * NDr; }
 
 // Per-warp shared scratch of the accept kernel: the stream state, the staged
 // lists (index and probability arrays of capacity KC), one list of residual
 // weights, 32 uniforms and the list lengths.
-inline __host__ __device__ size_t accept_scratch_bytes(int NS, int KC) {
-  const size_t n = (size_t)accept_lists(NS);
+inline __host__ __device__ size_t accept_scratch_bytes(int NSr, int NDr, int KC) {
+  const size_t n = (size_t)accept_lists(NSr, NDr);
   return (sizeof(StreamState) + n * KC * 8 + (size_t)KC * 4 + 32 * 4 + n * 4 + 15) / 16 * 16;
 }
 
 // Workspace carve-up, computed identically by the host for sizing.
 struct Layout {
   size_t h, qbuf, abuf, fbuf, kv, logits, otab, lidx, lprob, lcount, qidx, qprob, qcount, row_pos, row_code, prow, ppos,
-      pcode, plan, st, sstats, rope, top_k, temp, ctl, call, total;
+      pcode, row_slot, pslot, ttok, tree, plan, st, sstats, rope, top_k, temp, ctl, call, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-inline Layout make_layout(int H, int L, int nq, int nkv, int d, int F, int V, int G, int N, int KC, int Bmax,
-                          int KO) {
-  const int NS = N > 2 ? N : 2, ND = N > 1 ? N - 1 : 0, NDq = ND > 0 ? ND : 1;
+// NS row slots per stream, ND draft slots per row, GS KV slots per stream
+// and layer (chain rounds: NS = max(N, 2), ND = max(N - 1, 0), GS = G).
+inline Layout make_layout(int H, int L, int nq, int nkv, int d, int F, int V, int G, int NS, int ND, int GS, int KC,
+                          int Bmax, int KO) {
+  const int NDq = ND > 0 ? ND : 1;
   const size_t rows = (size_t)Bmax * NS;
   Layout o{};
   size_t off = 0;
@@ -195,7 +224,7 @@ inline Layout make_layout(int H, int L, int nq, int nkv, int d, int F, int V, in
   o.qbuf = take(4 * rows * nq * d);
   o.abuf = take(4 * rows * nq * d);
   o.fbuf = take(4 * rows * F);
-  o.kv = take(4 * (size_t)Bmax * L * 2 * G * nkv * d);
+  o.kv = take(4 * (size_t)Bmax * L * 2 * GS * nkv * d);
   o.logits = take(4 * rows * (1 + ND) * V);
   o.otab = take(4 * (size_t)(G - 1) * KO * V);
   o.lidx = take(sizeof(int) * rows * (1 + ND) * KC);
@@ -209,6 +238,10 @@ inline Layout make_layout(int H, int L, int nq, int nkv, int d, int F, int V, in
   o.prow = take(sizeof(int) * rows);
   o.ppos = take(sizeof(int) * rows);
   o.pcode = take(sizeof(int) * rows);
+  o.row_slot = take(sizeof(int) * rows);
+  o.pslot = take(sizeof(int) * rows);
+  o.ttok = take(sizeof(int) * (size_t)Bmax * 64);
+  o.tree = take(sizeof(TreeTab));
   o.plan = take(sizeof(Plan));
   o.st = take(sizeof(StreamState) * (size_t)Bmax);
   o.sstats = take(sizeof(StreamStats) * (size_t)Bmax);

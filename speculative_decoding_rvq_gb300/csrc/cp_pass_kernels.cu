@@ -306,12 +306,14 @@ __device__ __forceinline__ void gemv_out(const FrameParams& P, int l, const int*
         qd[e] = r0;
         qd[e + half] = r1;
       } else {
-        float* kd = P.kv + (((((size_t)b * P.L + l) * 2 + 0) * P.G + pos) * P.nkv + (hh - P.nq)) * P.d;
+        const int slot = P.tree_n ? __ldcg(P.pslot + gi) : pos;  // KV slot (a tree node's own slot)
+        float* kd = P.kv + (((((size_t)b * P.L + l) * 2 + 0) * P.GS + slot) * P.nkv + (hh - P.nq)) * P.d;
         kd[e] = r0;
         kd[e + half] = r1;
       }
     } else {
-      float* vd = P.kv + (((((size_t)b * P.L + l) * 2 + 1) * P.G + pos) * P.nkv + (hh - P.nq - P.nkv)) * P.d;
+      const int slot = P.tree_n ? __ldcg(P.pslot + gi) : pos;
+      float* vd = P.kv + (((((size_t)b * P.L + l) * 2 + 1) * P.GS + slot) * P.nkv + (hh - P.nq - P.nkv)) * P.d;
       vd[e] = y0;
       vd[e + half] = y1;
     }
@@ -1546,18 +1548,24 @@ __global__ void __launch_bounds__(kThreads, 2) mv_kernel(const __grid_constant__
 #include "cp_t5.cuh"
 
 // ------------------------------------------------------------- attention
-// Causal GQA attention over positions 0..pos of the stream's KV cache (this
-// pass's rows were appended by the QKV kernel), one CTA per (pass row, KV
-// group).  The row's plan entry is read before the dependency wait; after it
-// the group's K and V rows of positions 0..pos and the group's queries are
-// staged in shared memory by one round of asynchronous 16-byte copies.  Then
-// one warp per query head: lane j scores position j (and j + 32), the dot
-// product over the head dimensions taken in 4-element chunks starting at the
-// lane's own chunk (so the lanes of a quarter warp read distinct banks), a
-// fixed order per position; the weights exp(s_j - max) / den with den the
-// warp's butterfly sum; then each output pair sums the weighted value rows in
-// position order.  Every order depends on the position and the head shape
-// only, never on the other rows of the pass.
+// Causal GQA attention of one pass row over its keys in the stream's KV
+// cache (this pass's rows were appended by the QKV kernel), one CTA per
+// (pass row, KV group).  The keys of a chain row at position pos are the
+// canonical positions 0..pos.  A tree node's row ("RVQ Position Aware
+// Speculative Decoding for On Device TTS", section 2.2, sparse tree
+// attention) sees the canonical positions 0..base (the committed prefix and
+// the round's root row, base = pos - depth) and then the slots of its
+// ancestors and of itself, in node order, which along one path is position
+// order.  The row's plan entry is read before the dependency wait; after it
+// the group's K and V rows of the keys and the group's queries are staged in
+// shared memory by one round of asynchronous 16-byte copies.  Then one warp
+// per query head: lane j scores key j (and j + 32), the dot product over the
+// head dimensions taken in 4-element chunks starting at the lane's own chunk
+// (so the lanes of a quarter warp read distinct banks), a fixed order per
+// key; the weights exp(s_j - max) / den with den the warp's butterfly sum;
+// then each output pair sums the weighted value rows in key order.  Every
+// order depends on the keys and the head shape only, never on the other rows
+// of the pass.
 constexpr int kAttnThreads = 128;
 __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const __grid_constant__ FrameParams P, int l) {
   extern __shared__ __align__(16) float asmem[];
@@ -1565,23 +1573,42 @@ __global__ void __launch_bounds__(kAttnThreads) attention_kernel(const __grid_co
   const int i = blockIdx.x / P.nkv, g = blockIdx.x - i * P.nkv;
   const int nrows = __ldcg(&P.plan->nrows);  // written before the pass starts
   if (i >= nrows) return;
-  const int r = __ldcg(P.prow + i), pos = __ldcg(P.ppos + i), b = r / P.NS;
+  const int r = __ldcg(P.prow + i), b = r / P.NS;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = kAttnThreads / 32;
   const int d = P.d, grp = P.nq / P.nkv, d4 = d / 4, lines = d / 2;
-  const int np = pos + 1;
+  // keys: canonical 0..base, then (tree node rows) the ancestor-or-self slots
+  int base = __ldcg(P.ppos + i);
+  unsigned long long anc = 0;
+  if (P.tree_n) {
+    const int slot = __ldcg(P.pslot + i);
+    if (slot >= P.G) {
+      const int node = slot - P.G;
+      base -= __ldg(&P.tree->dep[node]);
+      anc = __ldg(&P.tree->anc[node]);
+    }
+  }
+  const int np = base + 1 + __popcll(anc);
+  const int pos = np - 1;                  // index of the last key (the row itself)
   float* ks = asmem;                       // [np][d]
   float* vs = ks + (size_t)P.G * d;        // [np][d]
   float* qs = vs + (size_t)P.G * d;        // [grp][d]
   float* ws = qs + (size_t)grp * d;        // [nw][64] softmax weights
   const size_t pstride = (size_t)P.nkv * d;
-  const float* kb = P.kv + ((((size_t)b * P.L + l) * 2 + 0) * P.G) * pstride + (size_t)g * d;
-  const float* vb = kb + (size_t)P.G * pstride;
+  const float* kb = P.kv + ((((size_t)b * P.L + l) * 2 + 0) * P.GS) * pstride + (size_t)g * d;
+  const float* vb = kb + (size_t)P.GS * pstride;
   const float* qb = P.qbuf + (size_t)r * P.nq * d + (size_t)g * grp * d;
   pdl_wait();
   for (int idx = tid; idx < np * d4; idx += kAttnThreads) {
     const int j = idx / d4, c = idx - j * d4;
-    cp_async16(ks + (size_t)j * d + 4 * c, kb + (size_t)j * pstride + 4 * c);
-    cp_async16(vs + (size_t)j * d + 4 * c, vb + (size_t)j * pstride + 4 * c);
+    // key j's KV slot: j itself up to base, then the (j - base - 1)-th set bit of anc
+    int sj = j;
+    if (j > base) {
+      unsigned long long m = anc;
+      for (int q = j - base - 1; q > 0; --q) m &= m - 1;
+      sj = P.G + __ffsll((long long)m) - 1;
+    }
+    cp_async16(ks + (size_t)j * d + 4 * c, kb + (size_t)sj * pstride + 4 * c);
+    cp_async16(vs + (size_t)j * d + 4 * c, vb + (size_t)sj * pstride + 4 * c);
   }
   for (int idx = tid; idx < grp * d4; idx += kAttnThreads) cp_async16(qs + 4 * idx, qb + 4 * idx);
   cp_async_wait_all();
@@ -1819,8 +1846,12 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(const __grid_constant
     for (int v = threadIdx.x; v < P.V; v += kThreads) reinterpret_cast<float*>(keys)[v] = __ldcg(src + v);
   }
   __syncthreads();
-  const int n = block_topk(P.V, __ldg(P.top_k + b), __ldg(P.temp + b), keys, hw, ebuf, sx, P.lidx + li * P.KC,
-                           P.lprob + li * P.KC);
+  // tree rounds: a draft slot keeps the need[t] largest raw logits (candidate
+  // ranks do not depend on the temperature; T = 1 leaves z = logit exactly)
+  const bool rank_slot = P.tree_n > 0 && t > 0;
+  const int kk = rank_slot ? __ldg(&P.tree->need[t]) : __ldg(P.top_k + b);
+  const float TT = rank_slot ? 1.0f : __ldg(P.temp + b);
+  const int n = block_topk(P.V, kk, TT, keys, hw, ebuf, sx, P.lidx + li * P.KC, P.lprob + li * P.KC);
   if (threadIdx.x == 0) P.lcount[li] = n;
 }
 
@@ -1838,10 +1869,11 @@ constexpr int kMirrorRows = 64;
 __shared__ int g_mirror_on;
 __shared__ int g_mpos[kMirrorRows];
 __shared__ int g_mcode[kMirrorRows];
+__shared__ int g_mslot[kMirrorRows];
 
 __device__ __forceinline__ void mirror_init(const FrameParams& P, const CallArgs& ca) {
   if (threadIdx.x == 0) g_mirror_on = (gridDim.x == 1 && ca.B * P.NS <= kMirrorRows) ? 1 : 0;
-  for (int i = threadIdx.x; i < kMirrorRows; i += blockDim.x) { g_mpos[i] = -1; g_mcode[i] = 0; }
+  for (int i = threadIdx.x; i < kMirrorRows; i += blockDim.x) { g_mpos[i] = -1; g_mcode[i] = 0; g_mslot[i] = 0; }
   __syncthreads();
 }
 
@@ -1852,13 +1884,15 @@ template <typename WT>
 __device__ __noinline__ void set_pass_rows(const FrameParams& P, int b, const StreamState& S, const int* codes_in) {
   const int lane = threadIdx.x & 31;
   __syncwarp();
-  if (lane < P.NS) {
-    const int on = lane < S.m;
-    P.row_pos[b * P.NS + lane] = on ? S.pos0 + lane : -1;
-    P.row_code[b * P.NS + lane] = on ? codes_in[lane] : 0;
+  for (int k = lane; k < P.NS; k += 32) {  // rows at consecutive positions from pos0, KV slot = position
+    const int on = k < S.m;
+    P.row_pos[b * P.NS + k] = on ? S.pos0 + k : -1;
+    P.row_code[b * P.NS + k] = on ? codes_in[k] : 0;
+    P.row_slot[b * P.NS + k] = on ? S.pos0 + k : 0;
     if (g_mirror_on) {
-      g_mpos[b * P.NS + lane] = on ? S.pos0 + lane : -1;
-      g_mcode[b * P.NS + lane] = on ? codes_in[lane] : 0;
+      g_mpos[b * P.NS + k] = on ? S.pos0 + k : -1;
+      g_mcode[b * P.NS + k] = on ? codes_in[k] : 0;
+      g_mslot[b * P.NS + k] = on ? S.pos0 + k : 0;
     }
   }
   if (lane == 0) {
@@ -1986,8 +2020,9 @@ struct AcceptScratch {
 
 __device__ __forceinline__ AcceptScratch accept_scratch(const FrameParams& P, unsigned char* base_all) {
   const int warp = threadIdx.x >> 5;
-  const int n = accept_lists(P.NS);
-  unsigned char* base = base_all + (size_t)warp * accept_scratch_bytes(P.NS, P.KC);
+  const int NSr = accept_rows(P.NS, P.tree_n), NDr = accept_drafts(P.NS, P.ND, P.tree_n);
+  const int n = accept_lists(NSr, NDr);
+  unsigned char* base = base_all + (size_t)warp * accept_scratch_bytes(NSr, NDr, P.KC);
   AcceptScratch a;
   a.S = reinterpret_cast<StreamState*>(base);
   a.idx = reinterpret_cast<int*>(base + sizeof(StreamState));
@@ -1995,8 +2030,8 @@ __device__ __forceinline__ AcceptScratch accept_scratch(const FrameParams& P, un
   a.r = a.prob + (size_t)n * P.KC;
   a.u = a.r + P.KC;
   a.cnt = reinterpret_cast<int*>(a.u + 32);
-  a.NS = P.NS;
-  a.NDr = P.NS > 2 ? P.NS - 1 : 1;
+  a.NS = NSr;
+  a.NDr = NDr;
   return a;
 }
 
@@ -2155,6 +2190,9 @@ __device__ void accept_prefetch(const FrameParams& P, int b, AcceptScratch& A) {
   __syncwarp();
 }
 
+template <typename WT>
+__device__ void accept_stream_tree(const FrameParams& P, const CallArgs& ca, int b, AcceptScratch& A);
+
 // The acceptance decision of stream b for the pass that just ran ("Speculative
 // Decoding, Beyond Text", section 02; "CodePredictor Speculative Decoding",
 // "How a round works" step 3), then the next pass's rows.  Warp-wide, after
@@ -2178,6 +2216,10 @@ __device__ void accept_stream(const FrameParams& P, const CallArgs& ca, int b, A
     if (next >= ca.P) retire_stream(P, b, S);
     else setup_teacher_chunk<WT>(P, ca, b, S);
     store_state(P, b, S);
+    return;
+  }
+  if (P.tree_n) {
+    accept_stream_tree<WT>(P, ca, b, A);
     return;
   }
   // Stage the lists this decision reads (the saved draft lists q_t of a
@@ -2288,6 +2330,216 @@ __device__ void accept_stream(const FrameParams& P, const CallArgs& ca, int b, A
   store_state(P, b, S);
 }
 
+// ------------------------------------------------------- sparse-tree rounds
+// "RVQ Position Aware Speculative Decoding for On Device TTS", section 2.2
+// and Figure 2.  The drafts of depth t are the ranked candidates of
+// head_{s+t} on h_s: node i carries the rank[i]-th largest draft logit of its
+// depth (value descending, index ascending).  One pass verifies the round's
+// root row (position s + 1, the committed code c_s) and a row per kept node
+// short of the frame end (position s + 1 + depth, its own KV slot G + i,
+// attending to the prefix and its ancestors).  The walk then starts at the
+// root: at a node with target law p, its children are tested in rank order
+// as point-mass drafts (accept child c iff u < p'(c) with p' the remaining
+// mass renormalised, else remove c); a node without an accepted child
+// draws one code from what remains (a correction, or the bonus), so every
+// committed code keeps the autoregressive law.
+
+// Nodes of the tree kept at codes-left R: depth <= R, rank < V, parent kept
+// (bit i).
+__device__ __forceinline__ unsigned long long tree_keep(const FrameParams& P, int R) {
+  unsigned long long keep = 0;
+  for (int i = 0; i < P.tree_n; ++i) {
+    const int par = __ldg(&P.tree->parent[i]);
+    if (__ldg(&P.tree->dep[i]) <= R && __ldg(&P.tree->rank[i]) < P.V && (par < 0 || ((keep >> par) & 1ull)))
+      keep |= 1ull << i;
+  }
+  return keep;
+}
+
+// After codes up to depth s_new are committed in a tree context: finish the
+// frame, or set up the next round's tree from the draft slots of row hrow
+// (whose output is h_{s_new}).  Warp-wide; lane 0 owns the scalar state.
+template <typename WT>
+__device__ __noinline__ void after_commit_tree(const FrameParams& P, const CallArgs& ca, int b, AcceptScratch& A,
+                                               int s_new, int hrow) {
+  StreamState& S = *A.S;
+  const int lane = threadIdx.x & 31;
+  StreamStats* ss = P.sstats + b;
+  __syncwarp();
+  const int frame = S.frame;
+  __syncwarp();
+  if (s_new >= P.G - 1) {
+    if (lane == 0) { bump(ss->frames); bump(ss->committed, P.G - 1); }
+    const int nf = frame + 1;
+    if (nf < ca.n_frames) setup_frame<WT>(P, ca, b, S, nf);
+    else retire_stream(P, b, S);
+    return;
+  }
+  const int R = P.G - 1 - s_new;
+  const unsigned long long keep = tree_keep(P, R);
+  const int slots = 1 + P.ND;
+  int* tok = P.ttok + (size_t)b * 64;
+  // candidates of depth t: the draft slot's list holds the need[t] largest
+  // logits in index order; rank them by (logit descending, index ascending)
+  if (lane == 0) {
+    for (int t = 1; t <= P.tree->dmax && t <= R; ++t) {
+      const size_t li = (size_t)hrow * slots + t;
+      const int n = min(P.lcount[li], 64);
+      int ord[64];
+      float val[64];
+      for (int j = 0; j < n; ++j) {
+        const int v = P.lidx[li * P.KC + j];
+        const float x = P.logits[li * P.V + v];
+        int at = j;  // insertion: after every entry with a larger logit, or an equal one (lower index)
+        while (at > 0 && val[at - 1] < x) { val[at] = val[at - 1]; ord[at] = ord[at - 1]; --at; }
+        val[at] = x;
+        ord[at] = v;
+      }
+      for (int i = 0; i < P.tree_n; ++i)
+        if (((keep >> i) & 1ull) && __ldg(&P.tree->dep[i]) == t) {
+          const int rk = __ldg(&P.tree->rank[i]);
+          tok[i] = valid_code(P, rk < n ? ord[rk] : -1);
+        }
+    }
+  }
+  __syncwarp();
+  // the next pass's rows: the root (position s_new + 1, code c_{s_new}) in
+  // row slot 0, kept node i short of the frame end in row slot i + 1
+  long long kvpos = 0;
+  int m = 0;
+  for (int k = lane; k < P.NS; k += 32) {
+    int pos = -1, code = 0, slot = 0;
+    if (k == 0) {
+      pos = s_new + 1; code = S.codes[s_new]; slot = pos;
+    } else {
+      const int i = k - 1, dep = __ldcg(&P.tree->dep[i]);
+      if (i < P.tree_n && ((keep >> i) & 1ull) && dep < R) {
+        pos = s_new + 1 + dep; code = __ldcg(tok + i); slot = P.G + i;
+      }
+    }
+    P.row_pos[b * P.NS + k] = pos;
+    P.row_code[b * P.NS + k] = code;
+    P.row_slot[b * P.NS + k] = slot;
+    if (g_mirror_on) { g_mpos[b * P.NS + k] = pos; g_mcode[b * P.NS + k] = code; g_mslot[b * P.NS + k] = slot; }
+    if (pos >= 0) { ++m; kvpos += s_new + 2 + (k == 0 ? 0 : __ldcg(&P.tree->dep[k - 1])); }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    m += __shfl_xor_sync(0xffffffffu, m, o);
+    kvpos += __shfl_xor_sync(0xffffffffu, kvpos, o);
+  }
+  if (lane == 0) {
+    S.s = s_new;
+    S.n_d = 0;
+    S.m = m;
+    S.pos0 = s_new + 1;
+    S.phase = kPhaseSpec;
+    atomicAdd((unsigned long long*)&P.ctl->kv_bytes,
+              (unsigned long long)(kvpos * P.L * 2 * P.nkv * P.d * (long long)sizeof(float)));
+    atomicAdd((unsigned long long*)&P.ctl->weight_bytes, (unsigned long long)((long long)m * P.H * sizeof(WT)));
+  }
+  __syncwarp();
+}
+
+// The tree round's decision for stream b (or the frame prefill's commit of
+// c_1), the accepted path's K/V copied to its canonical positions, then the
+// next round.  Warp-wide; lane 0 walks the tree.
+template <typename WT>
+__device__ void accept_stream_tree(const FrameParams& P, const CallArgs& ca, int b, AcceptScratch& A) {
+  StreamState& S = *A.S;
+  const int lane = threadIdx.x & 31;
+  StreamStats* ss = P.sstats + b;
+  const int slots = 1 + P.ND, KC = P.KC;
+  const int s = S.s;
+  const uint32_t fr = (uint32_t)S.frame_abs;
+  int s_new = 0, hrow = 0, acc_n = 0;
+  if (lane == 0) {
+    if (S.phase == kPhasePrefill) {
+      // the prefill scored c_1 on the row of E_0(c_0)
+      const size_t li = (size_t)(b * P.NS + 1) * slots;
+      const float u = philox_uniform(P.seed, (uint32_t)b, fr, 1u, kTarget);
+      const int c = valid_code(P, list_sample(P.lidx + li * KC, P.lprob + li * KC, P.lcount[li], u));
+      S.codes[1] = c;
+      ca.codes_out[((size_t)S.frame * ca.B + b) * P.G + 1] = c;
+      s_new = 1;
+      hrow = b * P.NS + 1;
+      bump(ss->passes);
+    } else {
+      const int R = P.G - 1 - s;
+      const unsigned long long keep = tree_keep(P, R);
+      const int* tok = P.ttok + (size_t)b * 64;
+      float* work = A.r;  // the current node's remaining mass, aligned with its list
+      int cur = -1, d = 0;
+      while (s + d < P.G - 1) {
+        const size_t li = (size_t)(b * P.NS + cur + 1) * slots;  // the row of node cur (root: row 0)
+        const int* pidx = P.lidx + li * KC;
+        const float* pp = P.lprob + li * KC;
+        const int pn = P.lcount[li];
+        for (int j = 0; j < pn; ++j) work[j] = pp[j];
+        int taken = -1, ci = 0;
+        for (int i = 0; i < P.tree_n && taken < 0; ++i) {
+          if (!((keep >> i) & 1ull) || __ldg(&P.tree->parent[i]) != cur) continue;
+          float Sm = 0.0f;
+          for (int j = 0; j < pn; ++j) Sm = __fadd_rn(Sm, work[j]);
+          const int y = tok[i];
+          int at = -1;
+          for (int j = 0; j < pn; ++j)
+            if (pidx[j] == y) { at = j; break; }
+          const float rr = Sm > 0.0f ? __fdiv_rn(at >= 0 ? work[at] : 0.0f, Sm) : 0.0f;
+          const float u = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + d + 1), kTreeAccept + (uint32_t)ci);
+          if (u < rr) taken = i;
+          else if (at >= 0) work[at] = 0.0f;
+          ++ci;
+        }
+        if (taken >= 0) {
+          S.codes[s + d + 1] = tok[taken];
+          S.drafts[d < 8 ? d : 7] = taken;  // the accepted path (node per depth)
+          cur = taken;
+          ++d;
+          ++acc_n;
+          bump(ss->accepted[d < 9 ? d : 8]);
+          continue;
+        }
+        const float u = philox_uniform(P.seed, (uint32_t)b, fr, (uint32_t)(s + d + 1), kTarget);
+        int y = list_sample(pidx, work, pn, u);
+        if (y < 0) y = list_sample(pidx, pp, pn, u);
+        S.codes[s + d + 1] = valid_code(P, y);
+        ++d;
+        if (ci > 0) bump(ss->rejections);
+        else bump(ss->bonus);
+        break;
+      }
+      s_new = s + d;
+      hrow = b * P.NS + cur + 1;
+      for (int j = s + 1; j <= s_new; ++j) ca.codes_out[((size_t)S.frame * ca.B + b) * P.G + j] = S.codes[j];
+      bump(ss->rounds);
+      bump(ss->passes);
+    }
+    if (ca.committed_out) ca.committed_out[b] = s_new + 1;
+  }
+  s_new = __shfl_sync(0xffffffffu, s_new, 0);
+  hrow = __shfl_sync(0xffffffffu, hrow, 0);
+  acc_n = __shfl_sync(0xffffffffu, acc_n, 0);
+  __syncwarp();
+  // the accepted nodes' K/V (tree slots) to canonical positions s + 2 .. s + 1 + acc_n,
+  // which the next round's rows read as their prefix
+  if (s_new < P.G - 1 && acc_n > 0) {
+    const int d4 = P.nkv * P.d / 4;  // float4 per slot
+    const int per = 2 * P.L * d4;
+    for (int q = lane; q < acc_n * per; q += 32) {
+      const int j = q / per, rem = q - j * per;
+      const int lk = rem / d4, c = rem - lk * d4;  // lk = 2 layer + (0: K, 1: V)
+      const size_t base = ((size_t)b * P.L * 2 + lk) * P.GS;
+      const float4* src = reinterpret_cast<const float4*>(P.kv + (base + P.G + S.drafts[j]) * P.nkv * P.d) + c;
+      float4* dst = reinterpret_cast<float4*>(P.kv + (base + s + 2 + j) * P.nkv * P.d) + c;
+      *dst = __ldcg(src);
+    }
+  }
+  __syncwarp();
+  after_commit_tree<WT>(P, ca, b, A, s_new, hrow);
+  store_state(P, b, S);
+}
+
 // The rows of the next pass, compacted, and the lm_heads it needs (head_j
 // for j in [pos, pos + ND] of every row at pos >= 1).  One warp.
 __device__ int build_plan(const FrameParams& P, const CallArgs& ca) {
@@ -2306,6 +2558,7 @@ __device__ int build_plan(const FrameParams& P, const CallArgs& ca) {
       P.prow[at] = r;
       P.ppos[at] = pos;
       P.pcode[at] = g_mirror_on ? g_mcode[r] : __ldcg(P.row_code + r);
+      P.pslot[at] = g_mirror_on ? g_mslot[r] : __ldcg(P.row_slot + r);
       if (pos >= 1)
         for (int t = 0; t <= P.ND && pos + t <= P.G - 1; ++t) mask |= 1ull << (pos + t);
     }
@@ -2553,7 +2806,10 @@ size_t attention_smem(const FrameParams& P) {
 size_t topk_smem(const FrameParams& P) {
   return ((size_t)P.V * 4 + 15) / 16 * 16 + (size_t)cpk::kWarps * 1024 + ((size_t)P.KC * 4 + 15) / 16 * 16 + 256;
 }
-size_t accept_smem(const FrameParams& P, int warps) { return (size_t)warps * cpk::accept_scratch_bytes(P.NS, P.KC); }
+size_t accept_smem(const FrameParams& P, int warps) {
+  return (size_t)warps * cpk::accept_scratch_bytes(cpk::accept_rows(P.NS, P.tree_n),
+                                                   cpk::accept_drafts(P.NS, P.ND, P.tree_n), P.KC);
+}
 
 // Small-batch tensor path: the weight-row slots of each GEMV kind, or false
 // when the shape does not fit it (then the context keeps the other paths).

@@ -131,10 +131,57 @@ int offset_lookaheads(const cp_spec_config* cfg, int N) {
   return cfg->draft_offsets < ND ? cfg->draft_offsets : ND;
 }
 
-cpk::Layout layout_for(const cp_spec_model* m, const cp_spec_config* cfg, int N) {
+// Row slots per stream, draft slots per row and KV slots per stream and
+// layer: chain rounds NS = max(N, 2), ND = max(N - 1, 0), GS = G; tree
+// rounds NS = 1 + nodes (the root row, then one per node), ND = the tree's
+// depth, GS = G + nodes.
+struct Slots {
+  int NS, ND, GS;
+};
+Slots slots_for(const cp_spec_model* m, int N, const cpk::TreeTab* tree) {
+  if (tree) return Slots{1 + tree->n, tree->dmax, m->num_code_groups + tree->n};
+  return Slots{N > 2 ? N : 2, N > 1 ? N - 1 : 0, m->num_code_groups};
+}
+
+cpk::Layout layout_for(const cp_spec_model* m, const cp_spec_config* cfg, int N, const cpk::TreeTab* tree = nullptr) {
   const int KC = list_capacity(m, cfg);
+  const Slots sl = slots_for(m, N, tree);
   return cpk::make_layout(m->hidden, m->n_layers, m->n_q_heads, m->n_kv_heads, m->head_dim, m->ffn, m->vocab,
-                          m->num_code_groups, N, KC, cfg->max_streams, offset_lookaheads(cfg, N));
+                          m->num_code_groups, sl.NS, sl.ND, sl.GS, KC, cfg->max_streams, offset_lookaheads(cfg, N));
+}
+
+// Checks a sparse tree ("RVQ Position Aware Speculative Decoding for On
+// Device TTS", section 2.2, Figure 2) and derives its table: 1..62 nodes,
+// parents first, siblings in ascending rank without repeats, depth at most
+// CP_SPEC_MAX_WINDOW - 1, and every rank below the list capacity (a draft
+// slot's list holds the candidates up to the largest rank of its depth).
+cp_spec_status build_tree(const cp_spec_model* m, const cp_spec_config* cfg, const cp_spec_tree* t, cpk::TreeTab* out) {
+  if (!t) return fail(nullptr, CP_SPEC_E_INVALID, "tree is null");
+  if (t->n < 1 || t->n > cpk::kTreeMaxNodes || !t->parent || !t->rank)
+    return fail(nullptr, CP_SPEC_E_INVALID, "tree needs 1..%d nodes with parent and rank arrays", cpk::kTreeMaxNodes);
+  cpk::TreeTab T;
+  memset(&T, 0, sizeof T);
+  T.n = t->n;
+  const int KC = list_capacity(m, cfg);
+  for (int i = 0; i < t->n; ++i) {
+    const int par = t->parent[i], rk = t->rank[i];
+    if (par < -1 || par >= i) return fail(nullptr, CP_SPEC_E_INVALID, "tree node %d: parent must be -1 or an earlier node", i);
+    if (rk < 0 || rk >= KC || rk >= m->vocab)
+      return fail(nullptr, CP_SPEC_E_INVALID, "tree node %d: rank %d outside [0, %d)", i, rk, std::min(KC, m->vocab));
+    for (int j = 0; j < i; ++j)
+      if (t->parent[j] == par && t->rank[j] >= rk)
+        return fail(nullptr, CP_SPEC_E_INVALID, "tree node %d: siblings must come in ascending rank", i);
+    T.parent[i] = par;
+    T.rank[i] = rk;
+    T.dep[i] = par < 0 ? 1 : T.dep[par] + 1;
+    T.anc[i] = (par < 0 ? 0ull : T.anc[par]) | (1ull << i);
+    if (T.dep[i] > CP_SPEC_MAX_WINDOW - 1)
+      return fail(nullptr, CP_SPEC_E_INVALID, "tree node %d: depth above %d", i, CP_SPEC_MAX_WINDOW - 1);
+    T.dmax = std::max(T.dmax, T.dep[i]);
+    T.need[T.dep[i]] = std::max(T.need[T.dep[i]], rk + 1);
+  }
+  *out = T;
+  return CP_SPEC_OK;
 }
 
 template <typename T>
@@ -200,7 +247,8 @@ struct DevicePlan {
 
 // Queries the current device and checks that the configuration fits the
 // pass kernels (shared memory of the top-k and accept kernels).
-cp_spec_status plan_device(const cp_spec_model* model, const cp_spec_config* config, int N, DevicePlan* dp) {
+cp_spec_status plan_device(const cp_spec_model* model, const cp_spec_config* config, int N, DevicePlan* dp,
+                           const cpk::TreeTab* tree = nullptr) {
   int dev = 0, sms = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -208,8 +256,10 @@ cp_spec_status plan_device(const cp_spec_model* model, const cp_spec_config* con
   const int KC = list_capacity(model, config);
   cp_spec_status v = check_shapes(model, N, KC);
   if (v != CP_SPEC_OK) return v;
-  const int NS = N > 2 ? N : 2;
-  const size_t per_warp = cpk::accept_scratch_bytes(NS, KC);
+  const Slots sl = slots_for(model, N, tree);
+  const int tn = tree ? tree->n : 0;
+  const size_t per_warp =
+      cpk::accept_scratch_bytes(cpk::accept_rows(sl.NS, tn), cpk::accept_drafts(sl.NS, sl.ND, tn), KC);
   const int aw = (int)std::min<size_t>(cpk::kWarps, kSmemPerSm / per_warp);
   if (aw < 1)
     return fail(nullptr, CP_SPEC_E_UNSUPPORTED, "top_k %d too large for verify window %d (accept lists exceed shared memory)",
@@ -223,19 +273,23 @@ cp_spec_status plan_device(const cp_spec_model* model, const cp_spec_config* con
 // Fills the launch-invariant parameters: model shape, weight pointers and
 // the carve-up of the workspace at `ws`.
 void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, const cp_spec_config* config, int N,
-                 const DevicePlan& dp, const cpk::Layout& lay, unsigned char* ws, cpk::FrameParams* out) {
+                 const DevicePlan& dp, const cpk::Layout& lay, unsigned char* ws, cpk::FrameParams* out,
+                 const cpk::TreeTab* tree = nullptr) {
   cpk::FrameParams& P = *out;
   memset(&P, 0, sizeof P);
   const int L = model->n_layers;
-  const int NS = N > 2 ? N : 2;
+  const Slots sl = slots_for(model, N, tree);
+  const int NS = sl.NS;
   P.H = model->hidden; P.L = L; P.nq = model->n_q_heads; P.nkv = model->n_kv_heads; P.d = model->head_dim;
   P.F = model->ffn; P.V = model->vocab; P.G = model->num_code_groups; P.dtype = model->dtype;
   P.eps = model->rms_eps;
-  P.N = N; P.NS = NS; P.ND = N > 1 ? N - 1 : 0; P.KC = dp.KC;
+  P.N = N; P.NS = NS; P.ND = sl.ND; P.KC = dp.KC;
+  P.tree_n = tree ? tree->n : 0;
+  P.GS = sl.GS;
   P.Bmax = config->max_streams;
   P.kernels_per_pass = 5 * L + 3;
   P.KO = offset_lookaheads(config, N);
-  P.adapt_pct = config->adapt_accept_pct;
+  P.adapt_pct = tree ? 0 : config->adapt_accept_pct;  // the tree fixes the drafts of every round
   P.adapt_min = config->adapt_min_reached;
   // bf16 contexts with many rows per pass run the GEMVs on tensor cores
   // (every GEMV width a multiple of 32); the choice depends on the context,
@@ -269,6 +323,8 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
   P.qidx = at<int>(ws, lay.qidx); P.qprob = at<float>(ws, lay.qprob); P.qcount = at<int>(ws, lay.qcount);
   P.row_pos = at<int>(ws, lay.row_pos); P.row_code = at<int>(ws, lay.row_code);
   P.prow = at<int>(ws, lay.prow); P.ppos = at<int>(ws, lay.ppos); P.pcode = at<int>(ws, lay.pcode);
+  P.row_slot = at<int>(ws, lay.row_slot); P.pslot = at<int>(ws, lay.pslot); P.ttok = at<int>(ws, lay.ttok);
+  P.tree = at<cpk::TreeTab>(ws, lay.tree);
   P.plan = at<cpk::Plan>(ws, lay.plan);
   P.st = at<cpk::StreamState>(ws, lay.st); P.sstats = at<cpk::StreamStats>(ws, lay.sstats); P.rope = at<float2>(ws, lay.rope);
   P.top_k = at<int>(ws, lay.top_k); P.temp = at<float>(ws, lay.temp); P.ctl = at<cpk::Control>(ws, lay.ctl);
@@ -375,8 +431,13 @@ size_t cp_spec_workspace_bytes(const cp_spec_model* model, const cp_spec_config*
   return layout_for(model, config, effective_window(model, config)).total;
 }
 
-cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* weights, const cp_spec_config* config,
-                            void* d_workspace, size_t workspace_bytes, cp_spec_ctx** out) {
+}  // extern "C"
+
+namespace {
+
+// cp_spec_init, with a sparse tree (tree != null) or chain rounds.
+cp_spec_status init_impl(const cp_spec_model* model, const cp_spec_weights* weights, const cp_spec_config* config,
+                         const cp_spec_tree* tree_in, void* d_workspace, size_t workspace_bytes, cp_spec_ctx** out) {
   if (!out) return fail(nullptr, CP_SPEC_E_INVALID, "out is null");
   *out = nullptr;
   cp_spec_status v = validate(model, config, nullptr);
@@ -384,12 +445,20 @@ cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* w
   v = check_weights(model, config, weights);
   if (v != CP_SPEC_OK) return v;
   if (!d_workspace || !aligned16(d_workspace)) return fail(nullptr, CP_SPEC_E_INVALID, "workspace null or not 16-byte aligned");
-  const int N = effective_window(model, config);
-  const cpk::Layout lay = layout_for(model, config, N);
+  cpk::TreeTab tab;
+  const cpk::TreeTab* tree = nullptr;
+  if (tree_in) {
+    v = build_tree(model, config, tree_in, &tab);
+    if (v != CP_SPEC_OK) return v;
+    if (model->num_code_groups < 3) return fail(nullptr, CP_SPEC_E_INVALID, "tree rounds need at least 3 code groups");
+    tree = &tab;
+  }
+  const int N = tree ? tree->dmax + 1 : effective_window(model, config);
+  const cpk::Layout lay = layout_for(model, config, N, tree);
   if (workspace_bytes < lay.total)
     return fail(nullptr, CP_SPEC_E_WORKSPACE, "workspace %zu bytes < required %zu", workspace_bytes, lay.total);
   DevicePlan dp;
-  v = plan_device(model, config, N, &dp);
+  v = plan_device(model, config, N, &dp, tree);
   if (v != CP_SPEC_OK) return v;
 
   cp_spec_ctx* c = new (std::nothrow) cp_spec_ctx();
@@ -409,10 +478,11 @@ cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* w
   c->staged = c->need_setup = false;
 
   cpk::FrameParams& P = c->base;
-  fill_params(model, weights, config, N, dp, lay, c->ws, &P);
+  fill_params(model, weights, config, N, dp, lay, c->ws, &P, tree);
 
   cudaError_t e = cpk_host::configure_kernels(P, dp.accept_warps);
   if (e == cudaSuccess) e = cudaMemset(c->ws, 0, lay.total);
+  if (e == cudaSuccess && tree) e = cudaMemcpy((void*)P.tree, tree, sizeof *tree, cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
     e = cudaMemset(P.row_pos, 0xFF, sizeof(int) * (size_t)config->max_streams * P.NS);
   if (e == cudaSuccess)
@@ -427,11 +497,34 @@ cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* w
   }
   c->launches += P.KO > 0 ? 2 : 1;
   *out = c;
-  if (N != window_of(config)) {
+  if (!tree && N != window_of(config)) {
     c->err = "speculation disabled: fewer than 3 code groups leave no draft slot; running the autoregressive loop";
     return CP_SPEC_W_AR_FALLBACK;
   }
   return CP_SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+cp_spec_status cp_spec_init(const cp_spec_model* model, const cp_spec_weights* weights, const cp_spec_config* config,
+                            void* d_workspace, size_t workspace_bytes, cp_spec_ctx** out) {
+  return init_impl(model, weights, config, nullptr, d_workspace, workspace_bytes, out);
+}
+
+size_t cp_spec_workspace_bytes_tree(const cp_spec_model* model, const cp_spec_config* config, const cp_spec_tree* tree) {
+  if (validate(model, config, nullptr) != CP_SPEC_OK) return 0;
+  cpk::TreeTab tab;
+  if (build_tree(model, config, tree, &tab) != CP_SPEC_OK) return 0;
+  return layout_for(model, config, tab.dmax + 1, &tab).total;
+}
+
+cp_spec_status cp_spec_init_tree(const cp_spec_model* model, const cp_spec_weights* weights,
+                                 const cp_spec_config* config, const cp_spec_tree* tree, void* d_workspace,
+                                 size_t workspace_bytes, cp_spec_ctx** out) {
+  if (!tree) return fail(nullptr, CP_SPEC_E_INVALID, "tree is null");
+  return init_impl(model, weights, config, tree, d_workspace, workspace_bytes, out);
 }
 
 cp_spec_status cp_spec_set_stream_sampling(cp_spec_ctx* c, int32_t n, const int32_t* h_top_k, const float* h_temp) {

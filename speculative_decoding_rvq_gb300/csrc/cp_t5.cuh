@@ -412,8 +412,9 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
       const int gi = s_list[tid], r = pr.prow[gi], pos = pr.ppos[gi];
       long long e0, e1 = 0;
       if (KIND == kQKV) {
+        const int slot = P.tree_n ? __ldcg(P.pslot + gi) : pos;                           // KV slot of the row
         e0 = (long long)r * P.nq * P.d;                                                     // q row
-        e1 = ((((long long)(r / P.NS) * P.L + l) * 2) * P.G + pos) * P.nkv * P.d;        // K row of the position
+        e1 = ((((long long)(r / P.NS) * P.L + l) * 2) * P.GS + slot) * P.nkv * P.d;       // K row of the slot
       } else if (KIND == kO || KIND == kDown) {
         e0 = (long long)r * P.H;
       } else if (KIND == kGU) {
@@ -451,7 +452,7 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
         e = uu - hh * half;
         if (hh < P.nq) { qkv_dst = P.qbuf; qkv_off = (long long)hh * P.d + e; }
         else if (hh < P.nq + P.nkv) { qkv_dst = P.kv; qkv_off = (long long)(hh - P.nq) * P.d + e; }
-        else { qkv_dst = P.kv; qkv_off = (long long)P.G * P.nkv * P.d + (long long)(hh - P.nq - P.nkv) * P.d + e; }
+        else { qkv_dst = P.kv; qkv_off = (long long)P.GS * P.nkv * P.d + (long long)(hh - P.nq - P.nkv) * P.d + e; }
       }
       int hv = 0, head = 0;
       if (KIND == kHeads) {
