@@ -106,7 +106,7 @@ def measured_peaks():
     return 6800.0, "fallback"
 
 
-PASS_KERNEL_SOURCES = ("cp_common.cuh", "cp_sampling.cuh", "cp_frame.cuh", "cp_pass_kernels.cu")
+PASS_KERNEL_SOURCES = ("cp_common.cuh", "cp_sampling.cuh", "cp_frame.cuh", "cp_t5.cuh", "cp_pass_kernels.cu")
 
 
 def kernel_source_hash():
@@ -593,6 +593,21 @@ def profile_rounds(args):
     print(json.dumps({"profile_rounds": done, "passes": st["passes"], "kernel_launches": st["kernel_launches"]}))
 
 
+def profile_accept(args):
+    """Profiling case for ncu: one acceptance call of the microbench kind (8192 rounds, N = 4,
+    V 2048, rho 0.7, top-k 50, T 0.9), after one untimed call.  Inputs 470 MB > L2."""
+    import torch
+    from speculative_decoding_rvq_gb300 import binding
+    R, N, V = 8192, 4, 2048
+    g = torch.Generator(device="cuda").manual_seed(1)
+    tgt = torch.randn((R, N, V), device="cuda", generator=g) * 3.0
+    drf = (0.7 * tgt[:, : N - 1] + 0.51 ** 0.5 * torch.randn((R, N - 1, V), device="cuda", generator=g) * 3.0).contiguous()
+    for _ in range(2):
+        tok, na, _ = binding.accept_batch(tgt, drf, TOP_K, TEMP, SEED, 0)
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_accept": R, "mean_accepted": round(float(na.float().mean().item()), 4)}))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -608,9 +623,13 @@ def main():
     ap.add_argument("--profile-rounds", type=int, default=0,
                     help="run this many step-wise passes (direct kernel launches, for a profiler) and exit")
     ap.add_argument("--profile-streams", type=int, default=1, help="streams of the --profile-rounds case")
+    ap.add_argument("--profile-accept", action="store_true", help="run one acceptance-kernel call and exit")
     args = ap.parse_args()
     if args.profile_rounds > 0:
         profile_rounds(args)
+        return
+    if args.profile_accept:
+        profile_accept(args)
         return
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
