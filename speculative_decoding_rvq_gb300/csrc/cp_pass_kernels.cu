@@ -2813,9 +2813,9 @@ size_t accept_smem(const FrameParams& P, int warps) {
 
 // Small-batch tensor path: the weight-row slots of each GEMV kind, or false
 // when the shape does not fit it (then the context keeps the other paths).
-// A kind whose per-CTA tile fits the weight budget holds it whole (one
-// phase, every row copied before the dependency wait); a larger tile (the
-// lm_heads) streams through two banks.
+// Every layer kind's per-CTA tile must fit the weight budget and is held
+// whole (one phase, every row copied before the dependency wait); the
+// lm_heads tile may be larger and streams through two banks.
 constexpr size_t kMvWeightBudget = 100 * 1024;   // weight region of one CTA
 constexpr size_t kMvSmemLimit = 220 * 1024;      // dynamic shared memory of one CTA
 bool plan_mv(FrameParams& P, int sms) {
@@ -2837,6 +2837,9 @@ bool plan_mv(FrameParams& P, int sms) {
     }
     const long long need = (U + sms - 1) / sms * rpu;  // rows of the largest tile
     long long S = std::min<long long>(need, (long long)(kMvWeightBudget / RS));
+    // a layer GEMV whose tile does not fit one phase would serialise its
+    // banks' copies on every pass: such shapes keep the CUDA-core kernel
+    if (S < need && kind != cpk::kHeads) return false;
     if (S < need) S = std::max<long long>(S / 2 * 2, 4);
     while (S >= 4 && cpk::mv_smem_layout(kind, (int)S, K, rows_cap, P.G, P.d).total > kMvSmemLimit) S -= 2;
     if (S < 4 || (S < need && S / 2 < rpu)) return false;
