@@ -341,18 +341,24 @@ cp_spec_status cp_spec_status_word(cp_spec_ctx* ctx, void* stream);
 cp_spec_status cp_spec_read_stats(cp_spec_ctx* ctx, cp_spec_stats* h_stats, void* stream);
 cp_spec_status cp_spec_reset_stats(cp_spec_ctx* ctx, void* stream);
 
-/* Diagnostic hook for tests of the failure path (the pages have no
- * counterpart).  wait_limit_ns (1e4 .. 6e10; default 2e9) bounds every
- * device-side wait of the context's kernels (a weight or input copy that has
- * not landed): after it the kernel records CP_SPEC_E_DEVICE_TIMEOUT in the
- * status word, waits (with the same bound) for its own copies still in
- * flight and returns; the pass loop then stops.  stall_first_wait = 1 makes
- * one wait of the first decoder kernel of every pass (CTA 0) expect 16 bytes
- * that no copy delivers, so that wait always runs out; 0 restores normal
- * operation.  Nothing traps or spins without a bound.  Synchronises the
- * device if the context's call graph exists (it is rebuilt on the next
- * call). */
-cp_spec_status cp_spec_test_hooks(cp_spec_ctx* ctx, uint64_t wait_limit_ns, int32_t stall_first_wait);
+/* Diagnostic hook for tests (the pages have no counterpart).
+ * wait_limit_ns (1e4 .. 6e10; default 2e9) bounds every device-side wait of
+ * the context's kernels (a weight or input copy that has not landed): after
+ * it the kernel records CP_SPEC_E_DEVICE_TIMEOUT in the status word, waits
+ * (with the same bound) for its own copies still in flight and returns; the
+ * pass loop then stops.  flags (0 .. 3):
+ *   bit 0 (1): one wait of the first decoder kernel of every pass (CTA 0)
+ *     never completes, so that wait always runs out;
+ *   bit 1 (2): after each decision the accept kernel writes NaN into every
+ *     KV slot of the stream that the next pass must not read (positions past
+ *     the committed depth, the tree nodes' slots, and at a frame's end the
+ *     whole cache), so a pass that read a stale slot would show NaN
+ *     ("Speculative Decoding, Beyond Text", section 07: the logical length
+ *     and the valid-position mask).
+ * 0 restores normal operation.  Nothing traps or spins without a bound.
+ * Synchronises the device if the context's call graph exists (it is rebuilt
+ * on the next call). */
+cp_spec_status cp_spec_test_hooks(cp_spec_ctx* ctx, uint64_t wait_limit_ns, int32_t flags);
 
 /* Number of launches the library has enqueued on this context: kernels
  * launched directly, plus one per launch of the context's call graph (whose

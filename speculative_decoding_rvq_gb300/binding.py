@@ -259,8 +259,9 @@ class CpSpec:
         """cp_spec_status_word as a code (clears the word)."""
         return int(self.lib.cp_spec_status_word(self.ctx, _stream()))
 
-    def test_hooks(self, wait_limit_ns: int = 2_000_000_000, stall_first_wait: bool = False):
-        _check(self.lib.cp_spec_test_hooks(self.ctx, int(wait_limit_ns), 1 if stall_first_wait else 0), self.ctx)
+    def test_hooks(self, wait_limit_ns: int = 2_000_000_000, stall_first_wait: bool = False, poison_kv: bool = False):
+        flags = (1 if stall_first_wait else 0) | (2 if poison_kv else 0)
+        _check(self.lib.cp_spec_test_hooks(self.ctx, int(wait_limit_ns), flags), self.ctx)
 
     def stats(self) -> dict:
         st = Stats()

@@ -132,6 +132,7 @@ struct FrameParams {
   int t5_rb[5];     // ... pass rows per CTA tile, per GEMV kind (16, 32 or 64)
   int t5_stages[5]; // ... stages of the weight / input ring, per GEMV kind
   int test_stall;   // test hook: one bounded wait of the first GEMV of a pass never completes
+  int test_poison;  // test hook: the accept kernel writes NaN into the KV slots the next pass must not read
   int tree_n;       // sparse-tree rounds: nodes of the tree (0 = chain rounds)
   int GS;           // KV slots per stream and layer: G canonical positions, then tree_n node slots
   unsigned long long wait_ns;         // limit of every bounded device-side wait

@@ -2190,6 +2190,24 @@ __device__ void accept_prefetch(const FrameParams& P, int b, AcceptScratch& A) {
   __syncwarp();
 }
 
+// Test hook: NaN into every KV slot of stream b from `from` on (all layers,
+// K and V) -- the slots the next pass must write before any row reads them.
+// Warp-wide.
+__device__ void poison_kv(const FrameParams& P, int b, int from) {
+  const int lane = threadIdx.x & 31;
+  __syncwarp();
+  if (from < 0) from = 0;
+  const int per = P.nkv * P.d / 4;        // float4 per slot
+  const int n = (P.GS - from) * per;      // per (layer, K/V)
+  const float4 nan4 = make_float4(__int_as_float(0x7fc00000), __int_as_float(0x7fc00000),
+                                  __int_as_float(0x7fc00000), __int_as_float(0x7fc00000));
+  for (int lk = 0; lk < 2 * P.L; ++lk) {
+    float4* base = reinterpret_cast<float4*>(P.kv + (((size_t)b * P.L * 2 + lk) * P.GS + from) * P.nkv * P.d);
+    for (int q = lane; q < n; q += 32) base[q] = nan4;
+  }
+  __syncwarp();
+}
+
 template <typename WT>
 __device__ void accept_stream_tree(const FrameParams& P, const CallArgs& ca, int b, AcceptScratch& A);
 
@@ -2326,6 +2344,7 @@ __device__ void accept_stream(const FrameParams& P, const CallArgs& ca, int b, A
   s_new = __shfl_sync(0xffffffffu, s_new, 0);
   hrow = __shfl_sync(0xffffffffu, hrow, 0);
   __syncwarp();
+  if (P.test_poison) poison_kv(P, b, s_new >= P.G - 1 ? 0 : s_new + 1);
   after_commit<WT>(P, ca, b, A, s_new, hrow);
   store_state(P, b, S);
 }
@@ -2536,6 +2555,7 @@ __device__ void accept_stream_tree(const FrameParams& P, const CallArgs& ca, int
     }
   }
   __syncwarp();
+  if (P.test_poison) poison_kv(P, b, s_new >= P.G - 1 ? 0 : s_new + 1);
   after_commit_tree<WT>(P, ca, b, A, s_new, hrow);
   store_state(P, b, S);
 }

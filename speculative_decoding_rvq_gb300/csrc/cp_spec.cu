@@ -302,6 +302,7 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
   else cpk_host::plan_t5(P, dp.sms);        // tcgen05 tiles where the shape fits them
   P.wait_ns = cpk::kDefaultWaitNs;
   P.test_stall = 0;
+  P.test_poison = 0;
   P.seed = config->seed;
   P.cond = 0;
   const long long eb = model->dtype == 1 ? 2 : 4;
@@ -759,11 +760,11 @@ cp_spec_status cp_spec_reset_stats(cp_spec_ctx* c, void* stream) {
   return check_cuda(c, e, "reset stats");
 }
 
-cp_spec_status cp_spec_test_hooks(cp_spec_ctx* c, uint64_t wait_limit_ns, int32_t stall_first_wait) {
+cp_spec_status cp_spec_test_hooks(cp_spec_ctx* c, uint64_t wait_limit_ns, int32_t flags) {
   if (!c) return fail(nullptr, CP_SPEC_E_INVALID, "null context");
   if (wait_limit_ns < 10000ull || wait_limit_ns > 60ull * 1000000000ull)
     return fail(c, CP_SPEC_E_INVALID, "wait_limit_ns must be in [1e4, 6e10]");
-  if (stall_first_wait != 0 && stall_first_wait != 1) return fail(c, CP_SPEC_E_INVALID, "stall_first_wait must be 0 or 1");
+  if (flags < 0 || flags > 3) return fail(c, CP_SPEC_E_INVALID, "flags must be in [0, 3]");
   // the parameter block is part of the call graph: drop the graph (rebuilt on the next call)
   if (c->graph) {
     cudaError_t e = cudaDeviceSynchronize();
@@ -772,7 +773,8 @@ cp_spec_status cp_spec_test_hooks(cp_spec_ctx* c, uint64_t wait_limit_ns, int32_
     if (e != cudaSuccess) return check_cuda(c, e, "graph release");
   }
   c->base.wait_ns = wait_limit_ns;
-  c->base.test_stall = stall_first_wait;
+  c->base.test_stall = flags & 1;
+  c->base.test_poison = (flags >> 1) & 1;
   return CP_SPEC_OK;
 }
 

@@ -52,6 +52,8 @@ constexpr int kT5BStages = 3;
 constexpr int kT5ConvThreads = 256;       // warps 0-7: conversion and epilogue
 constexpr int kT5CopyThreads = 128;       // warps 8-11: copies
 constexpr int kT5Threads = kT5ConvThreads + kT5CopyThreads + 32;  // warp 12: MMA issue
+constexpr int kT5WRows = kT5M * 8 / kT5CopyThreads;  // weight rows per copy thread (one 16-byte chunk each)
+constexpr int kT5XRows = 64 * 16 / kT5CopyThreads;   // input rows per copy thread, at most
 
 struct T5Shared {
   uint64_t full[kT5MaxStages];   // ring stage holds its slab (one arrival per copy thread)
@@ -251,16 +253,16 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
   const uint32_t tmem = sh.tmem;
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 
-  if (warp >= 8 && warp < 12) {
+  if (warp >= kT5ConvThreads / 32 && warp < (kT5ConvThreads + kT5CopyThreads) / 32) {
     // ================= copy warps
     const int ct = tid - kT5ConvThreads;
     for (int r = ct; r < nun * kRpu; r += kT5CopyThreads) prefetch_l2(s_wrow[r], (uint32_t)K * 2u);
-    // weight chunks: rows (ct >> 3) + 16 q (q < 8), 16-byte chunk ct & 7 of each slab row;
-    // the rows share r mod 8, so each lands at the same swizzled chunk of its row
-    const unsigned char* wsrc[8];
+    // weight chunks: rows (ct >> 3) + (kT5CopyThreads / 8) q, 16-byte chunk ct & 7 of each
+    // slab row; the rows share r mod 8, so each lands at the same swizzled chunk of its row
+    const unsigned char* wsrc[kT5WRows];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const unsigned char* r = s_wrow[(ct >> 3) + 16 * q];
+    for (int q = 0; q < kT5WRows; ++q) {
+      const unsigned char* r = s_wrow[(ct >> 3) + (kT5CopyThreads / 8) * q];
       wsrc[q] = r != nullptr ? r + (ct & 7) * 16 : nullptr;
     }
     const uint32_t wdst = (uint32_t)((ct >> 3) * 128 + (((ct & 7) ^ ((ct >> 3) & 7)) << 4));
@@ -271,13 +273,13 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
       s_xstep[ct] = a.f != nullptr ? 256 : 128;
     }
     asm volatile("bar.sync 1, %0;" ::"n"(kT5CopyThreads) : "memory");  // the copy warps' row table
-    // input chunks: rows (ct >> 4) + 8 q (q < RB / 8), 16-byte chunk ct & 15 (fp32 rows:
-    // 16 chunks per slab row; bf16 code embeddings: 8)
-    const unsigned char* xsrc[8];
-    int xsteps[8];
+    // input chunks: rows (ct >> 4) + (kT5CopyThreads / 16) q, 16-byte chunk ct & 15 (fp32
+    // rows: 16 chunks per slab row; bf16 code embeddings: 8)
+    const unsigned char* xsrc[kT5XRows];
+    int xsteps[kT5XRows];
 #pragma unroll
-    for (int q = 0; q < 8; ++q) {
-      const int i = (ct >> 4) + 8 * q;
+    for (int q = 0; q < kT5XRows; ++q) {
+      const int i = (ct >> 4) + (kT5CopyThreads / 16) * q;
       const bool v = i < cnt && (ct & 15) * 16 < s_xstep[i];
       xsrc[q] = v ? s_xrow[i] + (ct & 15) * 16 : nullptr;
       xsteps[q] = v ? s_xstep[i] : 0;
@@ -293,12 +295,12 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
         }
         unsigned char* wst = abase + (size_t)st * kT5SlabBytes + wdst;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (wsrc[q] != nullptr) cp_async16(wst + q * 2048, wsrc[q] + (size_t)j * 128);
+        for (int q = 0; q < kT5WRows; ++q)
+          if (wsrc[q] != nullptr) cp_async16(wst + q * (kT5CopyThreads * 16), wsrc[q] + (size_t)j * 128);
         unsigned char* xst = rawb + (size_t)st * RB * 256 + xdst;
 #pragma unroll
-        for (int q = 0; q < 8; ++q)
-          if (xsrc[q] != nullptr) cp_async16(xst + q * 2048, xsrc[q] + (size_t)j * xsteps[q]);
+        for (int q = 0; q < kT5XRows; ++q)
+          if (xsrc[q] != nullptr) cp_async16(xst + q * (kT5CopyThreads * 16), xsrc[q] + (size_t)j * xsteps[q]);
         // one arrival on the stage's barrier once this thread's copies landed
         asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(&sh.full[st])) : "memory");
       }
@@ -306,7 +308,7 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
     cp_async_wait_all();
     // an aborted CTA leaves slabs nobody waits for: give their arrivals time to land
     if (!ok) __nanosleep(4000);
-  } else if (warp == 12) {
+  } else if (warp == (kT5ConvThreads + kT5CopyThreads) / 32) {
     // ================= MMA thread
     if (lane == 0) {
       bool ok = !stall || t5_wait(&sh.hbar, 0, abort, &P.ctl->status, P.wait_ns);

@@ -62,7 +62,7 @@ def test_test_hook_rejects_bad_arguments():
     from speculative_decoding_rvq_gb300 import binding
     spec, dw = _setup("fp32")
     cp = binding.CpSpec(spec, dw, 4, 50, 0.9, 5, max_streams=1)
-    for ns, st in ((100, 0), (2_000_000_000, 2)):
+    for ns, st in ((100, 0), (2_000_000_000, 4), (2_000_000_000, -1)):
         assert cp.lib.cp_spec_test_hooks(cp.ctx, ns, st) == binding.E_INVALID
 
 
