@@ -430,7 +430,7 @@ def batched(spec, dw, peak, streams=64, frames=500):
            "codes_per_s": round(streams * frames * (G - 1) / (ms / 1e3), 1),
            "passes": st["passes"], "us_per_pass": round(ms * 1e3 / st["passes"], 2),
            "hbm_frac": round((st["weight_bytes"] + st["kv_bytes"]) / (ms / 1e3) / 1e9 / peak, 4),
-           "gemv_path": "tcgen05 tiles (bf16 weights x inputs split hi/lo, TMEM accumulators)"}
+           "gemv_path": "tcgen05 tiles (TMA-staged bf16 weights x inputs split hi/lo, TMEM accumulators)"}
     cp.close()
     return out
 

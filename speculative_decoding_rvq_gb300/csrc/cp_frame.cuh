@@ -94,6 +94,13 @@ struct CallArgs {
   float* t_draft;        // [B][P-1][ND][V] or null
 };
 
+// Tensor map of a weight matrix for the tcgen05 tiles: layer l's wq, wk, wv,
+// wo, w_gate, w_up, w_down at 7 l + 0..6, the lm_heads (as one matrix of
+// (G - 1) V rows) at 7 L.
+enum : int { kMapQ = 0, kMapK = 1, kMapV = 2, kMapO = 3, kMapGate = 4, kMapUp = 5, kMapDown = 6 };
+constexpr int kT5M = 128;  // weight rows per tile (the MMA's M)
+__host__ __device__ inline int t5_map_index(int L, int l, int which) { return which < 0 ? 7 * L : 7 * l + which; }
+
 // Sparse draft tree of a context ("RVQ Position Aware Speculative Decoding
 // for On Device TTS", section 2.2, Figure 2): node i has parent[i] (-1: a
 // child of the committed code, else an earlier node) and rank[i], the rank
@@ -131,6 +138,7 @@ struct FrameParams {
   int t5;           // bf16 GEMVs as tcgen05 tiles (contexts with many rows per pass)
   int t5_rb[5];     // ... pass rows per CTA tile, per GEMV kind (16, 32 or 64)
   int t5_stages[5]; // ... stages of the weight / input ring, per GEMV kind
+  const unsigned char* tmaps;  // ... TMA tensor maps of the weight matrices, 128 bytes each (t5_map_index)
   int test_stall;   // test hook: one bounded wait of the first GEMV of a pass never completes
   int test_poison;  // test hook: the accept kernel writes NaN into the KV slots the next pass must not read
   int tree_n;       // sparse-tree rounds: nodes of the tree (0 = chain rounds)
@@ -207,7 +215,7 @@ inline __host__ __device__ size_t accept_scratch_bytes(int NSr, int NDr, int KC)
 // Workspace carve-up, computed identically by the host for sizing.
 struct Layout {
   size_t h, qbuf, abuf, fbuf, kv, logits, otab, lidx, lprob, lcount, qidx, qprob, qcount, row_pos, row_code, prow, ppos,
-      pcode, row_slot, pslot, ttok, tree, plan, st, sstats, rope, top_k, temp, ctl, call, total;
+      pcode, row_slot, pslot, ttok, tree, tmaps, plan, st, sstats, rope, top_k, temp, ctl, call, total;
 };
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -243,6 +251,7 @@ inline Layout make_layout(int H, int L, int nq, int nkv, int d, int F, int V, in
   o.pslot = take(sizeof(int) * rows);
   o.ttok = take(sizeof(int) * (size_t)Bmax * 64);
   o.tree = take(sizeof(TreeTab));
+  o.tmaps = take((size_t)(7 * L + 1) * 128);  // tensor maps of the weight matrices (tcgen05 tiles)
   o.plan = take(sizeof(Plan));
   o.st = take(sizeof(StreamState) * (size_t)Bmax);
   o.sstats = take(sizeof(StreamStats) * (size_t)Bmax);

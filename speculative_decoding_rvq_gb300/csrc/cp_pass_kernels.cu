@@ -2888,8 +2888,9 @@ static long long gemv_units_max(const FrameParams& P, int kind) {
 constexpr size_t kT5SmemBudget = 200 * 1024;
 bool plan_t5(FrameParams& P, int sms) {
   const int rows_cap = P.Bmax * P.NS;
+  // (a tile's RoPE halves are whole boxes of d/2 rows: d/2 divides 64)
   if (P.dtype != 1 || sms < 1 || P.H % 64 != 0 || (P.nq * P.d) % 64 != 0 || P.F % 64 != 0 || P.V % cpk::kT5M != 0 ||
-      P.d % 2 != 0)
+      P.d % 2 != 0 || P.d / 2 > 64 || 64 % (P.d / 2) != 0)
     return false;
   for (int kind = cpk::kQKV; kind <= cpk::kHeads; ++kind) {
     const int K = gemv_K_host(P, kind);

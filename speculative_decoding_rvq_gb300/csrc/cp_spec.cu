@@ -2,6 +2,7 @@
 //
 // Validates arguments, carves the caller's workspace, fills the launch
 // parameter block and enqueues the kernels.  Never allocates device memory.
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -13,6 +14,7 @@
 #include <mutex>
 #include <new>
 #include <string>
+#include <vector>
 
 #include "../../include/cp_spec.h"
 #include "cp_frame.cuh"
@@ -326,10 +328,62 @@ void fill_params(const cp_spec_model* model, const cp_spec_weights* weights, con
   P.prow = at<int>(ws, lay.prow); P.ppos = at<int>(ws, lay.ppos); P.pcode = at<int>(ws, lay.pcode);
   P.row_slot = at<int>(ws, lay.row_slot); P.pslot = at<int>(ws, lay.pslot); P.ttok = at<int>(ws, lay.ttok);
   P.tree = at<cpk::TreeTab>(ws, lay.tree);
+  P.tmaps = at<unsigned char>(ws, lay.tmaps);
   P.plan = at<cpk::Plan>(ws, lay.plan);
   P.st = at<cpk::StreamState>(ws, lay.st); P.sstats = at<cpk::StreamStats>(ws, lay.sstats); P.rope = at<float2>(ws, lay.rope);
   P.top_k = at<int>(ws, lay.top_k); P.temp = at<float>(ws, lay.temp); P.ctl = at<cpk::Control>(ws, lay.ctl);
   P.call = at<cpk::CallArgs>(ws, lay.call);
+}
+
+// TMA tensor maps of the weight matrices for the tcgen05 tiles: bf16, 2D
+// (K contiguous, then rows), boxes of 64 K elements (128 bytes, the
+// 128-byte swizzle span) by the rows one copy of a tile's slab covers (d/2 for
+// the RoPE halves of Wq / Wk / Wv, 64 for gate and up, 128 otherwise).
+// cuTensorMapEncodeTiled comes from the driver through the runtime's entry
+// point query.  Returns false (and leaves the tiles off) if the driver does
+// not provide it or a map is rejected.
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled() {
+  static std::once_flag once;
+  static EncodeTiledFn fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  });
+  return fn;
+}
+
+bool build_tmaps(const cpk::FrameParams& P, std::vector<CUtensorMap>* out) {
+  EncodeTiledFn enc = encode_tiled();
+  if (!enc) return false;
+  out->assign((size_t)7 * P.L + 1, CUtensorMap{});
+  auto one = [&](int idx, const void* base, long long rows, long long K, int box_rows) {
+    const cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+    const cuuint32_t box[2] = {64u, (cuuint32_t)box_rows};
+    const cuuint32_t es[2] = {1u, 1u};
+    return enc(&(*out)[idx], CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  const int half = P.d / 2, QD = P.nq * P.d, KD = P.nkv * P.d;
+  bool ok = true;
+  for (int l = 0; l < P.L && ok; ++l) {
+    ok = one(cpk::t5_map_index(P.L, l, cpk::kMapQ), P.wq[l], QD, P.H, half) &&
+         one(cpk::t5_map_index(P.L, l, cpk::kMapK), P.wk[l], KD, P.H, half) &&
+         one(cpk::t5_map_index(P.L, l, cpk::kMapV), P.wv[l], KD, P.H, half) &&
+         one(cpk::t5_map_index(P.L, l, cpk::kMapO), P.wo[l], P.H, QD, cpk::kT5M) &&
+         one(cpk::t5_map_index(P.L, l, cpk::kMapGate), P.w_gate[l], P.F, P.H, cpk::kT5M / 2) &&
+         one(cpk::t5_map_index(P.L, l, cpk::kMapUp), P.w_up[l], P.F, P.H, cpk::kT5M / 2) &&
+         one(cpk::t5_map_index(P.L, l, cpk::kMapDown), P.w_down[l], P.H, P.F, cpk::kT5M);
+  }
+  if (ok) ok = one(cpk::t5_map_index(P.L, 0, -1), P.head, (long long)(P.G - 1) * P.V, P.H, cpk::kT5M);
+  return ok;
 }
 
 // Pass cap of a call: every pass commits at least one code of every
@@ -480,10 +534,14 @@ cp_spec_status init_impl(const cp_spec_model* model, const cp_spec_weights* weig
 
   cpk::FrameParams& P = c->base;
   fill_params(model, weights, config, N, dp, lay, c->ws, &P, tree);
+  std::vector<CUtensorMap> maps;
+  if (P.t5 && !build_tmaps(P, &maps)) P.t5 = 0;  // no tensor maps: the tiles stay off
 
   cudaError_t e = cpk_host::configure_kernels(P, dp.accept_warps);
   if (e == cudaSuccess) e = cudaMemset(c->ws, 0, lay.total);
   if (e == cudaSuccess && tree) e = cudaMemcpy((void*)P.tree, tree, sizeof *tree, cudaMemcpyHostToDevice);
+  if (e == cudaSuccess && P.t5)
+    e = cudaMemcpy((void*)P.tmaps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice);
   if (e == cudaSuccess)
     e = cudaMemset(P.row_pos, 0xFF, sizeof(int) * (size_t)config->max_streams * P.NS);
   if (e == cudaSuccess)
@@ -676,6 +734,8 @@ cp_spec_status cp_spec_decode_frames_static(const cp_spec_model* model, const cp
 
   cpk::FrameParams P;
   fill_params(model, weights, config, N, dp, lay, ws, &P);
+  std::vector<CUtensorMap> maps;
+  if (P.t5 && !build_tmaps(P, &maps)) P.t5 = 0;
   cpk::CallArgs ca{};
   ca.mode = cpk::kModeDecode;
   ca.B = n_streams; ca.n_frames = n_frames; ca.first_frame = first_frame;
@@ -686,6 +746,9 @@ cp_spec_status cp_spec_decode_frames_static(const cp_spec_model* model, const cp
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(ws, 0, lay.total, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(P.row_pos, 0xFF, sizeof(int) * (size_t)config->max_streams * P.NS, s);
+  // the maps are staged from pageable host memory: the copy has read them when it returns
+  if (e == cudaSuccess && P.t5)
+    e = cudaMemcpyAsync((void*)P.tmaps, maps.data(), maps.size() * sizeof(CUtensorMap), cudaMemcpyHostToDevice, s);
   if (e == cudaSuccess)
     e = cpk_host::launch_init_tables(P.rope, P.G, P.d, (double)model->rope_theta, P.top_k, P.temp, config->max_streams,
                                      config->top_k, config->temperature, s);

@@ -13,23 +13,28 @@
 // N = 2 RB.  The MMAs (kind::f16, bf16 x bf16 -> fp32) accumulate into N
 // TMEM columns; the epilogue reads TMEM lane m (weight row m) and finishes
 // y = D[m][2i] + D[m][2i + 1].  For pair kinds (QKV: RoPE pair e, e + d/2 of
-// a head; gate/up) A row 2j holds the first and A row 2j + 1 the second row
-// of unit j, so one shuffle joins a pair.
+// a head; gate/up) A rows 0..63 hold the first rows of the tile's 64 units and
+// A rows 64..127 their second rows; the epilogue joins a pair through shared
+// memory.
 //
 // K runs in slabs of 64 elements.  A ring of `stages` stages holds per slab
 // the 128 weight rows in the 128-byte-swizzled K-major layout (atoms of 8
 // rows x 128 bytes, 16-byte chunk j of row r at chunk j ^ (r mod 8)) and the
 // tile's raw input rows (fp32, or bf16 for layer 0's code embeddings).  The
 // CTA's warps take three roles, linked by mbarriers:
-//   - four copy warps issue the cp.async copies of a slab into its ring stage
-//     once the MMAs of the stage's previous slab completed (`empty`); each
-//     copy thread's arrival on the stage's `full` barrier fires when its
-//     copies landed (cp.async.mbarrier.arrive.noinc), so a slab is released
-//     as soon as its data is there, whatever the MMAs are doing;
+//   - four copy warps fill a slab's ring stage once the MMAs of the stage's
+//     previous slab completed (`empty`): one thread issues the weight boxes
+//     as TMA tensor copies (cp.async.bulk.tensor with a 128-byte-swizzled
+//     map per weight matrix, 1-4 boxes per slab) with their byte count on
+//     the stage's `wfull` barrier, and every copy thread issues cp.async
+//     copies of the input rows and arrives on `full` when they landed
+//     (cp.async.mbarrier.arrive.noinc), so a slab is released as soon as its
+//     data is there, whatever the MMAs are doing;
 //   - eight conversion warps turn the raw rows of a slab into one of three B
 //     stages (gain, split hi / lo, sums of squares) once the MMAs that read
 //     the B stage before completed, and release it (`bfull`);
-//   - one thread issues the slab's four k16 MMAs and commits them to the
+//   - one warp waits for each converted slab and one of its lanes issues the
+//     slab's four k16 MMAs and commits them to the
 //     ring stage's `empty` barrier, which both the copy warps (ring stage
 //     free) and the conversion warps (B stage free) wait on.
 // The conversion warps execute a generic-to-async proxy fence after
@@ -45,18 +50,17 @@
 // j (their logit slots), compacted in pass-row order.
 #pragma once
 
-constexpr int kT5M = 128;                 // weight rows per tile (the MMA's M)
 constexpr int kT5MaxStages = 6;
 constexpr int kT5SlabBytes = kT5M * 128;  // one slab of the weight tile
 constexpr int kT5BStages = 3;
 constexpr int kT5ConvThreads = 256;       // warps 0-7: conversion and epilogue
 constexpr int kT5CopyThreads = 128;       // warps 8-11: copies
 constexpr int kT5Threads = kT5ConvThreads + kT5CopyThreads + 32;  // warp 12: MMA issue
-constexpr int kT5WRows = kT5M * 8 / kT5CopyThreads;  // weight rows per copy thread (one 16-byte chunk each)
 constexpr int kT5XRows = 64 * 16 / kT5CopyThreads;   // input rows per copy thread, at most
 
 struct T5Shared {
-  uint64_t full[kT5MaxStages];   // ring stage holds its slab (one arrival per copy thread)
+  uint64_t full[kT5MaxStages];   // ring stage holds its slab's input rows (one arrival per copy thread)
+  uint64_t wfull[kT5MaxStages];  // ring stage holds its slab's weight boxes (one arrival plus their bytes)
   uint64_t empty[kT5MaxStages];  // MMAs of the ring stage's slab completed
   uint64_t bfull[kT5BStages];    // B stage converted (one arrival per conversion warp)
   uint64_t dbar;                 // every MMA of the tile completed
@@ -116,7 +120,7 @@ __device__ __forceinline__ bool t5_wait(uint64_t* bar, uint32_t parity, volatile
 
 // Shared-memory carve-up (the host sizes the launch with the same arithmetic).
 struct T5Smem {
-  size_t a, b, raw, gain, ss, rows, list, wrow, xrow, ep, rope, total;
+  size_t a, b, raw, gain, ss, rows, list, wrow, xrow, ep, xch, rope, total;
 };
 __host__ __device__ inline T5Smem t5_smem_layout(int kind, int RB, int stages, int K, int rows_cap, int G, int d) {
   T5Smem o;
@@ -131,6 +135,7 @@ __host__ __device__ inline T5Smem t5_smem_layout(int kind, int RB, int stages, i
   o.wrow = off; off += (size_t)kT5M * 8;                     // global address of each weight row
   o.xrow = off; off += 64 * 8 + 64 * 4;                      // global address and bytes per slab of each input row
   o.ep = off; off += 64 * 24;                                // epilogue: two offsets and the position per row
+  o.xch = off; off += 2 * 64 * 8 * 4;                        // epilogue: second rows of the pairs, per warp group
   o.rope = off; off += kind == kQKV && (size_t)G * (d / 2) * 8 <= (size_t)kRopeSmemBytes ? (size_t)kRopeSmemBytes : 0;
   o.total = off + 1024;  // room to align the base to 1024 bytes
   return o;
@@ -225,6 +230,7 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
       mbar_init(&sh.full[i], kT5CopyThreads);
+      mbar_init(&sh.wfull[i], 1);
       mbar_init(&sh.empty[i], 1);
     }
     for (int i = 0; i < kT5BStages; ++i) mbar_init(&sh.bfull[i], kT5ConvThreads / 32);
@@ -237,9 +243,10 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
                  "r"(N) : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  if (tid < kT5M) {  // global address of weight row tid of the tile (null past the tile's rows)
-    const int j = u0 + (kPair ? (tid >> 1) : tid);
-    s_wrow[tid] = tid < nun * kRpu ? mv_row_src(P, KIND, l, sh.heads, j, kPair ? (tid & 1) : 0) : nullptr;
+  if (tid < kT5M) {  // global address of A row tid of the tile (null past the tile's rows), for the L2 prefetch
+    const int j = u0 + (kPair ? (tid & 63) : tid);
+    const bool in = kPair ? (tid & 63) < nun : tid < nun;
+    s_wrow[tid] = in ? mv_row_src(P, KIND, l, sh.heads, j, kPair ? (tid >> 6) : 0) : nullptr;
   }
   // RoPE table and norm gain (conversion threads, waited for before the epilogue / conversion)
   if (tid < kT5ConvThreads) {
@@ -257,15 +264,44 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
     // ================= copy warps
     const int ct = tid - kT5ConvThreads;
     for (int r = ct; r < nun * kRpu; r += kT5CopyThreads) prefetch_l2(s_wrow[r], (uint32_t)K * 2u);
-    // weight chunks: rows (ct >> 3) + (kT5CopyThreads / 8) q, 16-byte chunk ct & 7 of each
-    // slab row; the rows share r mod 8, so each lands at the same swizzled chunk of its row
-    const unsigned char* wsrc[kT5WRows];
-#pragma unroll
-    for (int q = 0; q < kT5WRows; ++q) {
-      const unsigned char* r = s_wrow[(ct >> 3) + (kT5CopyThreads / 8) * q];
-      wsrc[q] = r != nullptr ? r + (ct & 7) * 16 : nullptr;
+    // the slab's weight boxes (copy thread 0): map, first row, A row, rows
+    int bmap[4], by[4], barow[4], brows[4], nbox = 0;
+    if (ct == 0) {
+      if (KIND == kQKV) {
+        const int half = P.d / 2, nh = 64 / half;
+        for (int i = 0; i < nh; ++i) {
+          const int hh = u0 / half + i;
+          int which, lh;
+          if (hh < P.nq) { which = kMapQ; lh = hh; }
+          else if (hh < P.nq + P.nkv) { which = kMapK; lh = hh - P.nq; }
+          else if (hh < P.nq + 2 * P.nkv) { which = kMapV; lh = hh - P.nq - P.nkv; }
+          else break;
+          const int map = t5_map_index(P.L, l, which);
+          bmap[nbox] = map; by[nbox] = lh * P.d; barow[nbox] = i * half; brows[nbox] = half; ++nbox;
+          bmap[nbox] = map; by[nbox] = lh * P.d + half; barow[nbox] = 64 + i * half; brows[nbox] = half; ++nbox;
+        }
+      } else if (KIND == kGU) {
+        bmap[0] = t5_map_index(P.L, l, kMapGate); by[0] = u0; barow[0] = 0; brows[0] = 64;
+        bmap[1] = t5_map_index(P.L, l, kMapUp); by[1] = u0; barow[1] = 64; brows[1] = 64;
+        nbox = 2;
+      } else if (KIND == kHeads) {
+        const int hi = u0 / P.V;
+        bmap[0] = t5_map_index(P.L, 0, -1); by[0] = (sh.heads[hi] - 1) * P.V + (u0 - hi * P.V); barow[0] = 0;
+        brows[0] = kT5M;
+        nbox = 1;
+      } else {
+        bmap[0] = t5_map_index(P.L, l, KIND == kO ? kMapO : kMapDown); by[0] = u0; barow[0] = 0; brows[0] = kT5M;
+        nbox = 1;
+      }
     }
-    const uint32_t wdst = (uint32_t)((ct >> 3) * 128 + (((ct & 7) ^ ((ct >> 3) & 7)) << 4));
+    uint32_t wbytes = 0;
+    for (int q = 0; q < nbox; ++q) {
+      wbytes += (uint32_t)brows[q] * 128u;
+      // the maps were written to global memory by the host: acquire them for the tensor-map proxy
+      asm volatile("fence.proxy.tensormap::generic.acquire.gpu [%0], 128;" ::"l"(P.tmaps + (size_t)bmap[q] * 128)
+                   : "memory");
+    }
+    int last_w = -1;  // the last slab whose weight boxes thread 0 issued
     pdl_wait();
     if (ct < cnt) {  // input row ct of the tile
       const ActRow a = act_row<__nv_bfloat16>(P, sh.ca, pr, KIND, l, s_list[ct]);
@@ -293,10 +329,18 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
           ok = false;
           break;
         }
-        unsigned char* wst = abase + (size_t)st * kT5SlabBytes + wdst;
-#pragma unroll
-        for (int q = 0; q < kT5WRows; ++q)
-          if (wsrc[q] != nullptr) cp_async16(wst + q * (kT5CopyThreads * 16), wsrc[q] + (size_t)j * 128);
+        if (ct == 0) {  // the weight boxes, their bytes announced on the stage's barrier first
+          unsigned char* wst = abase + (size_t)st * kT5SlabBytes;
+          const uint32_t bar = smem_u32(&sh.wfull[st]);
+          last_w = j;
+          asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(wbytes) : "memory");
+          for (int q = 0; q < nbox; ++q)
+            asm volatile(
+                "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
+                ::"r"(smem_u32(wst + barow[q] * 128)), "l"(P.tmaps + (size_t)bmap[q] * 128), "r"(j * 64), "r"(by[q]),
+                  "r"(bar)
+                : "memory");
+        }
         unsigned char* xst = rawb + (size_t)st * RB * 256 + xdst;
 #pragma unroll
         for (int q = 0; q < kT5XRows; ++q)
@@ -306,21 +350,26 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
       }
     }
     cp_async_wait_all();
-    // an aborted CTA leaves slabs nobody waits for: give their arrivals time to land
-    if (!ok) __nanosleep(4000);
+    if (!ok) {
+      // an aborted CTA leaves slabs nobody waits for: the weight boxes of the
+      // last slab of each stage complete on their own barrier (bounded wait),
+      // and the input copies' arrivals are given time to land
+      if (ct == 0)
+        for (int j = max(0, last_w - NST + 1); j <= last_w; ++j)
+          mbar_wait_bounded(&sh.wfull[j % NST], (uint32_t)(j / NST) & 1u, &P.ctl->status, P.wait_ns);
+      __nanosleep(4000);
+    }
   } else if (warp == (kT5ConvThreads + kT5CopyThreads) / 32) {
-    // ================= MMA thread
-    if (lane == 0) {
-      bool ok = !stall || t5_wait(&sh.hbar, 0, abort, &P.ctl->status, P.wait_ns);
-      const uint32_t idesc = t5_idesc(N);
-      int s = 0;
-      for (; s < slabs && ok; ++s) {
-        const int bs = s % kT5BStages;
-        if (!t5_wait(&sh.bfull[bs], (uint32_t)(s / kT5BStages) & 1u, abort, &P.ctl->status, P.wait_ns)) {
-          ok = false;
-          break;
-        }
-        asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+    // ================= MMA warp: the whole warp waits (converged); lane 0 issues
+    bool ok = !stall || t5_wait(&sh.hbar, 0, abort, &P.ctl->status, P.wait_ns);
+    ok = __all_sync(0xffffffffu, ok);
+    const uint32_t idesc = t5_idesc(N);
+    for (int s = 0; s < slabs && ok; ++s) {
+      const int bs = s % kT5BStages;
+      ok = __all_sync(0xffffffffu, t5_wait(&sh.bfull[bs], (uint32_t)(s / kT5BStages) & 1u, abort, &P.ctl->status, P.wait_ns));
+      if (!ok) break;
+      asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+      if (lane == 0) {
         const uint32_t a0 = smem_u32(abase + (size_t)(s % NST) * kT5SlabBytes);
         const uint32_t b0 = smem_u32(bbase + (size_t)bs * RB * 256);
 #pragma unroll
@@ -333,11 +382,14 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
         asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(&sh.empty[s % NST]))
                      : "memory");
       }
-      // every MMA issued (or none) completes before the barrier's phase does
+      __syncwarp();
+    }
+    // every MMA issued (or none) completes before the barrier's phase does
+    if (lane == 0)
       asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(&sh.dbar))
                    : "memory");
-      if (!ok) mbar_wait_bounded(&sh.dbar, 0, &P.ctl->status, P.wait_ns);  // nothing in flight at exit
-    }
+    __syncwarp();
+    if (!ok && lane == 0) mbar_wait_bounded(&sh.dbar, 0, &P.ctl->status, P.wait_ns);  // nothing in flight at exit
   } else {
     // ================= conversion warps (then the epilogue)
     pdl_wait();
@@ -366,11 +418,11 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
       // slab s landed; the MMAs of slab s - kT5BStages (the B stage's last reader) completed
       const int sp = s - kT5BStages;
       if (!t5_wait(&sh.full[s % NST], (uint32_t)(s / NST) & 1u, abort, &P.ctl->status, P.wait_ns) ||
+          !t5_wait(&sh.wfull[s % NST], (uint32_t)(s / NST) & 1u, abort, &P.ctl->status, P.wait_ns) ||
           (sp >= 0 && !t5_wait(&sh.empty[sp % NST], (uint32_t)(sp / NST) & 1u, abort, &P.ctl->status, P.wait_ns))) {
         ok = false;
         break;
       }
-      asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the weight slab (cp.async writes)
       if (cv) {
         const unsigned char* raw = rawb + (size_t)(s % NST) * RB * 256 + ci * 256;
         unsigned char* bst = bbase + (size_t)bs * RB * 256;
@@ -435,16 +487,24 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
       s_inv[tid] = kNormed ? rsqrtf(t / (float)K + P.eps) : 1.0f;
     }
     if (ok && !t5_wait(&sh.dbar, 0, abort, &P.ctl->status, P.wait_ns)) ok = false;
-    asm volatile("bar.sync 2, %0;" ::"n"(kT5ConvThreads) : "memory");
-    if (ok && !*abort) {
+    // one decision for all conversion warps (the epilogue's group barriers need all of them)
+    int go = (ok && !*abort) ? 1 : 0;
+    asm volatile("{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.and.pred q, 2, %2, p;\n selp.b32 %0, 1, 0, q;\n}"
+                 : "=r"(go)
+                 : "r"(go), "n"(kT5ConvThreads)
+                 : "memory");
+    if (go) {
       asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
       // epilogue: warp w reads TMEM lanes 32 (w mod 4) .. + 31 (weight rows) and
       // the column chunks (w / 4), (w / 4) + 2, ... of 16 columns (8 tile rows)
       const int m = 32 * (warp & 3) + lane;
-      const bool mvalid = m < nun * kRpu;
+      const bool second = kPair && m >= 64;          // pair kinds: A rows 64..127 hold the second rows
+      const int mu = kPair ? (m & 63) : m;           // the row's unit within the tile
+      const bool mvalid = mu < nun;
+      float* xch = reinterpret_cast<float*>(smem + L.xch) + (warp >> 2) * 64 * 8;
       const float2* rope = rope_in_smem ? s_rope : P.rope;
       // per-lane constants of the weight row's unit
-      const int uu = u0 + (kPair ? (m >> 1) : m);
+      const int uu = u0 + mu;
       int half = 0, hh = 0, e = 0;
       float* qkv_dst = nullptr;
       long long qkv_off = 0;
@@ -470,13 +530,33 @@ __global__ void __launch_bounds__(kT5Threads, 1) t5_kernel(const __grid_constant
               "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
             : "r"(tmem + ((uint32_t)(32 * (warp & 3)) << 16) + (uint32_t)(16 * ch)));
         asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+        float yv[8], pv[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i = 8 * ch + q;
+          yv[q] = (__uint_as_float(v[2 * q]) + __uint_as_float(v[2 * q + 1])) * s_inv[i < cnt ? i : 0];
+          pv[q] = 0.0f;
+        }
+        if (kPair) {
+          // the second rows (warps 2, 3 of the group) hand their values to the first rows
+          // (warps 0, 1): named barrier 3 + group among the group's four warps
+          if (second)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) xch[(m - 64) * 8 + q] = yv[q];
+          asm volatile("bar.sync %0, 128;" ::"r"(3 + (warp >> 2)) : "memory");
+          if (!second)
+#pragma unroll
+            for (int q = 0; q < 8; ++q) pv[q] = xch[m * 8 + q];
+          asm volatile("bar.sync %0, 128;" ::"r"(3 + (warp >> 2)) : "memory");
+          if (second) continue;
+        }
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const int i = 8 * ch + q;
           const int ii = i < cnt ? i : 0;
-          const float y = (__uint_as_float(v[2 * q]) + __uint_as_float(v[2 * q + 1])) * s_inv[ii];
-          const float partner = __shfl_xor_sync(0xffffffffu, y, 1);  // the other row of a pair
-          if (i >= cnt || !mvalid || (kPair && (m & 1))) continue;
+          const float y = yv[q];
+          const float partner = pv[q];  // the other row of a pair
+          if (i >= cnt || !mvalid) continue;
           const long long e0 = s_ep[3 * ii];
           if (KIND == kQKV) {
             const int pos = (int)s_ep[3 * ii + 2];
