@@ -6,11 +6,13 @@
 //
 // Logit mode (rows 16-byte aligned): one warp owns a round.  It processes the
 // round's 2N-1 rows (top-k / temperature / softmax into index-ordered
-// lists), each row staged by cp.async into one of two warp-private buffers
-// while the warp works on the previous one -- the first row of the warp's
-// next round included -- then one lane samples the drafts and runs the exact
-// left-to-right acceptance with residual / bonus draws.  No CTA barrier: the
-// warps of a CTA run independent rounds.
+// lists), each row staged by cp.async into the warp's row buffer, then one
+// lane samples the drafts and runs the exact left-to-right acceptance with
+// residual / bonus draws.  No CTA barrier: the warps of a CTA run
+// independent rounds.  A row takes tens of microseconds of one warp's
+// instructions, so the warp does not prefetch the next row (its 1 us copy is
+// hidden by the other warps); one buffer instead of two leaves room for more
+// resident warps, which the issue-bound row processing needs.
 //
 // Probability mode (rows already processed float32 distributions), and
 // logit rows that are not 16-byte aligned: one CTA per round, one warp per
@@ -85,15 +87,13 @@ __device__ void round_accept(int r, int N, int V, int KC, unsigned long long see
 }
 
 // Logit mode, one warp per round (rows 16-byte aligned: V a multiple of 4 and
-// 16-byte aligned bases).  Per warp: two row buffers of V floats, the
-// histogram, the exp buffer and the round's lists.  Work item n of a warp is
-// row n mod nrows of its (n / nrows)-th round; item n + 1 is copied in while
-// item n is processed.
+// 16-byte aligned bases).  Per warp: a row buffer of V floats, the
+// histogram, the exp buffer and the round's lists.
 constexpr int kAcceptWarpWarps = 4;
 __host__ __device__ inline size_t accept_warp_bytes(int N, int V, int KC) {
   const int nrows = 2 * N - 1;
   const size_t buf = ((size_t)V * 4 + 15) / 16 * 16;
-  return 2 * buf + 1024 + ((size_t)KC * 4 + 15) / 16 * 16 + ((size_t)nrows * KC * 8 + (size_t)nrows * 4 + 15) / 16 * 16;
+  return buf + 1024 + ((size_t)KC * 4 + 15) / 16 * 16 + ((size_t)nrows * KC * 8 + (size_t)nrows * 4 + 15) / 16 * 16;
 }
 
 __global__ void __launch_bounds__(kAcceptWarpWarps * 32) accept_warp_kernel(int R, int N, int V, int k, float T,
@@ -109,10 +109,10 @@ __global__ void __launch_bounds__(kAcceptWarpWarps * 32) accept_warp_kernel(int 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const size_t buf_bytes = ((size_t)V * 4 + 15) / 16 * 16;
   unsigned char* wb = smem + (size_t)warp * accept_warp_bytes(N, V, KC);
-  uint32_t* buf[2] = {reinterpret_cast<uint32_t*>(wb), reinterpret_cast<uint32_t*>(wb + buf_bytes)};
-  uint32_t* hist = reinterpret_cast<uint32_t*>(wb + 2 * buf_bytes);
-  float* ebuf = reinterpret_cast<float*>(wb + 2 * buf_bytes + 1024);
-  int* lidx = reinterpret_cast<int*>(wb + 2 * buf_bytes + 1024 + ((size_t)KC * 4 + 15) / 16 * 16);
+  uint32_t* buf = reinterpret_cast<uint32_t*>(wb);
+  uint32_t* hist = reinterpret_cast<uint32_t*>(wb + buf_bytes);
+  float* ebuf = reinterpret_cast<float*>(wb + buf_bytes + 1024);
+  int* lidx = reinterpret_cast<int*>(wb + buf_bytes + 1024 + ((size_t)KC * 4 + 15) / 16 * 16);
   float* lprob = reinterpret_cast<float*>(lidx + (size_t)nrows * KC);
   int* lcnt = reinterpret_cast<int*>(lprob + (size_t)nrows * KC);
   const int wpc = blockDim.x >> 5;  // warps per CTA (set by the shared memory a warp needs)
@@ -122,18 +122,12 @@ __global__ void __launch_bounds__(kAcceptWarpWarps * 32) accept_warp_kernel(int 
     return i < ND ? drf + ((size_t)r * ND + i) * V : tgt + ((size_t)r * N + (i - ND)) * V;
   };
   if (gw >= R) return;
-  warp_copy_async(buf[0], src(gw, 0), V * 4);
-  asm volatile("cp.async.commit_group;" ::: "memory");
-  int n = 0;
   for (int r = gw; r < R; r += nw) {
-    for (int i = 0; i < nrows; ++i, ++n) {
-      // copy in the next item (this round's next row, or the next round's first)
-      const int r2 = i + 1 < nrows ? r : r + nw, i2 = i + 1 < nrows ? i + 1 : 0;
-      if (r2 < R) warp_copy_async(buf[(n + 1) & 1], src(r2, i2), V * 4);
-      asm volatile("cp.async.commit_group;" ::: "memory");
-      asm volatile("cp.async.wait_group 1;" ::: "memory");  // this item's copies
+    for (int i = 0; i < nrows; ++i) {
+      warp_copy_async(buf, src(r, i), V * 4);
+      cp_async_wait_all();
       __syncwarp();
-      const int c = warp_process_staged(buf[n & 1], V, k, T, hist, ebuf, lidx + (size_t)i * KC, lprob + (size_t)i * KC);
+      const int c = warp_process_staged(buf, V, k, T, hist, ebuf, lidx + (size_t)i * KC, lprob + (size_t)i * KC);
       if (lane == 0) lcnt[i] = c;
       __syncwarp();
     }
