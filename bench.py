@@ -276,7 +276,7 @@ def large_line(peak, frames=256):
     G = spec.num_code_groups
     out = {"model": "H2048, 8L, 32q/8kv x64, FFN6144, V4096, G32, bf16", "frames": frames, "temperature": 0.8}
     # N4_adaptive: the per-stream adaptive window (keep an offset at >= 30 % acceptance,
-    # judged after 16 reached drafts)
+    # decided after 16 reached drafts)
     for name, n, pct, B in (("N0", 0, 0, 1), ("N4", 4, 0, 1), ("N4_adaptive", 4, 30, 1), ("N4_B8", 4, 0, 8),
                             ("N4_B64", 4, 0, 64), ("N4_B256", 4, 0, 256)):
         F = frames
