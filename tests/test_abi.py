@@ -114,3 +114,40 @@ def test_context_free_calls_reject_bad_arguments(lib):
         assert getattr(lib, fn)(None, *args) == b.E_INVALID, fn
     assert lib.cp_spec_launch_count(None) >= 0
     lib.cp_spec_destroy(None)
+
+
+def _tree(b, par, rk):
+    import numpy as np
+    p = np.ascontiguousarray(par, dtype=np.int32)
+    r = np.ascontiguousarray(rk, dtype=np.int32)
+    return b.Tree(len(p), p.ctypes.data, r.ctypes.data), (p, r)
+
+
+def test_tree_workspace_validates_the_tree(lib):
+    """cp_spec_workspace_bytes_tree (host only): a well-formed tree ("RVQ Position Aware
+    Speculative Decoding for On Device TTS", section 2.2) is sized with one row slot per
+    node plus the root and one KV slot per node past the G positions; malformed trees
+    (parent not earlier, siblings out of rank order or repeated, depth above 7, rank at or
+    above the list capacity, more than 62 nodes) are rejected with 0."""
+    from speculative_decoding_rvq_gb300 import binding as b, synth as S
+    m = b.model_struct(S.TINY_FP32)
+    cfg = _cfg(b, top_k=8)
+    ok, keep = _tree(b, [-1, -1, 0, 0, 1, 2, 3], [0, 1, 0, 1, 0, 0, 0])
+    small, keep2 = _tree(b, [-1, 0, 1], [0, 0, 0])
+    n_ok = lib.cp_spec_workspace_bytes_tree(C.byref(m), C.byref(cfg), C.byref(ok))
+    n_small = lib.cp_spec_workspace_bytes_tree(C.byref(m), C.byref(cfg), C.byref(small))
+    assert n_ok > n_small > 0
+    bad = [
+        ([0], [0]),                                   # parent not earlier
+        ([-1, -1], [1, 0]),                           # siblings out of rank order
+        ([-1, -1], [0, 0]),                           # repeated rank
+        ([-1, 0, 1, 2, 3, 4, 5, 6], [0] * 8),         # depth 8
+        ([-1], [8]),                                  # rank at the list capacity (top-k 8)
+        ([-1] * 63, list(range(63))),                 # 63 nodes
+    ]
+    for par, rk in bad:
+        t, keep3 = _tree(b, par, rk)
+        assert lib.cp_spec_workspace_bytes_tree(C.byref(m), C.byref(_cfg(b, top_k=256)) if len(par) == 63
+                                                else C.byref(cfg), C.byref(t)) == 0, (par, rk)
+    empty, keep4 = _tree(b, [], [])
+    assert lib.cp_spec_workspace_bytes_tree(C.byref(m), C.byref(cfg), C.byref(empty)) == 0
