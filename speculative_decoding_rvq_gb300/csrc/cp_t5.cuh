@@ -37,11 +37,12 @@
 //     slab's four k16 MMAs and commits them to the
 //     ring stage's `empty` barrier, which both the copy warps (ring stage
 //     free) and the conversion warps (B stage free) wait on.
-// The conversion warps execute a generic-to-async proxy fence after
-// acquiring a slab and again after writing its B stage, before handing it
-// on, so the cp.async and st.shared writes are visible to the tensor core.
+// The conversion warps execute a generic-to-async proxy fence after writing
+// a B stage, before handing it on, so their st.shared writes are visible to
+// the tensor core (the weight boxes arrive through the async proxy itself).
 // Every wait is bounded; a wait that runs out raises the device status and
-// an abort flag that ends every other wait of the CTA.  A row's sum of
+// an abort flag that ends every other wait of the CTA, and an aborted CTA
+// waits (bounded) for its weight boxes still in flight before it exits.  A row's sum of
 // squares is 16 partial sums, one per 16-byte chunk column of the slab rows
 // (over the slabs in order), added in column order: no reduction order
 // depends on the tile height or on which rows share the pass.
