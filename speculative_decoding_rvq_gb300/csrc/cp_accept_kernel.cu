@@ -89,7 +89,7 @@ __device__ void round_accept(int r, int N, int V, int KC, unsigned long long see
 // Logit mode, one warp per round (rows 16-byte aligned: V a multiple of 4 and
 // 16-byte aligned bases).  Per warp: a row buffer of V floats, the
 // histogram, the exp buffer and the round's lists.
-constexpr int kAcceptWarpWarps = 4;
+constexpr int kAcceptWarpWarps = 2;
 __host__ __device__ inline size_t accept_warp_bytes(int N, int V, int KC) {
   const int nrows = 2 * N - 1;
   const size_t buf = ((size_t)V * 4 + 15) / 16 * 16;
@@ -201,7 +201,7 @@ cudaError_t launch_accept_batch(int R, int N, int V, int k, float T, unsigned lo
   const size_t per_warp = cpk::accept_warp_bytes(N, V, KC);
   const int wpc = (int)std::min<size_t>(cpk::kAcceptWarpWarps, kAcceptSmemLimit / per_warp);
   if (mode == 0 && wpc >= 1 && V % 4 == 0 && ((uintptr_t)tgt & 15u) == 0 && ((uintptr_t)drf & 15u) == 0) {
-    // one warp per round, as many warps per CTA as their shared memory allows (up to 4);
+    // one warp per round, as many warps per CTA as their shared memory allows (up to 2: small CTAs pack more warps per SM);
     // enough CTAs to fill every SM, at most one round per warp
     const size_t smem = per_warp * wpc;
     // the limit is the most a CTA may ask for, so calls of every shape can share it
