@@ -128,3 +128,28 @@ def test_malformed_trees_are_rejected(orc, par, rk):
     w, m, dw = _model(orc, spec)
     with pytest.raises(binding.CpSpecError):
         binding.CpSpec(spec, dw, 4, 50, 0.9, 1, tree=(par, rk))
+
+
+def test_tree_rounds_on_the_tcgen05_tiles(orc):
+    """8 streams x 8 row slots = 64 rows per pass: the GEMVs run as tcgen05 tiles, whose
+    epilogue appends each tree node's K/V to its own slot.  Greedy: the rank-0 chain tree
+    equals the chain path on the same tiles, and the sparse tree equals the oracle's tree
+    decode (which equals greedy AR)."""
+    from speculative_decoding_rvq_gb300 import binding, synth as S
+    spec = dataclasses.replace(S.TTS06B_BF16, n_layers=2)
+    w, m, dw = _model(orc, spec)
+    G = spec.num_code_groups
+    B = 8
+    x, c0 = S.gen_frames(spec, B, 1, seed=13)
+    ch = binding.CpSpec(spec, dw, 4, 50, 0.0, 1, max_streams=B)
+    gc = _decode(ch, x, c0, G)
+    tr = binding.CpSpec(spec, dw, 4, 50, 0.0, 1, max_streams=B, tree=([-1, 0, 1], [0, 0, 0]))
+    gt = _decode(tr, x, c0, G)
+    assert np.array_equal(gt, gc)
+    par, rk = TREES["sparse"]
+    sp = binding.CpSpec(spec, dw, 4, 50, 0.0, 1, max_streams=B, tree=(par, rk))
+    gs = _decode(sp, x, c0, G)
+    o, _, log = m.decode_frames_tree(par, rk, 50, 0.0, 1, x[:, :2], c0[:, :2], log_cap=10000)  # 2 streams: oracle time
+    compare_codes_with_margins(gs[:, :2], o, log, 1e-3, max_frac=0.5)
+    for cp in (ch, tr, sp):
+        cp.close()
