@@ -112,6 +112,97 @@ def test_tree_law_equals_autoregressive_law(orc):
     assert z < 3.7, (chi2, df)
 
 
+def _max_tree():
+    """A tree at both limits: 62 nodes, depth 7, parents first, siblings in
+    ascending rank.  Depth 1 holds ranks 0..7; below it the rank-0 path
+    keeps branching (8, 6, 4, 3, 3, 2 children), with smaller side branches."""
+    par, rk = [], []
+
+    def add(p, ranks):
+        first = len(par)
+        for r in ranks:
+            par.append(p)
+            rk.append(r)
+        return list(range(first, len(par)))
+
+    l1 = add(-1, range(8))
+    l2 = add(l1[0], range(8)) + add(l1[1], range(4))
+    for p in l1[2:]:
+        l2 += add(p, range(2))
+    l3 = add(l2[0], range(6))
+    for p in l2[1:8]:
+        l3 += add(p, [0])
+    l4 = add(l3[0], range(4))
+    for p in l3[1:6]:
+        l4 += add(p, [0])
+    l5 = add(l4[0], range(3))
+    l6 = add(l5[0], range(3))
+    add(l6[0], range(2))
+    return par, rk
+
+
+def test_max_tree_shape():
+    par, rk = _max_tree()
+    dep = []
+    for p in par:
+        dep.append(1 if p < 0 else dep[p] + 1)
+    assert len(par) == 62 and max(dep) == 7
+
+
+@pytest.mark.parametrize("G", [9, 16])
+def test_max_tree_greedy_equals_greedy_ar(orc, G):
+    spec = _small(G=G)
+    m = orc.Model(spec, S.gen_weights(spec, seed=3, std=0.5))
+    x, c0 = S.gen_frames(spec, 2, 4, seed=1)
+    ar, _, _ = m.decode_frames(0, 50, 0.0, 1, x, c0)
+    tr, st, _ = m.decode_frames_tree(*_max_tree(), 50, 0.0, 1, x, c0)
+    assert np.array_equal(tr, ar)
+    # the 8 depth-1 candidates are the whole vocabulary: every round accepts depth 1
+    assert st["accepted_by_offset"][1] == st["rounds"]
+
+
+@pytest.mark.parametrize("G", [9, 16])
+def test_max_tree_zero_heads_walks_to_full_depth(orc, G):
+    """Zero lm_heads: every logit is 0, so the greedy target is code 0 and the
+    rank-r candidate of every depth is code r.  The rank-0 path (depth 7) is
+    then accepted node by node as deep as the frame allows, the bonus follows
+    when the path stops short of c_{G-1}, and each round verifies the root
+    plus every node short of the frame end."""
+    spec = _small(G=G)
+    w = S.gen_weights(spec, seed=3, std=0.5)
+    w = {**w, "lm_head": np.zeros_like(w["lm_head"])}
+    m = orc.Model(spec, w)
+    F, B = 4, 2
+    x, c0 = S.gen_frames(spec, B, F, seed=1)
+    par, rk = _max_tree()
+    dep = []
+    for p in par:
+        dep.append(1 if p < 0 else dep[p] + 1)
+    codes, st, log = m.decode_frames_tree(par, rk, 50, 0.0, 1, x, c0, log_cap=500)
+    assert np.all(codes[:, :, 1:] == 0)
+    # expected rounds of one frame: from s = 1, accept min(7, G-1-s) codes, plus a bonus below G-1
+    acc = [0] * 9
+    rounds = bonus = 0
+    rows, s = [], 1
+    while s < G - 1:
+        n = min(7, G - 1 - s)
+        rows.append(1 + sum(1 for t in dep if s + t <= G - 1))
+        for t in range(1, n + 1):
+            acc[t] += 1
+        rounds += 1
+        s += n
+        if s < G - 1:
+            s += 1
+            bonus += 1
+    FB = F * B
+    assert st["rounds"] == FB * rounds and st["passes"] == FB * (rounds + 1)
+    assert st["committed"] == FB * (G - 1) and st["bonus"] == FB * bonus and st["rejections"] == 0
+    assert st["accepted_by_offset"] == [FB * a for a in acc]
+    first = log[log["s"] == 1]
+    assert np.all(first["n_acc"] == min(7, G - 2)) and np.all(first["m"] == rows[0])
+    assert sorted(set(log["m"][log["s"] > 0].tolist())) == sorted(set(rows))
+
+
 @pytest.mark.parametrize("par,rk", [([0], [0]), ([-1, -1], [1, 0]), ([-1, -1], [0, 0]), ([-1, 2, 0], [0, 0, 0]),
                                     ([-1], [-1])])
 def test_malformed_trees_are_rejected(orc, par, rk):
