@@ -465,13 +465,51 @@ def expected_accepted_greedy(tgt, drf) -> float:
     return float(torch.cumprod(eq, dim=1).sum(1).mean().item())
 
 
+def accepted_tail(tgt, drf, k: int, T: float) -> list:
+    """P(a round accepts at least j drafts) for j = 1..N-1, averaged over the rounds of
+    the given logits: prod_{t<=j} beta_t with beta_t = sum_v min(p_t(v), q_t(v)) when
+    sampling ("Speculative Decoding, Beyond Text", section 02), the indicator that the
+    first j draft argmaxes equal the target argmaxes when greedy (T = 0)."""
+    import torch
+    n = drf.shape[1]
+    if T > 0:
+        def proc(x):
+            z = x / T
+            v, i = z.topk(min(k, z.shape[-1]), dim=-1)
+            return torch.zeros_like(z).scatter_(-1, i, torch.softmax(v, dim=-1))
+        per = torch.minimum(proc(tgt[:, :n]), proc(drf)).sum(-1).to(torch.float64)
+    else:
+        per = (drf.argmax(-1) == tgt[:, :n].argmax(-1)).to(torch.float64)
+    return [float(v) for v in torch.cumprod(per, dim=1).mean(0).tolist()]
+
+
+def accept_extras(n_accepted, N: int, V: int, ms: float, tail: list, peak: float) -> dict:
+    """Per-line analysis of the acceptance microbench, from the kernel's accepted counts
+    [R]: the histogram of accepted drafts (fractions of rounds with 0..N-1) beside the
+    closed-form one from `tail` (P(n = j) = P(n >= j) - P(n >= j + 1)), and the bytes of
+    the rows a left-to-right chain must read, per second: the N - 1 draft rows and the
+    target rows up to the first rejection or the bonus (n + 1 of them), so (N + n) V 4
+    bytes for a round that accepts n."""
+    import torch
+    na = n_accepted.reshape(-1).long()
+    R = na.numel()
+    hist = torch.bincount(na, minlength=N)[:N].to(torch.float64) / R
+    t = [1.0] + list(tail) + [0.0]
+    rows = float((N + na).sum().item())
+    gbs = rows * V * 4 / (ms / 1e3) / 1e9
+    return {"accept_hist": [round(float(h), 4) for h in hist.tolist()],
+            "closed_form_hist": [round(t[j] - t[j + 1], 4) for j in range(N)],
+            "rows_touched_GB_s": round(gbs, 1), "rows_touched_hbm_frac": round(gbs / peak, 4)}
+
+
 def accept_microbench(peak):
     """Acceptance kernels alone (the acceptance-kernel microbench configuration): 65536
     independent rounds, V 2048, target logits N(0, 3^2), draft logits
     rho * target + sqrt(1 - rho^2) * N(0, 3^2) for rho in {0.3, 0.7, 0.95}, N in {2, 4, 8},
     top-k 50; sampling mode (T 0.9, Philox draws) and greedy mode (T 0, argmax equality).
-    Each line: rounds/s, the logit bytes read per second against the measured HBM peak, and
-    the mean accepted drafts per round beside its closed form for the same inputs."""
+    Each line: rounds/s, the logit bytes read per second against the measured HBM peak, the
+    mean accepted drafts per round and their histogram, each beside its closed form for the
+    same inputs, and the bytes of the rows the chain must read (rows touched) per second."""
     import torch
     from speculative_decoding_rvq_gb300 import binding
     R, V = 65536, 2048
@@ -504,6 +542,10 @@ def accept_microbench(peak):
                         expected_accepted(tgt, drf, TOP_K, TEMP) if T > 0 else expected_accepted_greedy(tgt, drf), 4)
                 except Exception as exc:  # analysis only: never lose the measured line over it
                     line["closed_form_accepted"] = f"unavailable: {type(exc).__name__}"
+                try:
+                    line.update(accept_extras(na, N, V, ms, accepted_tail(tgt, drf, TOP_K, T), peak))
+                except Exception as exc:  # analysis only, as above
+                    line["accept_hist"] = f"unavailable: {type(exc).__name__}"
                 res[f"N{N}_rho{rho}_{mode}"] = line
             del drf
         del tgt

@@ -42,3 +42,33 @@ def test_closed_form_predicts_the_oracle_acceptance(orc):
     emp = float(np.mean(n_acc))
     se = float(np.std(n_acc)) / np.sqrt(R)
     assert abs(emp - cf) < 4 * se + 1e-3, (emp, cf, se)
+
+
+def test_acceptance_histogram_and_rows_touched(orc):
+    """The benchmark's per-line histogram of accepted drafts, on the oracle's own
+    acceptance: within sampling error of the closed form P(n = j) (sampling), equal
+    to it (greedy, where acceptance is decided by argmaxes alone); the tail sums to
+    the closed-form mean; rows touched are (N + n) rows of V floats per round."""
+    import bench
+    from speculative_decoding_rvq_gb300 import synth as S
+    R, N, V, k = 4096, 4, 64, 10
+    tgt, drf = S.gen_accept_inputs(R, N, V, 0.7, seed=5, block_rounds=1024)
+    tt, dt = torch.from_numpy(tgt), torch.from_numpy(drf)
+    for T in (0.9, 0.0):
+        tail = bench.accepted_tail(tt, dt, k, T)
+        assert len(tail) == N - 1 and all(1.0 >= a >= b >= 0.0 for a, b in zip(tail, tail[1:]))
+        mean = bench.expected_accepted(tt, dt, k, T) if T > 0 else bench.expected_accepted_greedy(tt, dt)
+        assert abs(sum(tail) - mean) < 1e-6  # the mean's products are float32, the tail's float64
+        _, n_acc, _, _ = orc.accept_batch(tgt, drf, k, T, 9)
+        n_acc = np.asarray(n_acc)
+        ex = bench.accept_extras(torch.from_numpy(n_acc), N, V, 2.0, tail, 500.0)
+        got, cf = np.array(ex["accept_hist"]), np.array(ex["closed_form_hist"])
+        assert got.shape == cf.shape == (N,) and abs(got.sum() - 1) < 1e-3 and abs(cf.sum() - 1) < 1e-3
+        if T > 0:
+            se = np.sqrt(np.maximum(cf * (1 - cf), 1e-6) / R)
+            assert np.all(np.abs(got - cf) < 4 * se + 1e-3), (got, cf)
+        else:
+            assert np.array_equal(got, cf), (got, cf)
+        want = float(np.sum(N + n_acc.astype(np.int64))) * V * 4 / 2e-3 / 1e9
+        assert abs(ex["rows_touched_GB_s"] - round(want, 1)) < 1e-9
+        assert abs(ex["rows_touched_hbm_frac"] - round(want / 500.0, 4)) < 1e-9
