@@ -37,14 +37,6 @@ __device__ __forceinline__ float philox_uniform(uint64_t seed, uint32_t stream, 
 }
 
 // ----------------------------------------------------------------- memory
-__device__ __forceinline__ uint4 ldg_stream(const void* p) {
-  uint4 v;
-  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-               : "l"(p));
-  return v;
-}
-
 // Bulk prefetch of a byte range into L2 (Hopper/Blackwell bulk-copy unit).
 // addr and bytes must be multiples of 16.
 __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
@@ -125,18 +117,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// try_wait with a suspend-time hint: the thread sleeps until the phase
-// completes or about `hint_ns` passed, instead of spinning.
-__device__ __forceinline__ bool mbar_try_wait_hint(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-      : "memory");
-  return ok != 0;
-}
-
 // Wait for phase `parity` of `bar` to complete, bounded by timeout_ns of
 // %globaltimer; returns false (after raising the status word) on timeout.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status, uint64_t timeout_ns) {
@@ -158,18 +138,6 @@ __device__ __forceinline__ float key_float(uint32_t k) {
   return __uint_as_float((k & 0x80000000u) ? (k & 0x7FFFFFFFu) : ~k);
 }
 
-
-__device__ __forceinline__ uint64_t ld_acquire_u64(const unsigned long long* p) {
-  unsigned long long v;
-  asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
-  return v;
-}
-
-__device__ __forceinline__ int ld_relaxed_i32(const int* p) {
-  int v;
-  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
-  return v;
-}
 
 // bf16x2 word -> two floats (low half = element 0).
 __device__ __forceinline__ float2 bf16x2_to_f2(uint32_t w) {
@@ -198,22 +166,6 @@ __device__ __forceinline__ uint32_t float_key(float f) {
 enum : int { kStatusOk = 0, kStatusTimeout = -5, kStatusDevice = -7 };
 
 __device__ __forceinline__ void raise_status(int* status, int code) { atomicCAS(status, 0, code); }
-
-// ------------------------------------------------------ exchange elements
-// 64-bit words {value, flag}: the writer stores both halves with one 64-bit
-// access, so a reader that sees the expected flag also sees the value.
-__device__ __forceinline__ void xel_store(unsigned long long* p, float v, uint32_t flag) {
-  const unsigned long long w = ((unsigned long long)flag << 32) | (unsigned long long)__float_as_uint(v);
-  asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(w) : "memory");
-}
-
-// Two consecutive exchange elements (16-byte aligned) from L2.
-__device__ __forceinline__ void xel_load2(const unsigned long long* p, unsigned long long& a, unsigned long long& b) {
-  asm volatile("ld.relaxed.gpu.global.v2.b64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p));
-}
-
-__device__ __forceinline__ float xel_value(unsigned long long w) { return __uint_as_float((uint32_t)w); }
-__device__ __forceinline__ uint32_t xel_flag(unsigned long long w) { return (uint32_t)(w >> 32); }
 
 // ------------------------------------------------------------ arithmetic
 // e^d for d <= 0 in float32, the softmax exponential of the sampling path,

@@ -185,25 +185,6 @@ static __device__ __noinline__ int warp_process_row(const float* __restrict__ lo
   return warp_process_staged(keys, V, k, T, hist, ebuf, out_idx, out_prob);
 }
 
-// Builds the support list of a dense probability row (entries > 0) in index
-// order with one warp.  Returns the length.
-static __device__ __noinline__ int warp_compact_probs(const float* __restrict__ row, int V, int* out_idx,
-                                               float* out_prob) {
-  const int lane = threadIdx.x & 31;
-  const unsigned lt = (1u << lane) - 1u;
-  int base = 0;
-  for (int j0 = 0; j0 < V; j0 += 32) {
-    const int i = j0 + lane;
-    const float v = (i < V) ? row[i] : 0.0f;
-    const bool sel = v > 0.0f;
-    const uint32_t b = __ballot_sync(0xffffffffu, sel);
-    if (sel) { out_idx[base + __popc(b & lt)] = i; out_prob[base + __popc(b & lt)] = v; }
-    base += __popc(b);
-  }
-  __syncwarp();
-  return base;
-}
-
 // ---- single-thread helpers (sequential float32 semantics) ----
 template <typename LD = LdPlain>
 __device__ __forceinline__ int list_sample(const int* idx, const float* prob, int n, float u) {
