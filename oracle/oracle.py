@@ -62,11 +62,6 @@ class OrcStats(C.Structure):
         return d
 
 
-class OrcRoundRec(C.Structure):
-    _fields_ = [(n, C.c_int32) for n in ("frame", "stream", "s", "n_d", "m", "n_acc", "s_new", "pad")] + [
-        ("drafts", C.c_int32 * 8), ("min_margin", C.c_double)]
-
-
 ROUND_DTYPE = np.dtype([("frame", "<i4"), ("stream", "<i4"), ("s", "<i4"), ("n_d", "<i4"), ("m", "<i4"),
                         ("n_acc", "<i4"), ("s_new", "<i4"), ("pad", "<i4"), ("drafts", "<i4", (8,)),
                         ("min_margin", "<f8")])

@@ -164,18 +164,6 @@ def gen_draft_offsets(spec: ModelSpec, K: int, seed: int = 0, std: float = 0.25)
     return _normal(seed, _T_OFFSET, (K, spec.hidden), std)
 
 
-def weights_as_f64(spec: ModelSpec, w: dict) -> dict:
-    """Exact float64 copies of the stored weights (bf16 and fp32 are exact in f64)."""
-    def cv(a):
-        if a.dtype == np.uint16:
-            return bf16_bits_to_f32(a).astype(np.float64)
-        return a.astype(np.float64)
-
-    out = {k: cv(w[k]) for k in ("embed", "lm_head", "final_norm")}
-    out["layers"] = [{k: cv(v) for k, v in lw.items()} for lw in w["layers"]]
-    return out
-
-
 def gen_frames(spec: ModelSpec, n_streams: int, n_frames: int, seed: int = 1,
                first_frame: int = 0):
     """Per-frame talker hidden x ~ N(0,1) [F, B, H] float32 and seed code c0 ~ U[0, V) [F, B] int32.
