@@ -39,6 +39,15 @@ def test_static_rejects_scratch_above_maximum():
     assert b"static maximum" in lib.cp_spec_last_error(None)
     # one stream of the same model fits
     assert lib.cp_spec_workspace_bytes(C.byref(m), C.byref(b.Config(4, 50, 0.9, 1, 1))) <= (8 << 20)
+    # the boundary: 9 streams fit, 10 do not (the size is checked before any device work, so
+    # zero frames return at once)
+    nine, ten = b.Config(4, 50, 0.9, 1, 9), b.Config(4, 50, 0.9, 1, 10)
+    assert (lib.cp_spec_workspace_bytes(C.byref(m), C.byref(nine)) <= (8 << 20)
+            < lib.cp_spec_workspace_bytes(C.byref(m), C.byref(ten)))
+    assert lib.cp_spec_decode_frames_static(C.byref(m), C.byref(w), C.byref(nine), 9, 0, 0, 16, 16, 16, None,
+                                            None) == b.OK
+    assert lib.cp_spec_decode_frames_static(C.byref(m), C.byref(w), C.byref(ten), 10, 0, 0, 16, 16, 16, None,
+                                            None) == b.E_WORKSPACE
 
 
 def _gpu():
